@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one decode step of one attention layer over a batch of sequences
+whose K/V already sit in the paged pool: the new token of every sequence is
+written through its slot mapping (kv_append), then paged decode attention
+reads every sequence's blocks through its block table (split-KV partitions
+plus the log-sum-exp merge when the plan has more than one split).
+
+Default workload: Llama-3-8B-shaped paged decode (64 sequences, context
+lengths uniform in [512, 4096], 32 query / 8 kv heads, head_dim 128, bf16,
+16-token blocks shuffled across a pool 1.2x the blocks needed).
+
+Metric: KV bytes read by decode attention per second (valid tokens only:
+sum_b L_b * 2 * Hkv * D * 2 bytes) -- "value" -- plus decode tokens/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       [--splits S] [--impl reference]
+Under torchrun each rank runs an independent replica (weak scaling).
+Prints exactly one JSON line on stdout (rank 0).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn KV-read GB/s (fraction of HBM peak); decode tokens/s"
+L2_BYTES = 129 * 1000 ** 2
+FALLBACK_HBM_GBS = 6800.0
+
+DESCR = {
+    "llama3_8b_decode": "Llama-3-8B-shaped paged decode: 64 seqs, ctx U[512,4096], 32q/8kv heads, "
+                        "head_dim 128, bf16, 16-token blocks shuffled in a 1.2x pool",
+    "yi6b_long_decode": "Yi-6B-shaped long-context paged decode: 8 seqs, ctx log-U[32768,196608], "
+                        "32q/4kv heads, head_dim 128, bf16, split-KV + LSE merge",
+    "yi6b_long_decode_contig": "Yi-6B-shaped long-context decode on the contiguous "
+                               "(cuMemMap-backed) KV path, same inputs as yi6b_long_decode",
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                and parts[1] == workload and parts[2] == src_hash:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# Workload set-up (shared by both arms: host arrays only)
+# --------------------------------------------------------------------------
+def decode_workload(name):
+    base = name.replace("_contig", "")
+    cfg = W.CONFIGS[base]
+    lens = W.decode_lengths(base)
+    need = int(sum((int(L) + 15) // 16 for L in lens))  # blocks the contexts occupy
+    nb = int(math.ceil(cfg["pool_factor"] * need))
+    t0 = time.time()
+    inp = W.decode_inputs(base, nb)
+    log(f"[bench] generated {name} inputs in {time.time() - t0:.1f}s "
+        f"({nb} blocks, {int(lens.sum())} tokens)")
+    max_blocks = (cfg["len_hi"] + 15) // 16
+    return cfg, inp, nb, max_blocks
+
+
+# --------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import paged_kv_cache_196_gb300 as pk
+
+    torch.cuda.set_device(local_rank)
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    contig = args.workload.endswith("_contig")
+    cfg, inp, nb, max_blocks = decode_workload(args.workload)
+    lens = inp["lens"]
+    B, hq, hkv, d = len(lens), cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    e = 2
+    kv_bytes = int(lens.sum()) * 2 * hkv * d * e
+    scale = 1.0 / math.sqrt(d)
+
+    # ---- host block manager: the allocation of every context's blocks
+    alloc = pk.kv_allocator_create(nb)
+    pk.kv_allocator_set_order(alloc, inp["perm"])
+    tables = np.full((B, max_blocks), -1, np.int32)
+    for b, L in enumerate(lens):
+        pk.kv_prepare_append(alloc, tables[b], 0, 0, int(L), np.zeros(int(L), np.int64),
+                             np.zeros(0, np.int32), np.zeros(0, np.int32))
+    pk.kv_allocator_destroy(alloc)
+    last = lens.astype(np.int64) - 1  # the new token of sequence b is its last position
+
+    # ---- device state: the cache (paged pool or per-request virtual ranges)
+    if not contig:
+        pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+        kp, vp = pk.kv_pool_ptrs(pool)
+        _fill(kp, torch.from_numpy(inp["pool_k"].view(np.int16)))
+        _fill(vp, torch.from_numpy(inp["pool_v"].view(np.int16)))
+        d_tables = torch.from_numpy(tables).cuda()
+        slots = tables[np.arange(B), last // 16].astype(np.int64) * 16 + last % 16
+    else:
+        ctx = pk.kv_contig_create(B, cfg["len_hi"], hkv, d, pk.KV_BF16)
+        t0 = time.time()
+        for b, L in enumerate(lens):
+            pk.kv_contig_reserve(ctx, b)
+            pk.kv_contig_ensure(ctx, b, int(L))
+        map_s = time.time() - t0
+        head_stride, page, _ = pk.kv_contig_layout(ctx)
+        # sequence b's logical K/V (its blocks of the shuffled pool, in table
+        # order) written through the library's contiguous append
+        for b, L in enumerate(lens):
+            j = np.arange(int(L))
+            blk = tables[b, j // 16]
+            rk = torch.from_numpy(np.ascontiguousarray(inp["pool_k"][blk, :, j % 16]).view(np.int16)).cuda()
+            rv = torch.from_numpy(np.ascontiguousarray(inp["pool_v"][blk, :, j % 16]).view(np.int16)).cuda()
+            pk.kv_contig_append(ctx, rk, rv,
+                                torch.full((int(L),), b, dtype=torch.int32, device="cuda"),
+                                torch.arange(int(L), dtype=torch.int32, device="cuda"), int(L))
+            torch.cuda.synchronize()
+            del rk, rv
+        req_ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    d_lens = torch.from_numpy(lens).cuda()
+    q = torch.from_numpy(inp["q"].view(np.int16)).cuda()
+    g = W.rng(cfg["seed"] + 1000 + rank)
+    k_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
+    v_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
+    out = torch.empty((B, hq, d), dtype=torch.int16, device="cuda")
+    splits = args.splits
+    ws_bytes = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, splits)
+    ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
+    part_blocks, max_splits = pk.kv_decode_split_plan(B, hkv, max_blocks, splits)
+    if not contig:
+        d_slots = torch.from_numpy(slots).cuda()
+    else:
+        d_pos = torch.from_numpy(last.astype(np.int32)).cuda()
+
+    def append():
+        if contig:
+            pk.kv_contig_append(ctx, k_new, v_new, req_ids, d_pos, B)
+        else:
+            pk.kv_append(pool, k_new, v_new, d_slots, B)
+
+    def attend():
+        if contig:
+            pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, pk.KV_BF16,
+                                       None, splits, ws, ws_bytes)
+        else:
+            pk.paged_decode_attention(pool, q, d_tables, max_blocks, d_lens, B, hq, scale, out,
+                                      pk.KV_BF16, None, splits, ws, ws_bytes)
+
+    launches_per_step = 2 + (1 if max_splits > 1 else 0)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        append()
+        attend()
+    torch.cuda.synchronize()
+    err = pk.kv_contig_get_device_error(ctx) if contig else pk.kv_get_device_error(pool)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after warm-up")
+
+    # ---- timed region (device time, inputs resident in HBM)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        append()
+        ev[i][0].record()
+        attend()
+        ev[i][1].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * kv_bytes * K / (total_ms * 1e-3) / 1e9
+    tokens_per_s = world * B * K / (total_ms * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    Ke = min(K, 2000)
+    h_q = torch.from_numpy(inp["q"].view(np.int16)).pin_memory()
+    h_k = k_new.cpu().pin_memory()
+    h_v = v_new.cpu().pin_memory()
+    h_out = torch.empty((B, hq, d), dtype=torch.int16).pin_memory()
+    if contig:
+        h_idx = torch.from_numpy(last.astype(np.int32)).pin_memory()
+        d_idx = d_pos
+    else:
+        h_idx = torch.from_numpy(slots).pin_memory()
+        d_idx = d_slots
+    h_lens = torch.from_numpy(lens).pin_memory()
+    h2d = h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_idx.numel() * h_idx.element_size() \
+        + h_lens.numel() * 4
+    d2h = h_out.numel() * 2
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        append()
+        attend()
+        h_out.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * kv_bytes * Ke / (e2e_ms * 1e-3) / 1e9
+
+    err = pk.kv_contig_get_device_error(ctx) if contig else pk.kv_get_device_error(pool)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    peak, peak_kind = read_peaks()
+    achieved = kv_bytes / (attend_ms * 1e-3) / 1e9
+    src = source_hash("paged_kv_cache_196_gb300/csrc/decode.cu",
+                      "paged_kv_cache_196_gb300/csrc/common.cuh")
+    traffic = recorded_traffic("decode_kernel", args.workload, src)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": DESCR[args.workload],
+            "name": args.workload,
+            "batch": B,
+            "tokens": int(lens.sum()),
+            "kv_bytes_per_step": kv_bytes,
+            "num_splits": splits,
+            "part_blocks": part_blocks,
+            "max_splits": max_splits,
+            "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB L2); no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "decode_tokens_per_s": round(tokens_per_s, 1),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": ("contig_decode_attention" if contig else "paged_decode_attention")
+                      + " (decode kernel" + (" + split merge kernel)" if max_splits > 1 else ")"),
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": kv_bytes,
+            "avg_launch_ms": round(attend_ms, 5),
+        },
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / Ke, 5),
+                "steps": Ke},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if contig:
+        line["config"]["vmm"] = {"page_bytes": page, "map_seconds": round(map_s, 4),
+                                 "head_stride_tokens": head_stride}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, nb, max_blocks)
+    if dist:
+        tdist.barrier()
+    return line
+
+
+def _fill(ptr, src):
+    """Copies a host tensor into library-owned device memory (set-up only)."""
+    import torch
+
+    class _Raw:
+        pass
+
+    raw = _Raw()
+    raw.__cuda_array_interface__ = {"shape": tuple(src.shape), "typestr": "<i2",
+                                    "data": (ptr, False), "version": 3}
+    torch.as_tensor(raw, device="cuda").copy_(src.cuda())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timings (baseline leg and reference arm)
+# --------------------------------------------------------------------------
+def _oracle_tables(inp, max_blocks):
+    import oracle
+
+    return oracle.build_block_tables(inp["lens"], 16, inp["perm"], max_blocks)
+
+
+def cpu_baseline(cfg, inp, nb, max_blocks, budget_s=12.0):
+    """The oracle, as it stands, on a bounded sample: the first S sequences
+    (all query heads), S grown until about budget_s of CPU work."""
+    import oracle
+
+    tables = _oracle_tables(inp, max_blocks)
+    hkv, d, hq = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_q_heads"]
+    lens = inp["lens"]
+    B = len(lens)
+    done, spent, nbytes, S = 0, 0.0, 0, 1
+    while done < B and spent < budget_s:
+        S = min(S, B - done)
+        items = [(b, h) for b in range(done, done + S) for h in range(hq)]
+        t0 = time.time()
+        oracle.paged_decode(inp["pool_k"], inp["pool_v"], tables, lens, inp["q"],
+                            1 / math.sqrt(d), items=items)
+        spent += time.time() - t0
+        nbytes += int(lens[done:done + S].sum()) * 2 * hkv * d * 2
+        done += S
+        S *= 2
+    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {done} of {B} sequences, all {hq} query heads, fp64 "
+                      f"reassemble-then-softmax ({spent:.1f}s)"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one (sequence, query
+    head) of the workload, cycling through the batch."""
+    import oracle
+
+    cfg, inp, nb, max_blocks = decode_workload(args.workload)
+    tables = _oracle_tables(inp, max_blocks)
+    lens = inp["lens"]
+    B, hq, hkv, d = len(lens), cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+
+    def step(i):
+        b, h = (i // hq) % B, i % hq
+        oracle.paged_decode(inp["pool_k"], inp["pool_v"], tables, lens, inp["q"],
+                            1 / math.sqrt(d), items=[(b, h)])
+        return int(lens[b]) * 2 * d * 2  # this head's K and V bytes
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.time()
+    nbytes = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.time() - t0
+    value = nbytes / dt / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "name": args.workload, "batch": B},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one (sequence, query head) per step, cycling the batch; "
+                                   "a single item runs on one core"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="llama3_8b_decode", choices=sorted(DESCR))
+    ap.add_argument("--splits", type=int, default=0, help="0 = the library's automatic plan")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return  # the reference arm runs on rank 0 only
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,304 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 (sm_103a) paged KV-cache library.
+ *
+ * The cache holds the keys and values of past tokens; each new token's
+ * attention reads them again ("PagedAttention Nedir?", section "Once KV
+ * Cache'i Anlamak Gerekir").  It is cut into fixed-size blocks of
+ * block_size (= 16) tokens that may sit anywhere in a physical pool; a
+ * per-sequence block table maps logical block i to a physical block id
+ * ("Makale Bulteni -- PagedAttention ve vLLM", section "Iddia ve Gerceklik";
+ * "PagedAttention Nedir?", section "PagedAttention Nasil Calisir?").  The
+ * vAttention variant keeps each request's KV contiguous in virtual memory and
+ * backs it with physical pages on demand ("Makale Bulteni -- vAttention",
+ * section "Iddia ve Gerceklik: vAttention").
+ *
+ * Conventions for every call:
+ *   - Returns a kv_status; never throws, never aborts the process.
+ *   - Pointers documented "device" are CUDA device pointers (or managed /
+ *     mapped memory) that stay valid until the work on `stream` completes;
+ *     "host" pointers are read or written before the call returns.
+ *   - Kernels run asynchronously on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).
+ *   - Argument errors detected on the host return KV_ERR_ARG or
+ *     KV_ERR_UNSUPPORTED and launch nothing.  Errors the GPU detects
+ *     (a block id or slot outside the pool, a position outside the mapped
+ *     range, a pipeline wait that timed out) skip the offending element, let
+ *     the kernel finish, and set bits in a device error word that
+ *     kv_get_device_error / kv_contig_get_device_error read and clear.
+ *   - Element types: KV_F32 (IEEE fp32) or KV_BF16 (bfloat16).  q, k_new and
+ *     v_new use the pool's type; out may be KV_F32 or the pool's type.
+ *   - head_dim must be 64 or 128, block_size must be 16, num_q_heads must be
+ *     a multiple of num_kv_heads with num_q_heads / num_kv_heads <= 8.
+ *
+ * Pool layout (paged path): separate K and V arrays, each
+ *     [num_blocks][num_kv_heads][block_size][head_dim]
+ * so one (block, kv head) tile of 16 tokens is contiguous (4 KiB for bf16,
+ * head_dim 128).  Slot s of the pool is block s / 16, offset s % 16.
+ * Grouped-query attention: query head hq reads kv head hq / (Hq / Hkv).
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_ARG = -1,            /* invalid argument (null pointer, bad size, bad id) */
+    KV_ERR_OOM = -2,            /* no free block / device or physical memory exhausted */
+    KV_ERR_UNSUPPORTED = -3,    /* shape or type outside what the kernels implement */
+    KV_ERR_CUDA = -4,           /* a CUDA runtime or driver call failed */
+    KV_ERR_DEVICE_BOUNDS = -5,  /* the GPU met an out-of-range block id, slot or position */
+    KV_ERR_TIMEOUT = -6,        /* a bounded pipeline wait inside a kernel ran out */
+    KV_ERR_STATE = -7           /* call not valid in the object's current state */
+} kv_status;
+
+typedef enum { KV_F32 = 0, KV_BF16 = 1 } kv_dtype;
+
+/* Bits of the device error word. */
+#define KV_DEVERR_BLOCK_RANGE 0x1   /* block-table entry outside [0, num_blocks) */
+#define KV_DEVERR_SLOT_RANGE 0x2    /* slot_mapping entry >= num_blocks * block_size */
+#define KV_DEVERR_TIMEOUT 0x4       /* an mbarrier wait exceeded its time limit */
+#define KV_DEVERR_UNMAPPED 0x8      /* contiguous path: position beyond the mapped range */
+
+const char *kv_status_string(kv_status s);
+
+/* Number of blocks a sequence of n_tokens needs and the slots left unused in
+ * its last block ("PagedAttention Nedir?", "Nasil Calisir?": 35 tokens at 16
+ * per block need 3 blocks and leave 13 slots unused).  Host only. */
+kv_status kv_blocks_for_tokens(int64_t n_tokens, int block_size, int64_t *blocks,
+                               int64_t *unused_slots);
+
+/* ======================================================================
+ * Host block allocator: free list + reference counts.
+ * "Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve Gerceklik": when a
+ * sequence's current block is full a free block is taken from the pool;
+ * forked / branched sequences share blocks by pointer, copy-on-write.
+ * "PagedAttention Nedir?", step 5: blocks no longer needed are reused.
+ * Pure host code: usable without a GPU.  Not thread-safe.
+ * ==================================================================== */
+typedef struct kv_allocator *kv_allocator_t;
+
+/* Creates an allocator over block ids 0..num_blocks-1, all free, handed out
+ * in increasing id order.  *out owns host memory; free with
+ * kv_allocator_destroy. */
+kv_status kv_allocator_create(int num_blocks, kv_allocator_t *out);
+kv_status kv_allocator_destroy(kv_allocator_t a);
+
+/* Sets the order in which free blocks are handed out (a permutation of
+ * 0..num_blocks-1, host array of n = num_blocks ids).  Only valid while every
+ * block is free (KV_ERR_STATE otherwise). */
+kv_status kv_allocator_set_order(kv_allocator_t a, const int32_t *order, int n);
+
+/* Takes n free blocks (refcount becomes 1) into ids_out (host, n entries).
+ * KV_ERR_OOM and no change if fewer than n are free. */
+kv_status kv_allocator_alloc(kv_allocator_t a, int n, int32_t *ids_out);
+
+/* refcount += 1 for each listed block (sharing a prefix, forking a
+ * sequence).  Each id must be allocated (KV_ERR_ARG otherwise, no change). */
+kv_status kv_allocator_share(kv_allocator_t a, int n, const int32_t *ids);
+
+/* refcount -= 1 for each listed block; a block whose count reaches zero goes
+ * back to the free list.  Freeing a free block is KV_ERR_ARG (no change). */
+kv_status kv_allocator_free(kv_allocator_t a, int n, const int32_t *ids);
+
+kv_status kv_allocator_refcount(kv_allocator_t a, int32_t id, int *refcount);
+kv_status kv_allocator_num_free(kv_allocator_t a, int *num_free);
+
+/* Host step of appending n_new tokens to one sequence (the block manager's
+ * part of a decode or prefill step).
+ *   table_row    host int32[max_blocks]: the sequence's block table row, updated
+ *                in place;
+ *   *num_blocks  blocks currently in the row (in/out);
+ *   cur_len      tokens currently stored (positions 0..cur_len-1);
+ *   slots_out    host int64[n_new]: pool slot of positions cur_len..cur_len+n_new-1;
+ *   cow_src/cow_dst host int32[*n_cow] capacity; on return *n_cow pairs.
+ * A new block is taken whenever a position opens one.  If a position falls in
+ * an existing block whose refcount is > 1, that block is copied on write:
+ * a fresh block is taken, the pair (old, new) is reported in cow_src/cow_dst,
+ * the old block's refcount drops by one and the row points at the new block.
+ * The caller must run kv_copy_blocks on the reported pairs before writing
+ * the new tokens.  On KV_ERR_OOM (not enough free blocks) or KV_ERR_ARG
+ * (row or cow capacity too small) nothing is changed. */
+kv_status kv_prepare_append(kv_allocator_t a, int block_size, int32_t *table_row,
+                            int max_blocks, int *num_blocks, int64_t cur_len, int n_new,
+                            int64_t *slots_out, int32_t *cow_src, int32_t *cow_dst,
+                            int *n_cow);
+
+/* ======================================================================
+ * Device pool.
+ * ==================================================================== */
+typedef struct kv_pool *kv_pool_t;
+
+/* Allocates the K and V pools (num_blocks * num_kv_heads * block_size *
+ * head_dim elements each) on the current device, a device error word, and a
+ * host allocator over the blocks.  Pool memory is uninitialised. */
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         kv_dtype dtype, kv_pool_t *out);
+kv_status kv_pool_destroy(kv_pool_t p);
+
+/* Device addresses of the K and V pools (owned by the pool). */
+kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool);
+
+/* The pool's allocator (borrowed; destroyed with the pool). */
+kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out);
+
+/* KV append: writes the new tokens' keys and values into their pool slots
+ * ("Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve Gerceklik";
+ * "PagedAttention Nedir?", "Nasil Calisir?" steps 1-3).
+ *   k_new, v_new   device [num_tokens][num_kv_heads][head_dim], pool dtype;
+ *   slot_mapping   device int64[num_tokens]; a negative slot is skipped; a
+ *                  slot >= num_blocks*block_size is skipped and sets
+ *                  KV_DEVERR_SLOT_RANGE.
+ * Exact byte copy.  Two tokens naming the same slot: unspecified winner. */
+kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
+                    const int64_t *slot_mapping, int num_tokens, void *stream);
+
+/* Copy-on-write block copies: for i < n, every head and slot of K and V of
+ * block src[i] is copied to block dst[i] (device int32 arrays).  Pairs must
+ * not overlap (no dst is another pair's src).  Out-of-range ids are skipped
+ * and set KV_DEVERR_BLOCK_RANGE. */
+kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, int n,
+                         void *stream);
+
+/* Scratch memory the decode call needs for a split plan: partial outputs
+ * fp32 [batch][num_q_heads][splits][head_dim] and their log-sum-exp
+ * [batch][num_q_heads][splits].  num_splits as in paged_decode_attention
+ * (0 = automatic).  Host only. */
+kv_status kv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int max_blocks, int num_splits, size_t *bytes);
+
+/* The split plan paged_decode_attention / contig_decode_attention will use:
+ * each sequence's tokens are cut into partitions of *part_blocks blocks
+ * (16 tokens each), at most *max_splits per sequence.  Host only. */
+kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits,
+                               int *part_blocks, int *max_splits);
+
+/* Paged decode attention: one query token per sequence attends all
+ * seq_lens[b] tokens of its cache, reading K/V blocks through the block
+ * table ("PagedAttention Nedir?", "Nasil Calisir?" step 4), with
+ *     o = softmax(scale * q K^T) V,   lse = log sum_j exp(scale * q.k_j).
+ *   q             device [batch][num_q_heads][head_dim], pool dtype;
+ *   block_tables  device int32[batch][max_blocks]; entries at index >=
+ *                 ceil(seq_lens[b]/16) are never read;
+ *   seq_lens      device int32[batch], 0 <= seq_lens[b] <= max_blocks*16;
+ *   out           device [batch][num_q_heads][head_dim] of out_dtype;
+ *   lse_out       device fp32[batch][num_q_heads] or NULL;
+ *   num_splits    0 = automatic; else the number of partitions the longest
+ *                 possible sequence (max_blocks blocks) is cut into;
+ *   workspace     device scratch of at least kv_decode_workspace_size bytes
+ *                 (may be NULL when that size is 0).
+ * An empty sequence gives out = 0 and lse = -inf.  The result does not depend
+ * on where the blocks sit in the pool (bit-identical for any placement). */
+kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *block_tables,
+                                 int max_blocks, const int32_t *seq_lens, int batch,
+                                 int num_q_heads, float scale, void *out, kv_dtype out_dtype,
+                                 float *lse_out, int num_splits, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* Chunked causal paged prefill ("Makale Bulteni -- vAttention", "Iddia ve
+ * Gerceklik": the prefill kernels are where paging costs most).  Sequence b
+ * holds seq_lens[b] tokens in the cache, the last T_b = cu_q[b+1] - cu_q[b]
+ * of which are the new chunk (already appended with kv_append).  Query row
+ * r = cu_q[b] + i sits at position (seq_lens[b] - T_b) + i and attends keys
+ * 0..(seq_lens[b] - T_b) + i.  QK^T and PV run on the tcgen05 tensor cores
+ * with fp32 accumulation in tensor memory.  Requires dtype KV_BF16 and
+ * head_dim 128.
+ *   q        device [cu_q[batch]][num_q_heads][head_dim];
+ *   cu_q     device int32[batch + 1], cu_q[0] = 0, non-decreasing;
+ *   max_q_len host: max_b T_b (sizes the grid);
+ *   out      device [cu_q[batch]][num_q_heads][head_dim] of out_dtype;
+ *   lse_out  device fp32[cu_q[batch]][num_q_heads] or NULL. */
+kv_status paged_prefill_attention(kv_pool_t p, const void *q, const int32_t *cu_q,
+                                  int max_q_len, const int32_t *block_tables, int max_blocks,
+                                  const int32_t *seq_lens, int batch, int num_q_heads,
+                                  float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                  void *stream);
+
+/* Synchronises `stream`, returns the device error word in *code (0 = none)
+ * and clears it.  Returns KV_ERR_DEVICE_BOUNDS or KV_ERR_TIMEOUT when bits are
+ * set, KV_OK otherwise. */
+kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream);
+
+/* ======================================================================
+ * Contiguous (vAttention-style) KV path.  "Makale Bulteni -- vAttention",
+ * "Iddia ve Gerceklik: vAttention": for each request a contiguous virtual
+ * range large enough for the maximum context is reserved
+ * (cuMemAddressRangeReserve) without using physical memory; physical pages
+ * are created and mapped (cuMemCreate, cuMemMap) only as the request grows,
+ * so the attention kernel sees one contiguous tensor per request.
+ *
+ * Per-request layout: K region [num_kv_heads][head_stride][head_dim] followed
+ * by the V region of the same shape, where head_stride >= max_tokens is
+ * max_tokens rounded up to whole physical pages (kv_contig_layout).
+ * Physical pages are the driver's minimum granularity (2 MiB on current
+ * GPUs); each mapped page of every head's K and V region is its own physical
+ * allocation.
+ * ==================================================================== */
+typedef struct kv_contig *kv_contig_t;
+
+/* Creates a context for up to max_requests requests of up to max_tokens
+ * tokens on the current device.  Reserves nothing yet. */
+kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, int head_dim,
+                           kv_dtype dtype, kv_contig_t *out);
+/* Unmaps, releases and frees everything the context holds. */
+kv_status kv_contig_destroy(kv_contig_t c);
+
+/* Layout facts: tokens per head region (head_stride), bytes of one physical
+ * page, bytes of virtual range reserved per request. */
+kv_status kv_contig_layout(kv_contig_t c, int64_t *head_stride, int64_t *page_bytes,
+                           int64_t *reserved_bytes_per_request);
+
+/* Reserves request req's virtual range (cuMemAddressRangeReserve).  No
+ * physical memory is used.  KV_ERR_STATE if already reserved. */
+kv_status kv_contig_reserve(kv_contig_t c, int req);
+
+/* Makes positions 0..n_tokens-1 of every head of request req backed by
+ * physical pages (cuMemCreate + cuMemMap + cuMemSetAccess for pages not yet
+ * mapped).  Synchronous host call.  KV_ERR_OOM if physical memory runs out
+ * (pages mapped by this call are undone). */
+kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens);
+
+/* Unmaps and releases all physical pages of request req and frees its
+ * virtual range.  The caller must have finished all work that uses it. */
+kv_status kv_contig_release(kv_contig_t c, int req);
+
+/* Device base addresses of request req's K and V regions. */
+kv_status kv_contig_ptrs(kv_contig_t c, int req, void **k_base, void **v_base);
+
+/* Mapped tokens of request req and physical bytes mapped over all requests. */
+kv_status kv_contig_stats(kv_contig_t c, int req, int64_t *mapped_tokens,
+                          int64_t *mapped_bytes_total);
+
+/* Append on the contiguous path: token t's K/V go to position positions[t]
+ * of request req_ids[t] (device int32 arrays).  A position at or beyond the
+ * request's mapped range, or an unreserved request, is skipped and sets
+ * KV_DEVERR_UNMAPPED. */
+kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
+                           const int32_t *req_ids, const int32_t *positions, int num_tokens,
+                           void *stream);
+
+/* Decode attention over the contiguous layout: sequence b is request
+ * req_ids[b] (device int32[batch]) with seq_lens[b] tokens.  Same maths and
+ * arguments as paged_decode_attention; max_tokens plays the role of
+ * max_blocks*16 in the split plan, so with the same num_splits and a table
+ * width of ceil(max_tokens/16) both paths cut the keys identically and give
+ * bit-identical results.  seq_lens[b] beyond the mapped range sets
+ * KV_DEVERR_UNMAPPED and is clamped. */
+kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *req_ids,
+                                  const int32_t *seq_lens, int batch, int num_q_heads,
+                                  float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                  int num_splits, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H */

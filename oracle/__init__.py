@@ -140,8 +140,11 @@ def paged_decode(pool_k, pool_v, tables, lens, q, scale, items=None):
 
 
 def linear_decode(k_bases, v_bases, req_ids, lens, q, scale, items=None):
-    """Decode over per-request linear buffers [Hkv][max_ctx][D] (one array per request)."""
+    """Decode over per-request linear buffers [Hkv][max_ctx][D] (one array per
+    request, all of the same shape)."""
     hkv, max_ctx, d = k_bases[0].shape
+    if any(a.shape != k_bases[0].shape for a in list(k_bases) + list(v_bases)):
+        raise ValueError("all request buffers must share one [Hkv][max_ctx][D] shape")
     B, hq, _ = q.shape
     kb = (ctypes.c_void_p * len(k_bases))(*[a.ctypes.data for a in k_bases])
     vb = (ctypes.c_void_p * len(v_bases))(*[a.ctypes.data for a in v_bases])

@@ -1,0 +1,343 @@
+"""Python binding of libpagedkv.so (the GB300 paged KV-cache library).
+
+Argument marshalling only: every function below has the name of a C entry
+point declared in ``include/paged_kv.h`` and forwards to it through ctypes.
+Tensors are passed as raw device (or host) pointers; streams default to the
+current PyTorch stream.  All compute runs in the library's CUDA kernels; there
+is no fallback path -- if the library cannot be built or loaded, importing the
+binding's functions raises.
+
+Non-zero statuses raise ``KVError``.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_blocks_for_tokens",
+    "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
+    "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
+    "kv_allocator_num_free", "kv_prepare_append", "kv_pool_create", "kv_pool_destroy",
+    "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks",
+    "kv_decode_workspace_size", "kv_decode_split_plan", "paged_decode_attention",
+    "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
+    "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
+    "kv_contig_ptrs", "kv_contig_stats", "kv_contig_append", "contig_decode_attention",
+    "kv_contig_get_device_error",
+]
+
+KV_F32 = 0
+KV_BF16 = 1
+
+STATUS = {0: "KV_OK", -1: "KV_ERR_ARG", -2: "KV_ERR_OOM", -3: "KV_ERR_UNSUPPORTED",
+          -4: "KV_ERR_CUDA", -5: "KV_ERR_DEVICE_BOUNDS", -6: "KV_ERR_TIMEOUT", -7: "KV_ERR_STATE"}
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({kv_status_string(status)})")
+
+
+_lib = None
+_i32, _i64, _f32, _vp, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+_P = ctypes.POINTER
+
+# name -> argtypes (every function returns kv_status unless listed in _RESTYPE)
+_SIGS = {
+    "kv_status_string": [_i32],
+    "kv_blocks_for_tokens": [_i64, _i32, _P(_i64), _P(_i64)],
+    "kv_allocator_create": [_i32, _P(_vp)],
+    "kv_allocator_destroy": [_vp],
+    "kv_allocator_set_order": [_vp, _vp, _i32],
+    "kv_allocator_alloc": [_vp, _i32, _vp],
+    "kv_allocator_share": [_vp, _i32, _vp],
+    "kv_allocator_free": [_vp, _i32, _vp],
+    "kv_allocator_refcount": [_vp, ctypes.c_int32, _P(_i32)],
+    "kv_allocator_num_free": [_vp, _P(_i32)],
+    "kv_prepare_append": [_vp, _i32, _vp, _i32, _P(_i32), _i64, _i32, _vp, _vp, _vp, _P(_i32)],
+    "kv_pool_create": [_i32, _i32, _i32, _i32, _i32, _P(_vp)],
+    "kv_pool_destroy": [_vp],
+    "kv_pool_ptrs": [_vp, _P(_vp), _P(_vp)],
+    "kv_pool_allocator": [_vp, _P(_vp)],
+    "kv_append": [_vp, _vp, _vp, _vp, _i32, _vp],
+    "kv_copy_blocks": [_vp, _vp, _vp, _i32, _vp],
+    "kv_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
+    "kv_decode_split_plan": [_i32, _i32, _i32, _i32, _P(_i32), _P(_i32)],
+    "paged_decode_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32,
+                               _vp, _sz, _vp],
+    "paged_prefill_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
+                                _vp, _vp],
+    "kv_get_device_error": [_vp, _P(_i32), _vp],
+    "kv_contig_create": [_i32, _i32, _i32, _i32, _i32, _P(_vp)],
+    "kv_contig_destroy": [_vp],
+    "kv_contig_layout": [_vp, _P(_i64), _P(_i64), _P(_i64)],
+    "kv_contig_reserve": [_vp, _i32],
+    "kv_contig_ensure": [_vp, _i32, _i64],
+    "kv_contig_release": [_vp, _i32],
+    "kv_contig_ptrs": [_vp, _i32, _P(_vp), _P(_vp)],
+    "kv_contig_stats": [_vp, _i32, _P(_i64), _P(_i64)],
+    "kv_contig_append": [_vp, _vp, _vp, _vp, _vp, _i32, _vp],
+    "contig_decode_attention": [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32, _vp,
+                                _sz, _vp],
+    "kv_contig_get_device_error": [_vp, _P(_i32), _vp],
+}
+_RESTYPE = {"kv_status_string": ctypes.c_char_p}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib(build: bool = True):
+    """The loaded library (built first if missing or stale and ``build``)."""
+    global _lib
+    if _lib is None:
+        path = _build.build() if build else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpagedkv.so not found at {path}; run paged_kv_cache_196_gb300/build.py")
+        L = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _RESTYPE.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    """Raw address of a tensor / numpy array / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise KVError(st, where)
+
+
+def kv_status_string(status: int) -> str:
+    return lib().kv_status_string(status).decode()
+
+
+def kv_blocks_for_tokens(n_tokens: int, block_size: int = 16):
+    b, u = _i64(), _i64()
+    _check(lib().kv_blocks_for_tokens(n_tokens, block_size, ctypes.byref(b), ctypes.byref(u)),
+           "kv_blocks_for_tokens")
+    return b.value, u.value
+
+
+# ---------------------------------------------------------------- allocator
+def kv_allocator_create(num_blocks: int) -> int:
+    h = _vp()
+    _check(lib().kv_allocator_create(num_blocks, ctypes.byref(h)), "kv_allocator_create")
+    return h.value
+
+
+def kv_allocator_destroy(a: int):
+    _check(lib().kv_allocator_destroy(a), "kv_allocator_destroy")
+
+
+def kv_allocator_set_order(a: int, order):
+    """order: int32 numpy array (host)."""
+    _check(lib().kv_allocator_set_order(a, _ptr(order), len(order)), "kv_allocator_set_order")
+
+
+def kv_allocator_alloc(a: int, ids_out):
+    """Fills ids_out (int32 numpy array) with len(ids_out) fresh blocks."""
+    _check(lib().kv_allocator_alloc(a, len(ids_out), _ptr(ids_out)), "kv_allocator_alloc")
+
+
+def kv_allocator_share(a: int, ids):
+    _check(lib().kv_allocator_share(a, len(ids), _ptr(ids)), "kv_allocator_share")
+
+
+def kv_allocator_free(a: int, ids):
+    _check(lib().kv_allocator_free(a, len(ids), _ptr(ids)), "kv_allocator_free")
+
+
+def kv_allocator_refcount(a: int, block_id: int) -> int:
+    r = _i32()
+    _check(lib().kv_allocator_refcount(a, block_id, ctypes.byref(r)), "kv_allocator_refcount")
+    return r.value
+
+
+def kv_allocator_num_free(a: int) -> int:
+    r = _i32()
+    _check(lib().kv_allocator_num_free(a, ctypes.byref(r)), "kv_allocator_num_free")
+    return r.value
+
+
+def kv_prepare_append(a: int, table_row, num_blocks: int, cur_len: int, n_new: int, slots_out,
+                      cow_src, cow_dst, block_size: int = 16):
+    """Host step of an append.  table_row (int32), slots_out (int64), cow_src/cow_dst
+    (int32, capacity = their length) are numpy arrays updated in place.
+    Returns (num_blocks, n_cow)."""
+    nb = _i32(num_blocks)
+    ncow = _i32(len(cow_src))
+    _check(lib().kv_prepare_append(a, block_size, _ptr(table_row), len(table_row),
+                                   ctypes.byref(nb), cur_len, n_new, _ptr(slots_out),
+                                   _ptr(cow_src), _ptr(cow_dst), ctypes.byref(ncow)),
+           "kv_prepare_append")
+    return nb.value, ncow.value
+
+
+# ---------------------------------------------------------------- pool
+def kv_pool_create(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                   dtype: int) -> int:
+    h = _vp()
+    _check(lib().kv_pool_create(num_blocks, block_size, num_kv_heads, head_dim, dtype,
+                                ctypes.byref(h)), "kv_pool_create")
+    return h.value
+
+
+def kv_pool_destroy(p: int):
+    _check(lib().kv_pool_destroy(p), "kv_pool_destroy")
+
+
+def kv_pool_ptrs(p: int):
+    k, v = _vp(), _vp()
+    _check(lib().kv_pool_ptrs(p, ctypes.byref(k), ctypes.byref(v)), "kv_pool_ptrs")
+    return k.value, v.value
+
+
+def kv_pool_allocator(p: int) -> int:
+    a = _vp()
+    _check(lib().kv_pool_allocator(p, ctypes.byref(a)), "kv_pool_allocator")
+    return a.value
+
+
+def kv_append(p: int, k_new, v_new, slot_mapping, num_tokens: int, stream=None):
+    _check(lib().kv_append(p, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), num_tokens,
+                           _stream(stream)), "kv_append")
+
+
+def kv_copy_blocks(p: int, src, dst, n: int, stream=None):
+    _check(lib().kv_copy_blocks(p, _ptr(src), _ptr(dst), n, _stream(stream)), "kv_copy_blocks")
+
+
+def kv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                             num_splits=0) -> int:
+    r = _sz()
+    _check(lib().kv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                          num_splits, ctypes.byref(r)), "kv_decode_workspace_size")
+    return r.value
+
+
+def kv_decode_split_plan(batch, num_kv_heads, max_blocks, num_splits=0):
+    pb, ms = _i32(), _i32()
+    _check(lib().kv_decode_split_plan(batch, num_kv_heads, max_blocks, num_splits,
+                                      ctypes.byref(pb), ctypes.byref(ms)), "kv_decode_split_plan")
+    return pb.value, ms.value
+
+
+def paged_decode_attention(p: int, q, block_tables, max_blocks: int, seq_lens, batch: int,
+                           num_q_heads: int, scale: float, out, out_dtype: int, lse_out=None,
+                           num_splits: int = 0, workspace=None, workspace_bytes: int = 0,
+                           stream=None):
+    _check(lib().paged_decode_attention(p, _ptr(q), _ptr(block_tables), max_blocks, _ptr(seq_lens),
+                                        batch, num_q_heads, scale, _ptr(out), out_dtype,
+                                        _ptr(lse_out), num_splits, _ptr(workspace),
+                                        workspace_bytes, _stream(stream)),
+           "paged_decode_attention")
+
+
+def paged_prefill_attention(p: int, q, cu_q, max_q_len: int, block_tables, max_blocks: int,
+                            seq_lens, batch: int, num_q_heads: int, scale: float, out,
+                            out_dtype: int, lse_out=None, stream=None):
+    _check(lib().paged_prefill_attention(p, _ptr(q), _ptr(cu_q), max_q_len, _ptr(block_tables),
+                                         max_blocks, _ptr(seq_lens), batch, num_q_heads, scale,
+                                         _ptr(out), out_dtype, _ptr(lse_out), _stream(stream)),
+           "paged_prefill_attention")
+
+
+def kv_get_device_error(p: int, stream=None) -> int:
+    """Returns the device error bits (and clears them); never raises on set bits."""
+    code = _i32()
+    st = lib().kv_get_device_error(p, ctypes.byref(code), _stream(stream))
+    if st not in (0, -5, -6):
+        raise KVError(st, "kv_get_device_error")
+    return code.value
+
+
+# ---------------------------------------------------------------- contiguous path
+def kv_contig_create(max_requests, max_tokens, num_kv_heads, head_dim, dtype) -> int:
+    h = _vp()
+    _check(lib().kv_contig_create(max_requests, max_tokens, num_kv_heads, head_dim, dtype,
+                                  ctypes.byref(h)), "kv_contig_create")
+    return h.value
+
+
+def kv_contig_destroy(c: int):
+    _check(lib().kv_contig_destroy(c), "kv_contig_destroy")
+
+
+def kv_contig_layout(c: int):
+    hs, pg, rb = _i64(), _i64(), _i64()
+    _check(lib().kv_contig_layout(c, ctypes.byref(hs), ctypes.byref(pg), ctypes.byref(rb)),
+           "kv_contig_layout")
+    return hs.value, pg.value, rb.value
+
+
+def kv_contig_reserve(c: int, req: int):
+    _check(lib().kv_contig_reserve(c, req), "kv_contig_reserve")
+
+
+def kv_contig_ensure(c: int, req: int, n_tokens: int):
+    _check(lib().kv_contig_ensure(c, req, n_tokens), "kv_contig_ensure")
+
+
+def kv_contig_release(c: int, req: int):
+    _check(lib().kv_contig_release(c, req), "kv_contig_release")
+
+
+def kv_contig_ptrs(c: int, req: int):
+    k, v = _vp(), _vp()
+    _check(lib().kv_contig_ptrs(c, req, ctypes.byref(k), ctypes.byref(v)), "kv_contig_ptrs")
+    return k.value, v.value
+
+
+def kv_contig_stats(c: int, req: int):
+    t, b = _i64(), _i64()
+    _check(lib().kv_contig_stats(c, req, ctypes.byref(t), ctypes.byref(b)), "kv_contig_stats")
+    return t.value, b.value
+
+
+def kv_contig_append(c: int, k_new, v_new, req_ids, positions, num_tokens: int, stream=None):
+    _check(lib().kv_contig_append(c, _ptr(k_new), _ptr(v_new), _ptr(req_ids), _ptr(positions),
+                                  num_tokens, _stream(stream)), "kv_contig_append")
+
+
+def contig_decode_attention(c: int, q, req_ids, seq_lens, batch: int, num_q_heads: int,
+                            scale: float, out, out_dtype: int, lse_out=None, num_splits: int = 0,
+                            workspace=None, workspace_bytes: int = 0, stream=None):
+    _check(lib().contig_decode_attention(c, _ptr(q), _ptr(req_ids), _ptr(seq_lens), batch,
+                                         num_q_heads, scale, _ptr(out), out_dtype, _ptr(lse_out),
+                                         num_splits, _ptr(workspace), workspace_bytes,
+                                         _stream(stream)),
+           "contig_decode_attention")
+
+
+def kv_contig_get_device_error(c: int, stream=None) -> int:
+    code = _i32()
+    st = lib().kv_contig_get_device_error(c, ctypes.byref(code), _stream(stream))
+    if st not in (0, -5, -6):
+        raise KVError(st, "kv_contig_get_device_error")
+    return code.value

@@ -1,0 +1,118 @@
+// Device-side helpers shared by the kernels: mbarriers, bulk (TMA) copies,
+// bfloat16 packing, bounded waits.  Inline PTX written for sm_100-family
+// parts (built for sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "paged_kv.h"
+
+#define KV_DEVICE __device__ __forceinline__
+
+namespace pkv {
+
+// A pipeline wait gives up after this many nanoseconds (then the kernel
+// records KV_DEVERR_TIMEOUT and winds down instead of spinning forever).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+KV_DEVICE uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+KV_DEVICE unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+KV_DEVICE void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+// Makes barrier initialisation visible to the async (TMA / tensor) proxy.
+KV_DEVICE void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+KV_DEVICE void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+KV_DEVICE void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+KV_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false
+// (after setting KV_DEVERR_TIMEOUT in *err) if that takes longer than
+// kWaitLimitNs.
+KV_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (err) atomicOr(err, KV_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------ bulk copies
+// One-dimensional bulk copy global -> shared, completion signalled on an
+// mbarrier as transaction bytes.  dst, src 16-byte aligned; bytes % 16 == 0.
+KV_DEVICE void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                        uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once (streamed KV).
+KV_DEVICE uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Named barrier over a subset of warps.
+KV_DEVICE void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- bf16
+// A 32-bit word holding two bfloat16 values (low half = lower index).
+// Widening bf16 -> fp32 is exact: the bf16 bits are the top half of fp32.
+KV_DEVICE float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+KV_DEVICE float bf16_to_float(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+
+KV_DEVICE uint16_t float_to_bf16_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+KV_DEVICE float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+}  // namespace pkv

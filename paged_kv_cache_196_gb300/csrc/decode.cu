@@ -1,0 +1,657 @@
+// Paged decode attention, its contiguous (vAttention-style) twin, and the
+// split-KV log-sum-exp merge.
+//
+// Maths: o = softmax(scale * q K^T) V over the sequence's logical keys, read
+// through the block table ("PagedAttention Nedir?", "Nasil Calisir?" step 4)
+// or from one contiguous per-request range ("Makale Bulteni -- vAttention",
+// "Iddia ve Gerceklik: vAttention").  The score matrix is never written out:
+// keys are visited block by block with a running max and sum ("PagedAttention
+// Nedir?", "FlashAttention ile Ayni mi?": the large intermediate attention
+// matrix is not materialised).
+//
+// Work decomposition.  One CTA handles (split s, kv head h, sequence b): the
+// blocks [s*PB, min((s+1)*PB, ceil(L/16))) of that sequence for all g query
+// heads that read kv head h, so every K/V byte is fetched once per kv head.
+// Warp kNW (the producer) copies the CTA's block-table slice into shared
+// memory once, then streams each (block, head) tile -- 16 tokens x head_dim,
+// contiguous in the pool -- with one-dimensional bulk (TMA) copies into an
+// NSTAGE-deep ring of shared-memory stages guarded by mbarriers.  Consumer
+// warp w owns the blocks i = w (mod kNW); it keeps its own running max, sum
+// and output accumulators, so no CTA-wide barrier is taken per block.  The kNW
+// partial states are merged once at the end; with several splits per
+// sequence a second kernel merges the splits through their log-sum-exp.
+//
+// Inside a consumer warp, half-warp hf takes token 2p+hf of pass p and lane
+// c = lane % 16 owns head_dim/16 consecutive dimensions.  Partial dot products
+// for the g heads are reduced across the 16 lanes with a reduce-scatter
+// (each exchange step halves the number of values carried), ending with lane c
+// holding the score of head c / (16/G).  Products use packed fp32x2 FMAs.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+constexpr int kNW = 4;                   // consumer warps per CTA
+constexpr int kDecodeThreads = (kNW + 1) * 32;
+constexpr int kBS = 16;                  // tokens per block
+constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
+constexpr int kNStage = 8;               // pipeline depth (a multiple of kNW)
+static_assert(kNStage % kNW == 0, "each stage must belong to one consumer warp");
+
+struct DecodeKParams {
+    const void *q;
+    const char *k_pool;
+    const char *v_pool;
+    const int32_t *tables;
+    int max_blocks;
+    int num_blocks;
+    const unsigned long long *k_bases;
+    const unsigned long long *v_bases;
+    const int32_t *req_ids;
+    const long long *mapped_tokens;
+    long long head_stride;
+    int max_requests;
+    const int32_t *seq_lens;
+    int num_q_heads;
+    int num_kv_heads;
+    int g;
+    float scale_log2;  // scale * log2(e): scores are kept in the log2 domain
+    int part_blocks;
+    int max_splits;
+    void *out;
+    int out_bf16;
+    float *lse;
+    float *ws_o;
+    float *ws_lse;
+    int *err;
+};
+
+template <int D, bool BF16>
+struct TileShape {
+    static constexpr int kElem = BF16 ? 2 : 4;
+    static constexpr int kBytes = kBS * D * kElem;  // one (block, kv head) tile
+    static constexpr int kDPL = D / 16;             // dimensions per lane
+    static constexpr int kPairs = kDPL / 2;
+};
+
+// Loads this lane's kDPL dimensions of row t of a tile as fp32 pairs.
+template <int D, bool BF16>
+KV_DEVICE void load_row(const char *tile, int t, int c, float2 (&x)[TileShape<D, BF16>::kPairs]) {
+    using S = TileShape<D, BF16>;
+    const char *row = tile + (size_t)t * D * S::kElem + (size_t)c * S::kDPL * S::kElem;
+    if constexpr (BF16) {
+        if constexpr (S::kDPL == 8) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(row);
+            x[0] = bf16x2_to_float2(w.x);
+            x[1] = bf16x2_to_float2(w.y);
+            x[2] = bf16x2_to_float2(w.z);
+            x[3] = bf16x2_to_float2(w.w);
+        } else {
+            const uint2 w = *reinterpret_cast<const uint2 *>(row);
+            x[0] = bf16x2_to_float2(w.x);
+            x[1] = bf16x2_to_float2(w.y);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < S::kDPL / 4; ++i) {
+            const float4 f = reinterpret_cast<const float4 *>(row)[i];
+            x[2 * i] = make_float2(f.x, f.y);
+            x[2 * i + 1] = make_float2(f.z, f.w);
+        }
+    }
+}
+
+// Sum of v[0..N) over the 16 lanes of a half-warp, scattered: on return v[0]
+// of lane c holds the total of entry c / (16/N_initial).  DIST walks 8,4,2,1.
+template <int N, int DIST>
+KV_DEVICE void reduce_scatter16(float *v, int lane) {
+    if constexpr (DIST > 0) {
+        if constexpr (N > 1) {
+            constexpr int H = N / 2;
+            const bool up = (lane & DIST) != 0;
+#pragma unroll
+            for (int k = 0; k < H; ++k) {
+                const float send = up ? v[k] : v[k + H];
+                const float keep = up ? v[k + H] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, DIST);
+            }
+            reduce_scatter16<H, DIST / 2>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], DIST);
+            reduce_scatter16<1, DIST / 2>(v, lane);
+        }
+    }
+}
+
+// Bytes of the stage ring; the final cross-warp merge reuses it.
+template <int D, int G, bool BF16>
+constexpr size_t decode_ring_bytes() {
+    constexpr size_t ring = (size_t)kNStage * 2 * TileShape<D, BF16>::kBytes;
+    constexpr size_t merge = (size_t)kNW * (G * D + 2 * G) * sizeof(float);
+    return ((ring > merge ? ring : merge) + 127) / 128 * 128;
+}
+
+// HS = 1: the two half-warps take different tokens (2 per pass) and every
+// lane carries all G heads.  HS = 2: both halves take the same token and each
+// carries G/2 heads (half the q and accumulator registers, for large G).
+template <int D, int G, int HS, bool BF16, bool LINEAR>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeKParams p) {
+    using S = TileShape<D, BF16>;
+    constexpr int kTile = S::kBytes;
+    constexpr int kPairs = S::kPairs;
+    constexpr int GH = G / HS;                 // heads per lane
+    constexpr int kLanesPerHead = 16 / GH;
+    constexpr int kPasses = 8 * HS;            // passes over a 16-token block
+    static_assert(GH >= 1 && (HS == 1 || HS == 2), "bad head split");
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- the slice of keys this CTA owns
+    long long L = p.seq_lens[b];
+    const char *k_lin = nullptr, *v_lin = nullptr;
+    if constexpr (LINEAR) {
+        const int req = p.req_ids[b];
+        if (req < 0 || req >= p.max_requests || p.k_bases[req] == 0) {
+            if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+            L = 0;
+        } else {
+            const long long mapped = p.mapped_tokens[req];
+            if (L > mapped) {
+                if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+                L = mapped;
+            }
+            k_lin = reinterpret_cast<const char *>(p.k_bases[req]);
+            v_lin = reinterpret_cast<const char *>(p.v_bases[req]);
+        }
+    }
+    // The split plan covers max_blocks blocks (the table width, or the
+    // contiguous path's max_tokens); longer lengths are clamped and flagged.
+    if (L > (long long)p.max_blocks * kBS) {
+        if (tid == 0 && split == 0 && h == 0)
+            atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
+        L = (long long)p.max_blocks * kBS;
+    }
+    if (L < 0) L = 0;
+    const int nblk = (int)((L + kBS - 1) / kBS);
+    const int blk0 = split * p.part_blocks;
+    if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
+    const int nloc = max(0, min(p.part_blocks, nblk - blk0));
+    const int nsplit = max(1, (nblk + p.part_blocks - 1) / p.part_blocks);
+
+    // ---- shared memory
+    extern __shared__ __align__(128) char smem[];
+    char *stages = smem;                                                   // kNStage x (K, V)
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + decode_ring_bytes<D, G, BF16>());
+    uint64_t *empty = full + kNStage;
+    int *stage_valid = reinterpret_cast<int *>(empty + kNStage);
+    float2 *pscr = reinterpret_cast<float2 *>(stage_valid + kNStage);      // [kNW][16][G]
+    float *ascr = reinterpret_cast<float *>(pscr + kNW * kBS * G);         // [kNW][G]
+    int32_t *tbl = reinterpret_cast<int32_t *>(ascr + kNW * G);            // [part_blocks]
+
+    if (warp == kNW) {
+        if constexpr (!LINEAR) {
+            const int32_t *row = p.tables + (size_t)b * p.max_blocks + blk0;
+            for (int i = lane; i < nloc; i += 32) tbl[i] = __ldg(row + i);
+        }
+        if (lane == 0) {
+            for (int s = 0; s < kNStage; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 32);
+            }
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+
+    // ======================================================== producer warp
+    if (warp == kNW) {
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first_policy();
+            int issued = 0;
+            for (int i = 0; i < nloc; ++i) {
+                const int st = i % kNStage, r = i / kNStage;
+                if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err)) break;
+                const char *ks;
+                const char *vs;
+                bool valid = true;
+                if constexpr (LINEAR) {
+                    const size_t off =
+                        ((size_t)h * p.head_stride + (size_t)(blk0 + i) * kBS) * D * S::kElem;
+                    ks = k_lin + off;
+                    vs = v_lin + off;
+                } else {
+                    const int id = tbl[i];
+                    valid = id >= 0 && id < p.num_blocks;
+                    if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                    const size_t off = ((size_t)(valid ? id : 0) * p.num_kv_heads + h) * kTile;
+                    ks = p.k_pool + off;
+                    vs = p.v_pool + off;
+                }
+                stage_valid[st] = valid ? 1 : 0;
+                char *dst = stages + st * 2 * kTile;
+                if (valid) {
+                    mbar_arrive_expect_tx(&full[st], 2 * kTile);
+                    bulk_g2s(dst, ks, kTile, &full[st], policy);
+                    bulk_g2s(dst + kTile, vs, kTile, &full[st], policy);
+                } else {
+                    mbar_arrive(&full[st]);
+                }
+                issued = i + 1;
+            }
+            // Do not leave while a copy into this CTA's shared memory may be in flight.
+            for (int st = 0; st < kNStage && st < issued; ++st) {
+                const int r_last = (issued - 1 - st) / kNStage;
+                mbar_wait(&full[st], r_last & 1, p.err);
+            }
+        }
+        return;
+    }
+
+    // ======================================================== consumer warps
+    const int hf = lane >> 4, c = lane & 15;
+    const int hoff = HS == 2 ? hf * GH : 0;             // first head this lane carries
+    const int my_head = hoff + c / kLanesPerHead;       // head whose score this lane ends with
+    const bool rep = (c % kLanesPerHead) == 0;          // one writer per (half, head)
+    const bool rep_once = rep && (HS == 2 || hf == 0);  // one writer per head
+
+    // q for this lane's heads and dimensions, pre-scaled into the log2 domain.
+    float2 qv[GH][kPairs];
+#pragma unroll
+    for (int j = 0; j < GH; ++j) {
+        const int jj = hoff + j;
+        if (jj < p.g) {
+            const size_t base = ((size_t)b * p.num_q_heads + h * p.g + jj) * D + c * S::kDPL;
+            float2 x[kPairs];
+            load_row<D, BF16>(reinterpret_cast<const char *>(p.q) + base * S::kElem, 0, 0, x);
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m)
+                qv[j][m] = make_float2(x[m].x * p.scale_log2, x[m].y * p.scale_log2);
+        } else {
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m) qv[j][m] = make_float2(0.f, 0.f);
+        }
+    }
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float2 acc[GH][kPairs];
+#pragma unroll
+    for (int j = 0; j < GH; ++j)
+#pragma unroll
+        for (int m = 0; m < kPairs; ++m) acc[j][m] = make_float2(0.f, 0.f);
+
+    float2 *pw = pscr + warp * kBS * G;
+    float *aw = ascr + warp * G;
+
+    for (int i = warp; i < nloc; i += kNW) {
+        const int st = i % kNStage, r = i / kNStage;
+        if (!mbar_wait(&full[st], r & 1, p.err)) break;
+        const char *kt = stages + st * 2 * kTile;
+        const char *vt = kt + kTile;
+        int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
+        if (!stage_valid[st]) ntok = 0;
+
+        // ---- scores for this lane's head
+        float s[kPasses];
+#pragma unroll
+        for (int pass = 0; pass < kPasses; ++pass) {
+            const int t = HS == 1 ? 2 * pass + hf : pass;
+            float2 kx[kPairs];
+            load_row<D, BF16>(kt, t, c, kx);
+            float part[GH];
+#pragma unroll
+            for (int j = 0; j < GH; ++j) {
+                float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < kPairs; ++m) a2 = ffma2(qv[j][m], kx[m], a2);
+                part[j] = a2.x + a2.y;
+            }
+            reduce_scatter16<GH, 8>(part, c);
+            s[pass] = t < ntok ? part[0] : -INFINITY;
+        }
+
+        // ---- online softmax update for this lane's head
+        float mb = s[0];
+#pragma unroll
+        for (int pass = 1; pass < kPasses; ++pass) mb = fmaxf(mb, s[pass]);
+        if (HS == 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+        const float m_new = fmaxf(m_run, mb);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = exp2f(m_run - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int pass = 0; pass < kPasses; ++pass) {
+            const float pr = exp2f(s[pass] - m_use);
+            psum += pr;
+            const int t = HS == 1 ? 2 * pass + hf : pass;
+            if (rep) pw[t * G + my_head] = make_float2(pr, pr);
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (rep_once) aw[my_head] = alpha;
+        __syncwarp();
+
+        // ---- rescale and accumulate P V
+#pragma unroll
+        for (int j = 0; j < GH; ++j) {
+            const float a = aw[hoff + j];
+            const float2 a2 = make_float2(a, a);
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m) acc[j][m] = __fmul2_rn(acc[j][m], a2);
+        }
+#pragma unroll
+        for (int pass = 0; pass < kPasses; ++pass) {
+            const int t = HS == 1 ? 2 * pass + hf : pass;
+            float2 vx[kPairs];
+            load_row<D, BF16>(vt, t, c, vx);
+            if (t >= ntok) {  // skip, never multiply: the unused slots may hold anything
+#pragma unroll
+                for (int m = 0; m < kPairs; ++m) vx[m] = make_float2(0.f, 0.f);
+            }
+            const float2 *prow = pw + t * G + hoff;
+#pragma unroll
+            for (int j = 0; j < GH; ++j) {
+                const float2 pj = prow[j];
+#pragma unroll
+                for (int m = 0; m < kPairs; ++m) acc[j][m] = ffma2(pj, vx[m], acc[j][m]);
+            }
+        }
+        __syncwarp();
+        mbar_arrive(&empty[st]);
+    }
+
+    if constexpr (HS == 1) {
+        // merge the two half-warps (same heads and dims, disjoint tokens)
+#pragma unroll
+        for (int j = 0; j < GH; ++j)
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m) {
+                acc[j][m].x += __shfl_xor_sync(0xffffffffu, acc[j][m].x, 16);
+                acc[j][m].y += __shfl_xor_sync(0xffffffffu, acc[j][m].y, 16);
+            }
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+    }
+
+    // ---- merge the kNW warps through shared memory (reusing the stage ring)
+    named_bar_sync(1, kNW * 32);  // every consumer is done reading stages
+    float *sm_o = reinterpret_cast<float *>(stages);   // [kNW][G][D]
+    float *sm_m = sm_o + kNW * G * D;                  // [kNW][G]
+    float *sm_l = sm_m + kNW * G;                      // [kNW][G]
+    if (HS == 2 || hf == 0) {
+#pragma unroll
+        for (int j = 0; j < GH; ++j)
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m)
+                *reinterpret_cast<float2 *>(sm_o + (warp * G + hoff + j) * D + c * S::kDPL +
+                                            2 * m) = acc[j][m];
+        if (rep_once) {
+            sm_m[warp * G + my_head] = m_run;
+            sm_l[warp * G + my_head] = l_run;
+        }
+    }
+    named_bar_sync(1, kNW * 32);
+
+    constexpr float kLn2 = 0.6931471805599453f;
+    for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
+        const int j = idx / D, d = idx - j * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * G + j]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+                const float f = exp2f(sm_m[w * G + j] - M);
+                num += f * sm_o[(w * G + j) * D + d];
+                den += f * sm_l[w * G + j];
+            }
+        }
+        const float o = den > 0.f ? num / den : 0.f;
+        const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
+        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
+        if (nsplit == 1) {
+            if (p.out_bf16)
+                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(o);
+            else
+                reinterpret_cast<float *>(p.out)[row * D + d] = o;
+            if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+        } else {
+            p.ws_o[(row * p.max_splits + split) * D + d] = o;
+            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
+        }
+    }
+}
+
+// Merges the per-split results of sequences cut into more than one split:
+// o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), lse in the log2 domain.
+// One warp per (sequence, query head); lanes cover head_dim.
+__global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws_o,
+                                                    const float *__restrict__ ws_lse,
+                                                    const int32_t *__restrict__ seq_lens,
+                                                    const long long *mapped_tokens,
+                                                    const int32_t *req_ids, int max_requests,
+                                                    int max_len_tokens, int batch,
+                                                    int num_q_heads, int head_dim,
+                                                    int part_blocks, int max_splits, void *out,
+                                                    int out_bf16, float *lse) {
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= batch * num_q_heads) return;
+    const int b = row / num_q_heads;
+    long long L = seq_lens[b];
+    if (mapped_tokens) {  // contiguous path: clamp exactly as the decode kernel did
+        const int req = req_ids[b];
+        L = (req < 0 || req >= max_requests) ? 0 : min(L, mapped_tokens[req]);
+    }
+    if (L > max_len_tokens) L = max_len_tokens;
+    if (L < 0) L = 0;
+    const int nblk = (int)((L + kBS - 1) / kBS);
+    const int nsplit = max(1, (nblk + part_blocks - 1) / part_blocks);
+    if (nsplit == 1) return;  // the decode kernel wrote the final result
+    const float *ls = ws_lse + (size_t)row * max_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ls[s]);
+    float den = 0.f;
+    for (int s = 0; s < nsplit; ++s) den += M == -INFINITY ? 0.f : exp2f(ls[s] - M);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int d = lane; d < head_dim; d += 32) {
+        float num = 0.f;
+        if (M != -INFINITY)
+            for (int s = 0; s < nsplit; ++s)
+                num += exp2f(ls[s] - M) * ws_o[((size_t)row * max_splits + s) * head_dim + d];
+        const float o = num * inv;
+        if (out_bf16)
+            reinterpret_cast<uint16_t *>(out)[(size_t)row * head_dim + d] = float_to_bf16_rn(o);
+        else
+            reinterpret_cast<float *>(out)[(size_t)row * head_dim + d] = o;
+    }
+    if (lse && lane == 0) lse[row] = den > 0.f ? (M + log2f(den)) * 0.6931471805599453f : -INFINITY;
+}
+
+void split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits, int *part_blocks,
+                int *max_splits) {
+    int pb;
+    if (max_blocks <= 0) {
+        pb = kNW;
+    } else if (num_splits > 0) {
+        pb = (max_blocks + num_splits - 1) / num_splits;
+    } else {
+        // Aim for about 8 CTAs per SM over the widest possible table.
+        const long long units = (long long)batch * num_kv_heads;
+        const long long target = 8LL * sm_count();
+        long long want = (target + units - 1) / units;
+        if (want < 1) want = 1;
+        pb = (int)((max_blocks + want - 1) / want);
+        if (pb < 16) pb = 16;
+    }
+    pb = (pb + kNW - 1) / kNW * kNW;
+    if (pb > kMaxPartBlocks) pb = kMaxPartBlocks;
+    if (pb < kNW) pb = kNW;
+    *part_blocks = pb;
+    *max_splits = max_blocks <= 0 ? 1 : (max_blocks + pb - 1) / pb;
+}
+
+size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_splits) {
+    if (max_splits <= 1) return 0;
+    return (size_t)batch * num_q_heads * max_splits * (head_dim + 1) * sizeof(float);
+}
+
+template <int D, int G, bool BF16, bool LINEAR>
+static size_t decode_smem_bytes(int part_blocks) {
+    return decode_ring_bytes<D, G, BF16>() + 2 * kNStage * sizeof(uint64_t) + kNStage * sizeof(int) +
+           (size_t)kNW * kBS * G * sizeof(float2) + (size_t)kNW * G * sizeof(float) +
+           (size_t)(LINEAR ? 0 : part_blocks) * sizeof(int32_t);
+}
+
+template <int D, int G, bool BF16, bool LINEAR>
+static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
+    const size_t smem = decode_smem_bytes<D, G, BF16, LINEAR>(kp.part_blocks);
+    // Large head groups split their heads across the two half-warps (register pressure).
+    constexpr int HS = (G >= 8 && D == 128) ? 2 : 1;
+    auto fn = decode_kernel<D, G, HS, BF16, LINEAR>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return KV_ERR_CUDA;
+    fn<<<grid, kDecodeThreads, smem, s>>>(kp);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int D, bool BF16, bool LINEAR>
+static kv_status launch_g(int G, const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_t<D, 1, BF16, LINEAR>(kp, grid, s);
+        case 2: return launch_t<D, 2, BF16, LINEAR>(kp, grid, s);
+        case 4: return launch_t<D, 4, BF16, LINEAR>(kp, grid, s);
+        case 8: return launch_t<D, 8, BF16, LINEAR>(kp, grid, s);
+    }
+    return KV_ERR_UNSUPPORTED;
+}
+
+kv_status launch_decode(const DecodeArgs &a, bool linear) {
+    if (a.batch < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0) return KV_ERR_ARG;
+    if (a.num_q_heads % a.num_kv_heads) return KV_ERR_ARG;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    if (g > 8) return KV_ERR_UNSUPPORTED;
+    if (a.head_dim != 64 && a.head_dim != 128) return KV_ERR_UNSUPPORTED;
+    if (a.out_dtype != KV_F32 && a.out_dtype != a.dtype) return KV_ERR_UNSUPPORTED;
+    if (a.batch == 0) return KV_OK;
+    if (!a.q || !a.seq_lens || !a.out) return KV_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(a.q) & 15) return KV_ERR_ARG;
+    const int G = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+    int pb = 0, ms = 0;
+    split_plan(a.batch, a.num_kv_heads, a.max_blocks, a.num_splits, &pb, &ms);
+    const size_t need = decode_workspace_bytes(a.batch, a.num_q_heads, a.head_dim, ms);
+    if (need > 0 && (!a.workspace || a.workspace_bytes < need)) return KV_ERR_ARG;
+    if (ms > 65535 || a.batch > 65535 || a.num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
+
+    DecodeKParams kp{};
+    kp.q = a.q;
+    kp.k_pool = static_cast<const char *>(a.k_pool);
+    kp.v_pool = static_cast<const char *>(a.v_pool);
+    kp.tables = a.block_tables;
+    kp.max_blocks = a.max_blocks;
+    kp.num_blocks = a.num_blocks;
+    kp.k_bases = a.k_bases;
+    kp.v_bases = a.v_bases;
+    kp.req_ids = a.req_ids;
+    kp.mapped_tokens = a.mapped_tokens;
+    kp.head_stride = a.head_stride;
+    kp.max_requests = a.max_requests;
+    kp.seq_lens = a.seq_lens;
+    kp.num_q_heads = a.num_q_heads;
+    kp.num_kv_heads = a.num_kv_heads;
+    kp.g = g;
+    kp.scale_log2 = a.scale * 1.4426950408889634f;
+    kp.part_blocks = pb;
+    kp.max_splits = ms;
+    kp.out = a.out;
+    kp.out_bf16 = a.out_dtype == KV_BF16;
+    kp.lse = a.lse;
+    kp.ws_o = static_cast<float *>(a.workspace);
+    kp.ws_lse = need > 0 ? kp.ws_o + (size_t)a.batch * a.num_q_heads * ms * a.head_dim : nullptr;
+    kp.err = a.err;
+
+    const dim3 grid(ms, a.num_kv_heads, a.batch);
+    kv_status st;
+    const bool bf = a.dtype == KV_BF16;
+    if (a.head_dim == 128) {
+        st = bf ? (linear ? launch_g<128, true, true>(G, kp, grid, a.stream)
+                          : launch_g<128, true, false>(G, kp, grid, a.stream))
+                : (linear ? launch_g<128, false, true>(G, kp, grid, a.stream)
+                          : launch_g<128, false, false>(G, kp, grid, a.stream));
+    } else {
+        st = bf ? (linear ? launch_g<64, true, true>(G, kp, grid, a.stream)
+                          : launch_g<64, true, false>(G, kp, grid, a.stream))
+                : (linear ? launch_g<64, false, true>(G, kp, grid, a.stream)
+                          : launch_g<64, false, false>(G, kp, grid, a.stream));
+    }
+    if (st != KV_OK || ms <= 1) return st;
+    const int rows = a.batch * a.num_q_heads;
+    merge_kernel<<<(rows + 3) / 4, 128, 0, a.stream>>>(
+        kp.ws_o, kp.ws_lse, a.seq_lens, linear ? a.mapped_tokens : nullptr, a.req_ids,
+        a.max_requests, a.max_blocks * kBS, a.batch, a.num_q_heads, a.head_dim, pb, ms, a.out,
+        kp.out_bf16, a.lse);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits,
+                               int *part_blocks, int *max_splits) {
+    if (!part_blocks || !max_splits || batch < 0 || num_kv_heads <= 0 || max_blocks < 0)
+        return KV_ERR_ARG;
+    split_plan(batch, num_kv_heads, max_blocks, num_splits, part_blocks, max_splits);
+    return KV_OK;
+}
+
+kv_status kv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int max_blocks, int num_splits, size_t *bytes) {
+    if (!bytes || batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks < 0)
+        return KV_ERR_ARG;
+    int pb, ms;
+    split_plan(batch, num_kv_heads, max_blocks, num_splits, &pb, &ms);
+    *bytes = decode_workspace_bytes(batch, num_q_heads, head_dim, ms);
+    return KV_OK;
+}
+
+kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *block_tables,
+                                 int max_blocks, const int32_t *seq_lens, int batch,
+                                 int num_q_heads, float scale, void *out, kv_dtype out_dtype,
+                                 float *lse_out, int num_splits, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    if (!p || max_blocks < 0 || (batch > 0 && max_blocks > 0 && !block_tables)) return KV_ERR_ARG;
+    DecodeArgs a{};
+    a.q = q;
+    a.k_pool = p->k;
+    a.v_pool = p->v;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.num_blocks = p->num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.head_dim = p->head_dim;
+    a.dtype = p->dtype;
+    a.scale = scale;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse_out;
+    a.num_splits = num_splits;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.err = p->err;
+    a.stream = as_stream(stream);
+    return launch_decode(a, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// Internal host-side definitions shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "paged_kv.h"
+
+struct kv_pool {
+    int num_blocks = 0;
+    int block_size = 0;
+    int num_kv_heads = 0;
+    int head_dim = 0;
+    kv_dtype dtype = KV_BF16;
+    int device = 0;
+    void *k = nullptr;  // [num_blocks][num_kv_heads][block_size][head_dim]
+    void *v = nullptr;
+    int *err = nullptr;  // device error word
+    kv_allocator_t alloc = nullptr;
+};
+
+namespace pkv {
+
+inline int dtype_bytes(kv_dtype t) { return t == KV_BF16 ? 2 : 4; }
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Maps a CUDA runtime error to a status (and clears sticky-free errors).
+inline kv_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KV_OK;
+    if (e == cudaErrorMemoryAllocation) return KV_ERR_OOM;
+    return KV_ERR_CUDA;
+}
+
+inline kv_status device_error_status(int code) {
+    if (code == 0) return KV_OK;
+    if (code & KV_DEVERR_TIMEOUT) return KV_ERR_TIMEOUT;
+    return KV_ERR_DEVICE_BOUNDS;
+}
+
+int sm_count();
+
+// ---- decode (shared by the paged and contiguous paths) ----
+struct DecodeArgs {
+    const void *q;
+    // paged addressing
+    const void *k_pool;
+    const void *v_pool;
+    const int32_t *block_tables;
+    int max_blocks;
+    int num_blocks;
+    // contiguous addressing
+    const unsigned long long *k_bases;  // per request
+    const unsigned long long *v_bases;
+    const int32_t *req_ids;
+    const long long *mapped_tokens;  // per request
+    long long head_stride;           // tokens per head region
+    int max_requests;
+    // common
+    const int32_t *seq_lens;
+    int batch;
+    int num_q_heads;
+    int num_kv_heads;
+    int head_dim;
+    kv_dtype dtype;
+    float scale;
+    void *out;
+    kv_dtype out_dtype;
+    float *lse;
+    int num_splits;
+    void *workspace;
+    size_t workspace_bytes;
+    int *err;
+    cudaStream_t stream;
+};
+
+void split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits, int *part_blocks,
+                int *max_splits);
+size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_splits);
+kv_status launch_decode(const DecodeArgs &a, bool linear);
+
+}  // namespace pkv

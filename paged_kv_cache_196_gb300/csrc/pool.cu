@@ -1,0 +1,191 @@
+// Device pool, KV append (slot-mapping write) and copy-on-write block copy.
+//
+// KV append: "Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve Gerceklik"
+// (a new token goes into the current block; a free block is taken when it is
+// full) and "PagedAttention Nedir?", "Nasil Calisir?" steps 1-3.  The host
+// decides the slots (kv_prepare_append); the kernel is an exact scatter.
+//
+// Copy-on-write: same page, "Iddia ve Gerceklik" (blocks shared by pointer
+// between parallel samples and branches, copied when written).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+// One thread moves one 16-byte chunk of K and the matching chunk of V.
+// Layout: k_new/v_new [T][Hkv][row_chunks] (16-byte chunks of a head row);
+// pools [NB][Hkv][BS][row_chunks].
+__global__ void __launch_bounds__(256) append_kernel(uint4 *__restrict__ k_pool,
+                                                     uint4 *__restrict__ v_pool,
+                                                     const uint4 *__restrict__ k_new,
+                                                     const uint4 *__restrict__ v_new,
+                                                     const int64_t *__restrict__ slots,
+                                                     long long total_chunks, int hkv,
+                                                     int row_chunks, int block_size,
+                                                     long long num_slots, int *err) {
+    const int per_token = hkv * row_chunks;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total_chunks;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_token;
+        const int rem = (int)(i - t * per_token);
+        const int h = rem / row_chunks, c = rem - h * row_chunks;
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (rem == 0) atomicOr(err, KV_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const long long blk = slot / block_size, off = slot - blk * block_size;
+        const long long dst = ((blk * hkv + h) * block_size + off) * row_chunks + c;
+        const uint4 kv = __ldg(k_new + i);
+        const uint4 vv = __ldg(v_new + i);
+        k_pool[dst] = kv;
+        v_pool[dst] = vv;
+    }
+}
+
+// Copies whole blocks (all heads and slots) of K and V: pair p moves block
+// src[p] to block dst[p].  block_chunks = 16-byte chunks per block per pool.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_pool,
+                                                          uint4 *__restrict__ v_pool,
+                                                          const int32_t *__restrict__ src,
+                                                          const int32_t *__restrict__ dst,
+                                                          int n, int block_chunks, int num_blocks,
+                                                          int *err) {
+    const long long total = (long long)n * block_chunks;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int p = (int)(i / block_chunks);
+        const int c = (int)(i - (long long)p * block_chunks);
+        const int s = __ldg(src + p), d = __ldg(dst + p);
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+            if (c == 0) atomicOr(err, KV_DEVERR_BLOCK_RANGE);
+            continue;
+        }
+        k_pool[(long long)d * block_chunks + c] = k_pool[(long long)s * block_chunks + c];
+        v_pool[(long long)d * block_chunks + c] = v_pool[(long long)s * block_chunks + c];
+    }
+}
+
+static int grid_for(long long work, int threads) {
+    long long blocks = (work + threads - 1) / threads;
+    long long cap = (long long)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    return blocks < 1 ? 1 : (int)blocks;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         kv_dtype dtype, kv_pool_t *out) {
+    if (!out || num_blocks <= 0 || num_kv_heads <= 0) return KV_ERR_ARG;
+    if (block_size != 16 || (head_dim != 64 && head_dim != 128) ||
+        (dtype != KV_F32 && dtype != KV_BF16))
+        return KV_ERR_UNSUPPORTED;
+    kv_pool *p = new (std::nothrow) kv_pool();
+    if (!p) return KV_ERR_OOM;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->num_kv_heads = num_kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = dtype;
+    cudaGetDevice(&p->device);
+    const size_t bytes = (size_t)num_blocks * num_kv_heads * block_size * head_dim * dtype_bytes(dtype);
+    kv_status st = KV_OK;
+    if (cudaMalloc(&p->k, bytes) != cudaSuccess || cudaMalloc(&p->v, bytes) != cudaSuccess ||
+        cudaMalloc(&p->err, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        st = KV_ERR_OOM;
+    } else if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess) {
+        st = KV_ERR_CUDA;
+    } else {
+        st = kv_allocator_create(num_blocks, &p->alloc);
+    }
+    if (st != KV_OK) {
+        kv_pool_destroy(p);
+        return st;
+    }
+    *out = p;
+    return KV_OK;
+}
+
+kv_status kv_pool_destroy(kv_pool_t p) {
+    if (!p) return KV_ERR_ARG;
+    if (p->k) cudaFree(p->k);
+    if (p->v) cudaFree(p->v);
+    if (p->err) cudaFree(p->err);
+    if (p->alloc) kv_allocator_destroy(p->alloc);
+    delete p;
+    return KV_OK;
+}
+
+kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool) {
+    if (!p) return KV_ERR_ARG;
+    if (k_pool) *k_pool = p->k;
+    if (v_pool) *v_pool = p->v;
+    return KV_OK;
+}
+
+kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out) {
+    if (!p || !out) return KV_ERR_ARG;
+    *out = p->alloc;
+    return KV_OK;
+}
+
+kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
+                    const int64_t *slot_mapping, int num_tokens, void *stream) {
+    if (!p || num_tokens < 0) return KV_ERR_ARG;
+    if (num_tokens == 0) return KV_OK;
+    if (!k_new || !v_new || !slot_mapping) return KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+        return KV_ERR_ARG;  // rows are moved as 16-byte chunks
+    const int row_chunks = p->head_dim * dtype_bytes(p->dtype) / 16;
+    const long long total = (long long)num_tokens * p->num_kv_heads * row_chunks;
+    append_kernel<<<grid_for(total, 256), 256, 0, as_stream(stream)>>>(
+        (uint4 *)p->k, (uint4 *)p->v, (const uint4 *)k_new, (const uint4 *)v_new, slot_mapping,
+        total, p->num_kv_heads, row_chunks, p->block_size,
+        (long long)p->num_blocks * p->block_size, p->err);
+    return cuda_status(cudaGetLastError());
+}
+
+kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, int n,
+                         void *stream) {
+    if (!p || n < 0) return KV_ERR_ARG;
+    if (n == 0) return KV_OK;
+    if (!src || !dst) return KV_ERR_ARG;
+    const int block_chunks = p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype) / 16;
+    copy_blocks_kernel<<<grid_for((long long)n * block_chunks, 256), 256, 0, as_stream(stream)>>>(
+        (uint4 *)p->k, (uint4 *)p->v, src, dst, n, block_chunks, p->num_blocks, p->err);
+    return cuda_status(cudaGetLastError());
+}
+
+kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream) {
+    if (!p || !code) return KV_ERR_ARG;
+    int h = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&h, p->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (h != 0 && cudaMemsetAsync(p->err, 0, sizeof(int), s) != cudaSuccess) return KV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+    *code = h;
+    return device_error_status(h);
+}
+
+}  // extern "C"

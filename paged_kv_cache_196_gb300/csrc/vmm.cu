@@ -1,0 +1,394 @@
+// Contiguous (vAttention-style) KV path.
+//
+// "Makale Bulteni -- vAttention", section "Iddia ve Gerceklik: vAttention":
+// at request start a contiguous virtual buffer large enough for the maximum
+// context is reserved (cuMemAddressRangeReserve) and uses no physical memory;
+// physical pages are created and mapped (cuMemCreate, cuMemMap) only as the
+// request grows; the attention kernel then sees one contiguous tensor and the
+// GPU's MMU/TLB does the translation.  The stock driver's smallest page for
+// this is its allocation granularity (2 MiB), which is what is used here.
+//
+// Per request: one reservation holding the K region [Hkv][head_stride][D]
+// followed by the V region of the same shape.  head_stride is max_tokens
+// rounded up to whole pages so every head's region starts on a page and
+// grows page by page.  Each page is its own physical allocation.
+//
+// Driver entry points are fetched through the runtime at first use, so the
+// library loads on machines without a GPU driver.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+struct DriverVmm {
+    CUresult (*getGranularity)(size_t *, const CUmemAllocationProp *, CUmemAllocationGranularity_flags) = nullptr;
+    CUresult (*addressReserve)(CUdeviceptr *, size_t, size_t, CUdeviceptr, unsigned long long) = nullptr;
+    CUresult (*addressFree)(CUdeviceptr, size_t) = nullptr;
+    CUresult (*create)(CUmemGenericAllocationHandle *, size_t, const CUmemAllocationProp *, unsigned long long) = nullptr;
+    CUresult (*release)(CUmemGenericAllocationHandle) = nullptr;
+    CUresult (*map)(CUdeviceptr, size_t, size_t, CUmemGenericAllocationHandle, unsigned long long) = nullptr;
+    CUresult (*unmap)(CUdeviceptr, size_t) = nullptr;
+    CUresult (*setAccess)(CUdeviceptr, size_t, const CUmemAccessDesc *, size_t) = nullptr;
+    bool ok = false;
+};
+
+static DriverVmm &driver() {
+    static DriverVmm d;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        auto get = [](const char *name, void **fn) {
+            cudaDriverEntryPointQueryResult q;
+            return cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) ==
+                       cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess && *fn != nullptr;
+        };
+        bool ok = true;
+        ok &= get("cuMemGetAllocationGranularity", (void **)&d.getGranularity);
+        ok &= get("cuMemAddressReserve", (void **)&d.addressReserve);
+        ok &= get("cuMemAddressFree", (void **)&d.addressFree);
+        ok &= get("cuMemCreate", (void **)&d.create);
+        ok &= get("cuMemRelease", (void **)&d.release);
+        ok &= get("cuMemMap", (void **)&d.map);
+        ok &= get("cuMemUnmap", (void **)&d.unmap);
+        ok &= get("cuMemSetAccess", (void **)&d.setAccess);
+        d.ok = ok;
+    });
+    return d;
+}
+
+// Writes new tokens at (request, position) of the contiguous layout.
+__global__ void __launch_bounds__(256) contig_append_kernel(
+    const unsigned long long *__restrict__ k_bases, const unsigned long long *__restrict__ v_bases,
+    const long long *__restrict__ mapped, const uint4 *__restrict__ k_new,
+    const uint4 *__restrict__ v_new, const int32_t *__restrict__ req_ids,
+    const int32_t *__restrict__ positions, long long total_chunks, int hkv, int row_chunks,
+    long long head_stride, int max_requests, int *err) {
+    const int per_token = hkv * row_chunks;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total_chunks;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_token;
+        const int rem = (int)(i - t * per_token);
+        const int h = rem / row_chunks, c = rem - h * row_chunks;
+        const int req = __ldg(req_ids + t);
+        const int pos = __ldg(positions + t);
+        if (req < 0 || req >= max_requests || pos < 0 || (long long)pos >= mapped[req] ||
+            k_bases[req] == 0) {
+            if (rem == 0) atomicOr(err, KV_DEVERR_UNMAPPED);
+            continue;
+        }
+        const long long dst = ((long long)h * head_stride + pos) * row_chunks + c;
+        reinterpret_cast<uint4 *>(k_bases[req])[dst] = __ldg(k_new + i);
+        reinterpret_cast<uint4 *>(v_bases[req])[dst] = __ldg(v_new + i);
+    }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+struct kv_contig {
+    int max_requests = 0, max_tokens = 0, hkv = 0, head_dim = 0;
+    kv_dtype dtype = KV_BF16;
+    int device = 0;
+    size_t page = 0;            // bytes per physical page
+    long long head_stride = 0;  // tokens per head region
+    size_t head_bytes = 0;      // bytes per head region (a whole number of pages)
+    size_t region_bytes = 0;    // K (or V) region = hkv * head_bytes
+    size_t reserve_bytes = 0;   // 2 * region_bytes
+    long long tokens_per_page = 0;
+    struct Req {
+        CUdeviceptr base = 0;
+        std::vector<CUmemGenericAllocationHandle> pages;  // [2][hkv][pages_per_head], 0 = unmapped
+        long long pages_mapped = 0;                       // per head region
+    };
+    std::vector<Req> reqs;
+    long long pages_per_head = 0;
+    long long mapped_bytes = 0;
+    unsigned long long *d_kbase = nullptr;
+    unsigned long long *d_vbase = nullptr;
+    long long *d_mapped = nullptr;
+    int *err = nullptr;
+};
+
+static kv_status sync_request(kv_contig *c, int req) {
+    const kv_contig::Req &r = c->reqs[req];
+    const unsigned long long kb = r.base, vb = r.base ? r.base + c->region_bytes : 0;
+    const long long mt = r.pages_mapped * c->tokens_per_page;
+    if (cudaMemcpy(c->d_kbase + req, &kb, sizeof(kb), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->d_vbase + req, &vb, sizeof(vb), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->d_mapped + req, &mt, sizeof(mt), cudaMemcpyHostToDevice) != cudaSuccess)
+        return KV_ERR_CUDA;
+    return KV_OK;
+}
+
+extern "C" {
+
+kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, int head_dim,
+                           kv_dtype dtype, kv_contig_t *out) {
+    if (!out || max_requests <= 0 || max_tokens <= 0 || num_kv_heads <= 0) return KV_ERR_ARG;
+    if ((head_dim != 64 && head_dim != 128) || (dtype != KV_F32 && dtype != KV_BF16))
+        return KV_ERR_UNSUPPORTED;
+    DriverVmm &d = driver();
+    if (!d.ok) return KV_ERR_CUDA;
+    if (cudaFree(nullptr) != cudaSuccess) return KV_ERR_CUDA;  // make the primary context current
+    kv_contig *c = new (std::nothrow) kv_contig();
+    if (!c) return KV_ERR_OOM;
+    cudaGetDevice(&c->device);
+    c->max_requests = max_requests;
+    c->max_tokens = max_tokens;
+    c->hkv = num_kv_heads;
+    c->head_dim = head_dim;
+    c->dtype = dtype;
+    CUmemAllocationProp prop{};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = c->device;
+    if (d.getGranularity(&c->page, &prop, CU_MEM_ALLOC_GRANULARITY_MINIMUM) != CUDA_SUCCESS ||
+        c->page == 0) {
+        delete c;
+        return KV_ERR_CUDA;
+    }
+    const size_t tok_bytes = (size_t)head_dim * dtype_bytes(dtype);
+    if (c->page % (16 * tok_bytes) != 0) {
+        delete c;
+        return KV_ERR_UNSUPPORTED;
+    }
+    c->tokens_per_page = (long long)(c->page / tok_bytes);
+    c->pages_per_head = ((long long)max_tokens + c->tokens_per_page - 1) / c->tokens_per_page;
+    c->head_stride = c->pages_per_head * c->tokens_per_page;
+    c->head_bytes = (size_t)c->pages_per_head * c->page;
+    c->region_bytes = c->head_bytes * num_kv_heads;
+    c->reserve_bytes = 2 * c->region_bytes;
+    try {
+        c->reqs.resize(max_requests);
+    } catch (...) {
+        delete c;
+        return KV_ERR_OOM;
+    }
+    if (cudaMalloc(&c->d_kbase, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
+        cudaMalloc(&c->d_vbase, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
+        cudaMalloc(&c->d_mapped, sizeof(long long) * max_requests) != cudaSuccess ||
+        cudaMalloc(&c->err, sizeof(int)) != cudaSuccess ||
+        cudaMemset(c->d_kbase, 0, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
+        cudaMemset(c->d_vbase, 0, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
+        cudaMemset(c->d_mapped, 0, sizeof(long long) * max_requests) != cudaSuccess ||
+        cudaMemset(c->err, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        kv_contig_destroy(c);
+        return KV_ERR_OOM;
+    }
+    *out = c;
+    return KV_OK;
+}
+
+kv_status kv_contig_layout(kv_contig_t c, int64_t *head_stride, int64_t *page_bytes,
+                           int64_t *reserved_bytes_per_request) {
+    if (!c) return KV_ERR_ARG;
+    if (head_stride) *head_stride = c->head_stride;
+    if (page_bytes) *page_bytes = (int64_t)c->page;
+    if (reserved_bytes_per_request) *reserved_bytes_per_request = (int64_t)c->reserve_bytes;
+    return KV_OK;
+}
+
+kv_status kv_contig_reserve(kv_contig_t c, int req) {
+    if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    kv_contig::Req &r = c->reqs[req];
+    if (r.base) return KV_ERR_STATE;
+    DriverVmm &d = driver();
+    CUdeviceptr base = 0;
+    if (d.addressReserve(&base, c->reserve_bytes, c->page, 0, 0) != CUDA_SUCCESS) return KV_ERR_OOM;
+    try {
+        r.pages.assign((size_t)2 * c->hkv * c->pages_per_head, 0);
+    } catch (...) {
+        d.addressFree(base, c->reserve_bytes);
+        return KV_ERR_OOM;
+    }
+    r.base = base;
+    r.pages_mapped = 0;
+    return sync_request(c, req);
+}
+
+kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
+    if (!c || req < 0 || req >= c->max_requests || n_tokens < 0 || n_tokens > c->max_tokens)
+        return KV_ERR_ARG;
+    kv_contig::Req &r = c->reqs[req];
+    if (!r.base) return KV_ERR_STATE;
+    const long long need = (n_tokens + c->tokens_per_page - 1) / c->tokens_per_page;
+    if (need <= r.pages_mapped) return KV_OK;
+    DriverVmm &d = driver();
+    CUmemAllocationProp prop{};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = c->device;
+    CUmemAccessDesc access{};
+    access.location = prop.location;
+    access.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+    std::vector<size_t> made;  // page slots filled by this call (for undo)
+    kv_status st = KV_OK;
+    for (int kv = 0; kv < 2 && st == KV_OK; ++kv)
+        for (int h = 0; h < c->hkv && st == KV_OK; ++h)
+            for (long long k = r.pages_mapped; k < need; ++k) {
+                const size_t slot = ((size_t)kv * c->hkv + h) * c->pages_per_head + k;
+                const CUdeviceptr va = r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page;
+                CUmemGenericAllocationHandle hdl = 0;
+                if (d.create(&hdl, c->page, &prop, 0) != CUDA_SUCCESS) {
+                    st = KV_ERR_OOM;
+                    break;
+                }
+                if (d.map(va, c->page, 0, hdl, 0) != CUDA_SUCCESS) {
+                    d.release(hdl);
+                    st = KV_ERR_CUDA;
+                    break;
+                }
+                r.pages[slot] = hdl;
+                made.push_back(slot);
+                if (d.setAccess(va, c->page, &access, 1) != CUDA_SUCCESS) {
+                    st = KV_ERR_CUDA;
+                    break;
+                }
+            }
+    if (st != KV_OK) {
+        for (size_t slot : made) {
+            const size_t kv = slot / ((size_t)c->hkv * c->pages_per_head);
+            const size_t rem = slot % ((size_t)c->hkv * c->pages_per_head);
+            const size_t h = rem / c->pages_per_head, k = rem % c->pages_per_head;
+            d.unmap(r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page, c->page);
+            d.release(r.pages[slot]);
+            r.pages[slot] = 0;
+        }
+        return st;
+    }
+    c->mapped_bytes += (long long)made.size() * (long long)c->page;
+    r.pages_mapped = need;
+    return sync_request(c, req);
+}
+
+kv_status kv_contig_release(kv_contig_t c, int req) {
+    if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    kv_contig::Req &r = c->reqs[req];
+    if (!r.base) return KV_OK;
+    DriverVmm &d = driver();
+    kv_status st = KV_OK;
+    for (size_t slot = 0; slot < r.pages.size(); ++slot) {
+        if (!r.pages[slot]) continue;
+        const size_t kv = slot / ((size_t)c->hkv * c->pages_per_head);
+        const size_t rem = slot % ((size_t)c->hkv * c->pages_per_head);
+        const size_t h = rem / c->pages_per_head, k = rem % c->pages_per_head;
+        if (d.unmap(r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page, c->page) !=
+                CUDA_SUCCESS ||
+            d.release(r.pages[slot]) != CUDA_SUCCESS)
+            st = KV_ERR_CUDA;
+        r.pages[slot] = 0;
+        c->mapped_bytes -= (long long)c->page;
+    }
+    if (d.addressFree(r.base, c->reserve_bytes) != CUDA_SUCCESS) st = KV_ERR_CUDA;
+    r.base = 0;
+    r.pages_mapped = 0;
+    r.pages.clear();
+    kv_status s2 = sync_request(c, req);
+    return st != KV_OK ? st : s2;
+}
+
+kv_status kv_contig_destroy(kv_contig_t c) {
+    if (!c) return KV_ERR_ARG;
+    for (int r = 0; r < c->max_requests; ++r)
+        if (c->reqs[r].base && c->d_kbase) kv_contig_release(c, r);
+    if (c->d_kbase) cudaFree(c->d_kbase);
+    if (c->d_vbase) cudaFree(c->d_vbase);
+    if (c->d_mapped) cudaFree(c->d_mapped);
+    if (c->err) cudaFree(c->err);
+    delete c;
+    return KV_OK;
+}
+
+kv_status kv_contig_ptrs(kv_contig_t c, int req, void **k_base, void **v_base) {
+    if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    const kv_contig::Req &r = c->reqs[req];
+    if (!r.base) return KV_ERR_STATE;
+    if (k_base) *k_base = reinterpret_cast<void *>(r.base);
+    if (v_base) *v_base = reinterpret_cast<void *>(r.base + c->region_bytes);
+    return KV_OK;
+}
+
+kv_status kv_contig_stats(kv_contig_t c, int req, int64_t *mapped_tokens,
+                          int64_t *mapped_bytes_total) {
+    if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    if (mapped_tokens) *mapped_tokens = c->reqs[req].pages_mapped * c->tokens_per_page;
+    if (mapped_bytes_total) *mapped_bytes_total = c->mapped_bytes;
+    return KV_OK;
+}
+
+kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
+                           const int32_t *req_ids, const int32_t *positions, int num_tokens,
+                           void *stream) {
+    if (!c || num_tokens < 0) return KV_ERR_ARG;
+    if (num_tokens == 0) return KV_OK;
+    if (!k_new || !v_new || !req_ids || !positions) return KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+        return KV_ERR_ARG;
+    const int row_chunks = c->head_dim * dtype_bytes(c->dtype) / 16;
+    const long long total = (long long)num_tokens * c->hkv * row_chunks;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    contig_append_kernel<<<(int)blocks, 256, 0, as_stream(stream)>>>(
+        c->d_kbase, c->d_vbase, c->d_mapped, (const uint4 *)k_new, (const uint4 *)v_new, req_ids,
+        positions, total, c->hkv, row_chunks, c->head_stride, c->max_requests, c->err);
+    return cuda_status(cudaGetLastError());
+}
+
+kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *req_ids,
+                                  const int32_t *seq_lens, int batch, int num_q_heads,
+                                  float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                  int num_splits, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (!c || (batch > 0 && !req_ids)) return KV_ERR_ARG;
+    DecodeArgs a{};
+    a.q = q;
+    a.max_blocks = (c->max_tokens + 15) / 16;  // the split plan of an equal-width block table
+    a.k_bases = c->d_kbase;
+    a.v_bases = c->d_vbase;
+    a.req_ids = req_ids;
+    a.mapped_tokens = c->d_mapped;
+    a.head_stride = c->head_stride;
+    a.max_requests = c->max_requests;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = c->hkv;
+    a.head_dim = c->head_dim;
+    a.dtype = c->dtype;
+    a.scale = scale;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse_out;
+    a.num_splits = num_splits;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.err = c->err;
+    a.stream = as_stream(stream);
+    return launch_decode(a, true);
+}
+
+kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream) {
+    if (!c || !code) return KV_ERR_ARG;
+    int h = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&h, c->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (h != 0 && cudaMemsetAsync(c->err, 0, sizeof(int), s) != cudaSuccess) return KV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+    *code = h;
+    return device_error_status(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,202 @@
+"""CPU tests of the C ABI: the library builds and loads, exports every entry
+point the header declares, and its host-only logic (block accounting, free
+list, reference counts, copy-on-write planning) is right.  No GPU needed.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_196_gb300 as pk
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^(?:kv_status|const char\s*\*)\s*(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 30
+    L = pk.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding forwards each of them under the same name
+    assert not [n for n in names if not hasattr(pk, n)]
+
+
+def test_status_strings():
+    assert pk.kv_status_string(0) == "ok"
+    assert "argument" in pk.kv_status_string(-1)
+
+
+def test_worked_example_block_accounting():
+    # "PagedAttention Nedir?", "Nasil Calisir?": 35 tokens at 16 per block
+    # need 3 blocks and leave 13 slots unused.
+    assert pk.kv_blocks_for_tokens(35, 16) == (3, 13)
+    for n in range(0, 300, 7):
+        assert pk.kv_blocks_for_tokens(n, 16) == (oracle.blocks_needed(n, 16),
+                                                 oracle.unused_slots(n, 16))
+
+
+def test_allocator_free_list_and_refcounts():
+    a = pk.kv_allocator_create(8)
+    try:
+        assert pk.kv_allocator_num_free(a) == 8
+        ids = np.zeros(3, np.int32)
+        pk.kv_allocator_alloc(a, ids)
+        assert ids.tolist() == [0, 1, 2]
+        assert pk.kv_allocator_num_free(a) == 5
+        pk.kv_allocator_share(a, ids[:1])
+        assert pk.kv_allocator_refcount(a, 0) == 2
+        pk.kv_allocator_free(a, ids)          # 0 -> 1 ref, 1 and 2 -> free
+        assert pk.kv_allocator_refcount(a, 0) == 1
+        assert pk.kv_allocator_num_free(a) == 7
+        with pytest.raises(pk.KVError):        # double free
+            pk.kv_allocator_free(a, ids[1:2])
+        with pytest.raises(pk.KVError):        # sharing a free block
+            pk.kv_allocator_share(a, ids[1:2])
+        with pytest.raises(pk.KVError) as e:   # more than is free
+            pk.kv_allocator_alloc(a, np.zeros(8, np.int32))
+        assert e.value.status == -2
+        assert pk.kv_allocator_num_free(a) == 7
+        # freed blocks are reused after the never-used ones (FIFO)
+        more = np.zeros(7, np.int32)
+        pk.kv_allocator_alloc(a, more)
+        assert more.tolist() == [3, 4, 5, 6, 7, 1, 2]
+    finally:
+        pk.kv_allocator_destroy(a)
+
+
+def test_allocator_rejects_over_free_within_one_call():
+    a = pk.kv_allocator_create(4)
+    ids = np.zeros(1, np.int32)
+    pk.kv_allocator_alloc(a, ids)
+    with pytest.raises(pk.KVError):
+        pk.kv_allocator_free(a, np.array([0, 0], np.int32))
+    assert pk.kv_allocator_refcount(a, 0) == 1
+    pk.kv_allocator_destroy(a)
+
+
+def test_set_order_only_when_all_free():
+    a = pk.kv_allocator_create(4)
+    pk.kv_allocator_set_order(a, np.array([2, 0, 3, 1], np.int32))
+    ids = np.zeros(2, np.int32)
+    pk.kv_allocator_alloc(a, ids)
+    assert ids.tolist() == [2, 0]
+    with pytest.raises(pk.KVError) as e:
+        pk.kv_allocator_set_order(a, np.array([0, 1, 2, 3], np.int32))
+    assert e.value.status == -7
+    with pytest.raises(pk.KVError):
+        b = pk.kv_allocator_create(4)
+        try:
+            pk.kv_allocator_set_order(b, np.array([0, 0, 1, 2], np.int32))
+        finally:
+            pk.kv_allocator_destroy(b)
+    pk.kv_allocator_destroy(a)
+
+
+def _build_tables_with_library(lens, perm, max_blocks):
+    a = pk.kv_allocator_create(len(perm))
+    pk.kv_allocator_set_order(a, perm)
+    tables = np.full((len(lens), max_blocks), -1, np.int32)
+    slots = []
+    for b, L in enumerate(lens):
+        s = np.zeros(int(L), np.int64)
+        nb, ncow = pk.kv_prepare_append(a, tables[b], 0, 0, int(L), s, np.zeros(0, np.int32),
+                                        np.zeros(0, np.int32))
+        assert ncow == 0 and nb == oracle.blocks_needed(int(L), 16)
+        slots.append(s)
+    free = pk.kv_allocator_num_free(a)
+    pk.kv_allocator_destroy(a)
+    return tables, slots, free
+
+
+def test_block_tables_match_oracle_on_tiny_workload():
+    cfg = W.CONFIGS["tiny_fp32"]
+    lens = np.array(cfg["lens"], np.int32)
+    perm = W.permutation(W.rng(cfg["seed"]), cfg["num_blocks"])
+    tables, slots, free = _build_tables_with_library(lens, perm, 3)
+    np.testing.assert_array_equal(tables, oracle.build_block_tables(lens, 16, perm, 3))
+    assert free == 16 - 5
+    # slot of logical token j = table[j // 16] * 16 + j % 16
+    for b, L in enumerate(lens):
+        j = np.arange(L)
+        np.testing.assert_array_equal(slots[b], tables[b, j // 16].astype(np.int64) * 16 + j % 16)
+
+
+def test_block_tables_match_oracle_on_llama_shaped_workload():
+    lens = W.decode_lengths("llama3_8b_decode")
+    need = sum(oracle.blocks_needed(int(L), 16) for L in lens)
+    nb = int(np.ceil(1.2 * need))
+    perm = W.permutation(W.rng(77), nb)
+    tables, _, free = _build_tables_with_library(lens, perm, 256)
+    np.testing.assert_array_equal(tables, oracle.build_block_tables(lens, 16, perm, 256))
+    assert free == nb - need
+
+
+def test_prepare_append_grows_and_copies_shared_blocks_on_write():
+    a = pk.kv_allocator_create(16)
+    parent = np.full(4, -1, np.int32)
+    s = np.zeros(20, np.int64)
+    nb, _ = pk.kv_prepare_append(a, parent, 0, 0, 20, s, np.zeros(0, np.int32), np.zeros(0, np.int32))
+    assert nb == 2 and parent[:2].tolist() == [0, 1]
+    # fork: the child shares both blocks
+    child = parent.copy()
+    pk.kv_allocator_share(a, child[:2])
+    assert pk.kv_allocator_refcount(a, 1) == 2
+    # the child writes position 20 (inside shared block 1): copy-on-write
+    src, dst = np.zeros(2, np.int32), np.zeros(2, np.int32)
+    s1 = np.zeros(1, np.int64)
+    nb_c, ncow = pk.kv_prepare_append(a, child, 2, 20, 1, s1, src, dst)
+    assert (nb_c, ncow) == (2, 1)
+    assert src[0] == 1 and dst[0] == child[1] and child[1] not in (0, 1)
+    assert s1[0] == child[1] * 16 + 4
+    assert pk.kv_allocator_refcount(a, 1) == 1 and pk.kv_allocator_refcount(a, child[1]) == 1
+    assert child[0] == 0 and pk.kv_allocator_refcount(a, 0) == 2  # untouched block still shared
+    # the parent now owns block 1 alone: appending needs no copy
+    nb_p, ncow = pk.kv_prepare_append(a, parent, 2, 20, 13, np.zeros(13, np.int64), src, dst)
+    assert (nb_p, ncow) == (3, 0)
+    pk.kv_allocator_destroy(a)
+
+
+def test_prepare_append_failure_changes_nothing():
+    a = pk.kv_allocator_create(3)
+    row = np.full(8, -1, np.int32)
+    with pytest.raises(pk.KVError) as e:
+        pk.kv_prepare_append(a, row, 0, 0, 64, np.zeros(64, np.int64), np.zeros(0, np.int32),
+                             np.zeros(0, np.int32))
+    assert e.value.status == -2
+    assert row.tolist() == [-1] * 8 and pk.kv_allocator_num_free(a) == 3
+    with pytest.raises(pk.KVError) as e:  # table row too short
+        pk.kv_prepare_append(a, row[:1], 0, 0, 20, np.zeros(20, np.int64), np.zeros(0, np.int32),
+                             np.zeros(0, np.int32))
+    assert e.value.status == -1
+    # a shared block with no room to report the copy is an argument error
+    nb, _ = pk.kv_prepare_append(a, row, 0, 0, 5, np.zeros(5, np.int64), np.zeros(0, np.int32),
+                                 np.zeros(0, np.int32))
+    pk.kv_allocator_share(a, row[:1])
+    with pytest.raises(pk.KVError):
+        pk.kv_prepare_append(a, row, nb, 5, 1, np.zeros(1, np.int64), np.zeros(0, np.int32),
+                             np.zeros(0, np.int32))
+    assert pk.kv_allocator_refcount(a, row[0]) == 2
+    pk.kv_allocator_destroy(a)
+
+
+def test_split_plan_and_workspace():
+    pb, ms = pk.kv_decode_split_plan(64, 8, 256, 4)
+    assert pb * ms >= 256 and pb % 4 == 0 and ms == -(-256 // pb)
+    assert pk.kv_decode_workspace_size(64, 32, 8, 128, 256, 1) == 0
+    ws = pk.kv_decode_workspace_size(64, 32, 8, 128, 256, 4)
+    assert ws == 64 * 32 * ms * 129 * 4

@@ -1,0 +1,158 @@
+"""Contiguous (vAttention-style) path on the GPU: virtual ranges reserved per
+request, physical pages mapped on demand, the same decode maths without a
+block table.  Checked against the oracle's linear-layout decode and, bit for
+bit, against the paged path on the same logical data and split plan."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_196_gb300 as pk
+import workloads as W
+from _gpu import assert_close_scaled, dev, host, pool_views, read_linear, require_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+class ContigCase:
+    def __init__(self, lens, max_tokens, hq, hkv, d, dtype, seed, req_order=None):
+        require_cuda()
+        self.bf16 = dtype == "bf16"
+        self.lens = np.asarray(lens, np.int32)
+        self.B, self.hq, self.hkv, self.d, self.max_tokens = len(lens), hq, hkv, d, max_tokens
+        g = W.rng(seed)
+        # logical content per sequence
+        self.K = [W.normal(g, (int(L), hkv, d), dtype) for L in lens]
+        self.V = [W.normal(g, (int(L), hkv, d), dtype) for L in lens]
+        self.q = W.normal(g, (self.B, hq, d), dtype)
+        self.req = np.asarray(req_order if req_order is not None else np.arange(self.B), np.int32)
+        self.ctx = pk.kv_contig_create(self.B + 2, max_tokens, hkv, d,
+                                       pk.KV_BF16 if self.bf16 else pk.KV_F32)
+        self.head_stride, self.page, self.reserved = pk.kv_contig_layout(self.ctx)
+        for b, L in enumerate(lens):
+            r = int(self.req[b])
+            pk.kv_contig_reserve(self.ctx, r)
+            pk.kv_contig_ensure(self.ctx, r, int(L))
+            if L:
+                pos = np.arange(L, dtype=np.int32)
+                pk.kv_contig_append(self.ctx, dev(self.K[b]), dev(self.V[b]),
+                                    dev(np.full(L, r, np.int32)), dev(pos), int(L))
+        torch.cuda.synchronize()
+        assert pk.kv_contig_get_device_error(self.ctx) == 0
+
+    def run(self, splits=0):
+        out = torch.empty((self.B, self.hq, self.d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((self.B, self.hq), dtype=torch.float32, device="cuda")
+        maxb = -(-self.max_tokens // 16)
+        wsb = pk.kv_decode_workspace_size(self.B, self.hq, self.hkv, self.d, maxb, splits)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+        pk.contig_decode_attention(self.ctx, dev(self.q), dev(self.req), dev(self.lens), self.B,
+                                   self.hq, 1 / math.sqrt(self.d), out, pk.KV_F32, lse, splits,
+                                   ws, wsb)
+        torch.cuda.synchronize()
+        assert pk.kv_contig_get_device_error(self.ctx) == 0
+        return host(out).astype(np.float64), host(lse).astype(np.float64)
+
+    def oracle_linear(self):
+        # The oracle's linear-layout decode on the generated logical content
+        # (one [Hkv][L][D] buffer per sequence); nothing is read back from the GPU.
+        n = max(1, int(self.lens.max()))
+        kb, vb = [], []
+        for k, v in zip(self.K, self.V):
+            kp = np.zeros((self.hkv, n, self.d), k.dtype)
+            vp = np.zeros((self.hkv, n, self.d), v.dtype)
+            kp[:, :len(k)] = k.transpose(1, 0, 2)
+            vp[:, :len(v)] = v.transpose(1, 0, 2)
+            kb.append(kp)
+            vb.append(vp)
+        return oracle.linear_decode(kb, vb, np.arange(self.B), self.lens, self.q,
+                                    1 / math.sqrt(self.d))
+
+    def close(self):
+        pk.kv_contig_destroy(self.ctx)
+
+
+def test_contig_append_lands_at_linear_positions():
+    c = ContigCase([35, 17, 0], 100, hq=4, hkv=2, d=64, dtype="f32", seed=40)
+    for b, L in enumerate(c.lens):
+        k_ptr, _ = pk.kv_contig_ptrs(c.ctx, int(c.req[b]))
+        got = read_linear(k_ptr, c.hkv, c.head_stride, int(L), c.d, False)
+        np.testing.assert_array_equal(got, c.K[b].transpose(1, 0, 2))
+    c.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_contig_decode_matches_oracle(dtype):
+    c = ContigCase([35, 17, 1, 300, 0, 1000], 1024, hq=16, hkv=2, d=128, dtype=dtype, seed=41,
+                   req_order=[3, 0, 5, 1, 2, 4])
+    ref, ref_lse = c.oracle_linear()
+    for splits in (1, 3, 0):
+        out, lse = c.run(splits)
+        assert_close_scaled(out, ref, 1e-5 if dtype == "f32" else 2e-3, f"splits={splits}")
+    c.close()
+
+
+def test_contig_equals_paged_bit_for_bit():
+    lens = [35, 17, 1, 300, 777, 64]
+    c = ContigCase(lens, 800, hq=16, hkv=4, d=128, dtype="bf16", seed=42)
+    # the same logical data in a shuffled paged pool
+    need = sum(oracle.blocks_needed(L, 16) for L in lens)
+    perm = W.permutation(W.rng(43), need + 5)
+    maxb = -(-800 // 16)
+    tables = oracle.build_block_tables(np.array(lens, np.int32), 16, perm, maxb)
+    pool = pk.kv_pool_create(need + 5, 16, 4, 128, pk.KV_BF16)
+    kv, vv = pool_views(pool, need + 5, 4, 128, True)
+    kv.zero_(); vv.zero_()
+    for b, L in enumerate(lens):
+        j = np.arange(L)
+        slots = (tables[b, j // 16].astype(np.int64) * 16 + j % 16)
+        pk.kv_append(pool, dev(c.K[b]), dev(c.V[b]), dev(slots), L)
+    for splits in (1, 4, 0):
+        out_c, lse_c = c.run(splits)
+        out_p = torch.empty((len(lens), 16, 128), dtype=torch.float32, device="cuda")
+        lse_p = torch.empty((len(lens), 16), dtype=torch.float32, device="cuda")
+        wsb = pk.kv_decode_workspace_size(len(lens), 16, 4, 128, maxb, splits)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+        pk.paged_decode_attention(pool, dev(c.q), dev(tables), maxb, dev(np.array(lens, np.int32)),
+                                  len(lens), 16, 1 / math.sqrt(128), out_p, pk.KV_F32, lse_p,
+                                  splits, ws, wsb)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(out_p), out_c.astype(np.float32))
+        np.testing.assert_array_equal(host(lse_p), lse_c.astype(np.float32))
+    pk.kv_pool_destroy(pool)
+    c.close()
+
+
+def test_pages_are_mapped_on_demand_and_released():
+    require_cuda()
+    ctx = pk.kv_contig_create(4, 100000, 4, 128, pk.KV_BF16)
+    head_stride, page, reserved = pk.kv_contig_layout(ctx)
+    tpp = page // (128 * 2)                                  # tokens per page
+    assert head_stride % tpp == 0 and head_stride >= 100000
+    assert reserved == 2 * 4 * head_stride * 128 * 2
+    pk.kv_contig_reserve(ctx, 1)
+    assert pk.kv_contig_stats(ctx, 1) == (0, 0)              # reserving maps nothing
+    pk.kv_contig_ensure(ctx, 1, 1)
+    assert pk.kv_contig_stats(ctx, 1) == (tpp, 2 * 4 * page)
+    pk.kv_contig_ensure(ctx, 1, tpp + 1)
+    assert pk.kv_contig_stats(ctx, 1) == (2 * tpp, 2 * 2 * 4 * page)
+    pk.kv_contig_ensure(ctx, 1, 5)                          # never shrinks
+    assert pk.kv_contig_stats(ctx, 1)[0] == 2 * tpp
+    with pytest.raises(pk.KVError):
+        pk.kv_contig_reserve(ctx, 1)                         # already reserved
+    with pytest.raises(pk.KVError):
+        pk.kv_contig_ensure(ctx, 2, 10)                      # not reserved
+    with pytest.raises(pk.KVError):
+        pk.kv_contig_ensure(ctx, 1, 100001)                  # beyond max_tokens
+    # a write past the mapped range is skipped and flagged, not faulted
+    k = np.zeros((1, 4, 128), np.uint16)
+    pk.kv_contig_append(ctx, dev(k), dev(k), dev(np.array([1], np.int32)),
+                        dev(np.array([2 * tpp], np.int32)), 1)
+    torch.cuda.synchronize()
+    assert pk.kv_contig_get_device_error(ctx) == 0x8
+    pk.kv_contig_release(ctx, 1)
+    assert pk.kv_contig_stats(ctx, 1) == (0, 0)
+    pk.kv_contig_reserve(ctx, 1)                             # reusable after release
+    pk.kv_contig_destroy(ctx)
