@@ -200,6 +200,28 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
                                  float *lse_out, int num_splits, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* paged_decode_attention without a workspace argument, for callers that
+ * cannot allocate device memory where they run decode (a plugin whose host
+ * framework owns all device memory; a serving loop that must not call
+ * cudaMalloc after start-up).  The pages have no counterpart: this is a
+ * packaging choice of this library.
+ *
+ * Same arguments, maths and results as paged_decode_attention with the same
+ * num_splits.  The split-KV partial results live in one fixed 8 MiB array in
+ * the library's device image (held on every GPU that loads the library until
+ * the process exits).  A split plan needing more scratch than that
+ * (kv_decode_workspace_size > 8 MiB) returns KV_ERR_UNSUPPORTED and launches
+ * nothing.  The call itself allocates nothing.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the array: calls whose kernels overlap on the GPU (unordered streams) race
+ * and give undefined results.  Nothing in the array has to start at zero. */
+kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32_t *block_tables,
+                                         int max_blocks, const int32_t *seq_lens, int batch,
+                                         int num_q_heads, float scale, void *out,
+                                         kv_dtype out_dtype, float *lse_out, int num_splits,
+                                         void *stream);
+
 /* Chunked causal paged prefill ("Makale Bulteni -- vAttention", "Iddia ve
  * Gerceklik": the prefill kernels are where paging costs most).  Sequence b
  * holds seq_lens[b] tokens in the cache, the last T_b = cu_q[b+1] - cu_q[b]

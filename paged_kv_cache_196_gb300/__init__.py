@@ -21,7 +21,7 @@ __all__ = [
     "kv_allocator_num_free", "kv_prepare_append", "kv_pool_create", "kv_pool_destroy",
     "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks",
     "kv_decode_workspace_size", "kv_decode_split_plan", "paged_decode_attention",
-    "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
+    "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_append", "contig_decode_attention",
     "kv_contig_get_device_error",
@@ -67,6 +67,8 @@ _SIGS = {
     "kv_decode_split_plan": [_i32, _i32, _i32, _i32, _P(_i32), _P(_i32)],
     "paged_decode_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32,
                                _vp, _sz, _vp],
+    "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
+                                       _vp, _i32, _vp],
     "paged_prefill_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                 _vp, _vp],
     "kv_get_device_error": [_vp, _P(_i32), _vp],
@@ -257,6 +259,19 @@ def paged_decode_attention(p: int, q, block_tables, max_blocks: int, seq_lens, b
                                         _ptr(lse_out), num_splits, _ptr(workspace),
                                         workspace_bytes, _stream(stream)),
            "paged_decode_attention")
+
+
+def paged_decode_attention_noalloc(p: int, q, block_tables, max_blocks: int, seq_lens,
+                                   batch: int, num_q_heads: int, scale: float, out,
+                                   out_dtype: int, lse_out=None, num_splits: int = 0,
+                                   stream=None):
+    """paged_decode_attention with the split scratch in the library's fixed
+    device array (for callers that cannot allocate); see the C header."""
+    _check(lib().paged_decode_attention_noalloc(p, _ptr(q), _ptr(block_tables), max_blocks,
+                                                _ptr(seq_lens), batch, num_q_heads, scale,
+                                                _ptr(out), out_dtype, _ptr(lse_out), num_splits,
+                                                _stream(stream)),
+           "paged_decode_attention_noalloc")
 
 
 def paged_prefill_attention(p: int, q, cu_q, max_q_len: int, block_tables, max_blocks: int,

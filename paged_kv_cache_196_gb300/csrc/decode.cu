@@ -30,6 +30,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -652,6 +653,71 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
     a.err = p->err;
     a.stream = as_stream(stream);
     return launch_decode(a, false);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided scratch.
+//
+// Some callers cannot allocate device memory at the point where they run
+// decode: a plugin inside a host framework that owns all device memory, or a
+// serving loop that must not call cudaMalloc after start-up (it can
+// synchronise the device and stall other streams).  For them the split-KV
+// partial results go to one fixed array that lives in the library's device
+// image instead of a caller-supplied workspace.
+//
+// The array is kStaticScratchBytes (8 MiB) per device and stays resident on
+// every GPU that loads the library until the process exits.  In host code
+// the array's name is only a host-side stand-in; its device address is looked
+// up once per device with cudaGetSymbolAddress (with that device current) on
+// the first call, so that first call should come before any stream capture.
+// Every call shares the array: calls that overlap on the GPU (different
+// streams without ordering) race on it.  Nothing in it needs to start at zero:
+// each split writes its partial result before the merge reads it.
+// ---------------------------------------------------------------------------
+namespace pkv {
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+constexpr int kStaticMaxDevices = 64;
+static __device__ __align__(256) float g_decode_scratch[kStaticScratchBytes / sizeof(float)];
+
+static kv_status static_scratch(void **ptr) {
+    static std::mutex mu;
+    static void *addr[kStaticMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+    if (dev < 0 || dev >= kStaticMaxDevices) return KV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return KV_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return KV_OK;
+}
+}  // namespace pkv
+
+extern "C" {
+
+kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32_t *block_tables,
+                                         int max_blocks, const int32_t *seq_lens, int batch,
+                                         int num_q_heads, float scale, void *out,
+                                         kv_dtype out_dtype, float *lse_out, int num_splits,
+                                         void *stream) {
+    if (!p || batch < 0 || num_q_heads <= 0 || max_blocks < 0) return KV_ERR_ARG;
+    int pb = 0, ms = 0;
+    split_plan(batch, p->num_kv_heads, max_blocks, num_splits, &pb, &ms);
+    const size_t need = decode_workspace_bytes(batch, num_q_heads, p->head_dim, ms);
+    if (need > kStaticScratchBytes) return KV_ERR_UNSUPPORTED;  // beyond the fixed scratch array
+    void *ws = nullptr;
+    if (need > 0) {
+        const kv_status st = static_scratch(&ws);
+        if (st != KV_OK) return st;
+    }
+    return paged_decode_attention(p, q, block_tables, max_blocks, seq_lens, batch, num_q_heads,
+                                  scale, out, out_dtype, lse_out, num_splits, ws,
+                                  need > 0 ? kStaticScratchBytes : 0, stream);
 }
 
 }  // extern "C"
