@@ -37,11 +37,23 @@
 
 namespace pkv {
 
-constexpr int kNW = 4;                   // consumer warps per CTA
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 8
+#endif
+#ifndef PKV_DECODE_MINB
+#define PKV_DECODE_MINB 3
+#endif
+#ifndef PKV_DECODE_HS8
+#define PKV_DECODE_HS8 2
+#endif
+constexpr int kNW = PKV_DECODE_WARPS;    // consumer warps per CTA
 constexpr int kDecodeThreads = (kNW + 1) * 32;
 constexpr int kBS = 16;                  // tokens per block
 constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
-constexpr int kNStage = 8;               // pipeline depth (a multiple of kNW)
+constexpr int kNStage = PKV_DECODE_STAGES;  // pipeline depth (a multiple of kNW)
 static_assert(kNStage % kNW == 0, "each stage must belong to one consumer warp");
 
 struct DecodeKParams {
@@ -141,7 +153,7 @@ constexpr size_t decode_ring_bytes() {
 // lane carries all G heads.  HS = 2: both halves take the same token and each
 // carries G/2 heads (half the q and accumulator registers, for large G).
 template <int D, int G, int HS, bool BF16, bool LINEAR>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeKParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel(const DecodeKParams p) {
     using S = TileShape<D, BF16>;
     constexpr int kTile = S::kBytes;
     constexpr int kPairs = S::kPairs;
@@ -297,6 +309,8 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeKPar
         int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
         if (!stage_valid[st]) ntok = 0;
 
+        const bool full_block = ntok == kBS;  // uniform across the warp
+
         // ---- scores for this lane's head
         float s[kPasses];
 #pragma unroll
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeKPar
                 part[j] = a2.x + a2.y;
             }
             reduce_scatter16<GH, 8>(part, c);
-            s[pass] = t < ntok ? part[0] : -INFINITY;
+            s[pass] = (full_block || t < ntok) ? part[0] : -INFINITY;
         }
 
         // ---- online softmax update for this lane's head
@@ -345,21 +359,37 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeKPar
 #pragma unroll
             for (int m = 0; m < kPairs; ++m) acc[j][m] = __fmul2_rn(acc[j][m], a2);
         }
+        if (full_block) {
 #pragma unroll
-        for (int pass = 0; pass < kPasses; ++pass) {
-            const int t = HS == 1 ? 2 * pass + hf : pass;
-            float2 vx[kPairs];
-            load_row<D, BF16>(vt, t, c, vx);
-            if (t >= ntok) {  // skip, never multiply: the unused slots may hold anything
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const int t = HS == 1 ? 2 * pass + hf : pass;
+                float2 vx[kPairs];
+                load_row<D, BF16>(vt, t, c, vx);
+                const float2 *prow = pw + t * G + hoff;
 #pragma unroll
-                for (int m = 0; m < kPairs; ++m) vx[m] = make_float2(0.f, 0.f);
+                for (int j = 0; j < GH; ++j) {
+                    const float2 pj = prow[j];
+#pragma unroll
+                    for (int m = 0; m < kPairs; ++m) acc[j][m] = ffma2(pj, vx[m], acc[j][m]);
+                }
             }
-            const float2 *prow = pw + t * G + hoff;
+        } else {
+            // Partial or invalid block: tokens at or past ntok are skipped, never
+            // multiplied by a zero weight -- the unused slots may hold anything.
 #pragma unroll
-            for (int j = 0; j < GH; ++j) {
-                const float2 pj = prow[j];
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const int t = HS == 1 ? 2 * pass + hf : pass;
+                if (t < ntok) {
+                    float2 vx[kPairs];
+                    load_row<D, BF16>(vt, t, c, vx);
+                    const float2 *prow = pw + t * G + hoff;
 #pragma unroll
-                for (int m = 0; m < kPairs; ++m) acc[j][m] = ffma2(pj, vx[m], acc[j][m]);
+                    for (int j = 0; j < GH; ++j) {
+                        const float2 pj = prow[j];
+#pragma unroll
+                        for (int m = 0; m < kPairs; ++m) acc[j][m] = ffma2(pj, vx[m], acc[j][m]);
+                    }
+                }
             }
         }
         __syncwarp();
@@ -482,13 +512,13 @@ void split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits, int
     } else if (num_splits > 0) {
         pb = (max_blocks + num_splits - 1) / num_splits;
     } else {
-        // Aim for about 8 CTAs per SM over the widest possible table.
-        const long long units = (long long)batch * num_kv_heads;
-        const long long target = 8LL * sm_count();
-        long long want = (target + units - 1) / units;
-        if (want < 1) want = 1;
-        pb = (int)((max_blocks + want - 1) / want);
-        if (pb < 16) pb = 16;
+        // Partitions sized so the widest possible tables would give about 16
+        // CTAs per SM: real lengths are shorter, and small partitions keep
+        // the last wave short.  At least 32 blocks (512 tokens) each.
+        const long long work = (long long)batch * num_kv_heads * max_blocks;
+        const long long target = 16LL * sm_count();
+        pb = (int)((work + target - 1) / target);
+        if (pb < 32) pb = 32;
     }
     pb = (pb + kNW - 1) / kNW * kNW;
     if (pb > kMaxPartBlocks) pb = kMaxPartBlocks;
@@ -513,7 +543,7 @@ template <int D, int G, bool BF16, bool LINEAR>
 static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
     const size_t smem = decode_smem_bytes<D, G, BF16, LINEAR>(kp.part_blocks);
     // Large head groups split their heads across the two half-warps (register pressure).
-    constexpr int HS = (G >= 8 && D == 128) ? 2 : 1;
+    constexpr int HS = (G >= 8 && D == 128) ? PKV_DECODE_HS8 : 1;
     auto fn = decode_kernel<D, G, HS, BF16, LINEAR>;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
