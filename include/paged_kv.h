@@ -228,14 +228,21 @@ kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32
  * of which are the new chunk (already appended with kv_append).  Query row
  * r = cu_q[b] + i sits at position (seq_lens[b] - T_b) + i and attends keys
  * 0..(seq_lens[b] - T_b) + i.  QK^T and PV run on the tcgen05 tensor cores
- * with fp32 accumulation in tensor memory.  Requires dtype KV_BF16 and
+ * (bf16 operands, fp32 accumulation in tensor memory; the softmax weights are
+ * rounded to bf16 for the PV product).  Requires pool dtype KV_BF16 and
  * head_dim 128.
- *   q        device [cu_q[batch]][num_q_heads][head_dim];
- *   cu_q     device int32[batch + 1], cu_q[0] = 0, non-decreasing;
+ *   q         device [total_q][num_q_heads][head_dim], bf16;
+ *   cu_q      device int32[batch + 1], cu_q[0] = 0, non-decreasing, cu_q[batch]
+ *             <= total_q;
+ *   total_q   host: rows of q and out;
  *   max_q_len host: max_b T_b (sizes the grid);
- *   out      device [cu_q[batch]][num_q_heads][head_dim] of out_dtype;
- *   lse_out  device fp32[cu_q[batch]][num_q_heads] or NULL. */
-kv_status paged_prefill_attention(kv_pool_t p, const void *q, const int32_t *cu_q,
+ *   out       device [total_q][num_q_heads][head_dim] of out_dtype; rows not
+ *             covered by any chunk are left untouched;
+ *   lse_out   device fp32[total_q][num_q_heads] or NULL.
+ * A sequence with seq_lens[b] < T_b, seq_lens[b] > max_blocks*16 or a chunk
+ * past total_q is skipped and sets KV_DEVERR_BLOCK_RANGE; so does an
+ * out-of-range block id (its keys read as zeros). */
+kv_status paged_prefill_attention(kv_pool_t p, const void *q, const int32_t *cu_q, int total_q,
                                   int max_q_len, const int32_t *block_tables, int max_blocks,
                                   const int32_t *seq_lens, int batch, int num_q_heads,
                                   float scale, void *out, kv_dtype out_dtype, float *lse_out,

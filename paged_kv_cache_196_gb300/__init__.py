@@ -69,8 +69,8 @@ _SIGS = {
                                _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _vp, _i32, _vp],
-    "paged_prefill_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
-                                _vp, _vp],
+    "paged_prefill_attention": [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
+                                _i32, _vp, _vp],
     "kv_get_device_error": [_vp, _P(_i32), _vp],
     "kv_contig_create": [_i32, _i32, _i32, _i32, _i32, _P(_vp)],
     "kv_contig_destroy": [_vp],
@@ -274,12 +274,13 @@ def paged_decode_attention_noalloc(p: int, q, block_tables, max_blocks: int, seq
            "paged_decode_attention_noalloc")
 
 
-def paged_prefill_attention(p: int, q, cu_q, max_q_len: int, block_tables, max_blocks: int,
-                            seq_lens, batch: int, num_q_heads: int, scale: float, out,
-                            out_dtype: int, lse_out=None, stream=None):
-    _check(lib().paged_prefill_attention(p, _ptr(q), _ptr(cu_q), max_q_len, _ptr(block_tables),
-                                         max_blocks, _ptr(seq_lens), batch, num_q_heads, scale,
-                                         _ptr(out), out_dtype, _ptr(lse_out), _stream(stream)),
+def paged_prefill_attention(p: int, q, cu_q, total_q: int, max_q_len: int, block_tables,
+                            max_blocks: int, seq_lens, batch: int, num_q_heads: int, scale: float,
+                            out, out_dtype: int, lse_out=None, stream=None):
+    _check(lib().paged_prefill_attention(p, _ptr(q), _ptr(cu_q), total_q, max_q_len,
+                                         _ptr(block_tables), max_blocks, _ptr(seq_lens), batch,
+                                         num_q_heads, scale, _ptr(out), out_dtype, _ptr(lse_out),
+                                         _stream(stream)),
            "paged_prefill_attention")
 
 

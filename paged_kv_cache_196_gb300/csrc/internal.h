@@ -1,5 +1,6 @@
 // Internal host-side definitions shared by the library's translation units.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -16,6 +17,10 @@ struct kv_pool {
     void *v = nullptr;
     int *err = nullptr;  // device error word
     kv_allocator_t alloc = nullptr;
+    // tiled-TMA descriptors of the K and V pools (built on first prefill)
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    bool tmaps_ready = false;
 };
 
 namespace pkv {
