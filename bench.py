@@ -47,7 +47,10 @@ DESCR = {
                         "32q/4kv heads, head_dim 128, bf16, split-KV + LSE merge",
     "yi6b_long_decode_contig": "Yi-6B-shaped long-context decode on the contiguous "
                                "(cuMemMap-backed) KV path, same inputs as yi6b_long_decode",
+    "yi34b_prefill": "Yi-34B-shaped chunked causal paged prefill: 4 seqs x (8192 cached + 2048 "
+                     "new) tokens in shuffled 16-token blocks, 56q/8kv heads, head_dim 128, bf16",
 }
+PREFILL_METRIC = "chunked causal paged prefill tensor TFLOP/s (fraction of dense bf16 peak)"
 
 
 def log(*a):
@@ -481,6 +484,117 @@ def run_reference(args):
     }
 
 
+def read_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, rank, world, local_rank):
+    """One prefill step: append the chunk's K/V through the slot mapping, then
+    chunked causal paged prefill attention of the chunk's queries."""
+    import torch
+
+    import paged_kv_cache_196_gb300 as pk
+
+    torch.cuda.set_device(local_rank)
+    cfg = W.CONFIGS["yi34b_prefill"]
+    B, hq, hkv, d = cfg["batch"], cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    c_len, t_len = cfg["cached_len"], cfg["chunk_len"]
+    L = c_len + t_len
+    max_blocks = (L + 15) // 16
+    nb = int(math.ceil(cfg["pool_factor"] * B * max_blocks))
+    t0 = time.time()
+    inp = W.prefill_inputs("yi34b_prefill", nb)
+    log(f"[bench] generated yi34b_prefill inputs in {time.time() - t0:.1f}s")
+    lens = np.full(B, L, np.int32)
+    alloc = pk.kv_allocator_create(nb)
+    pk.kv_allocator_set_order(alloc, inp["perm"])
+    tables = np.full((B, max_blocks), -1, np.int32)
+    slots = []
+    for b in range(B):
+        s = np.zeros(L, np.int64)
+        pk.kv_prepare_append(alloc, tables[b], 0, 0, L, s, np.zeros(0, np.int32),
+                             np.zeros(0, np.int32))
+        slots.append(s[c_len:])
+    pk.kv_allocator_destroy(alloc)
+    slots = np.concatenate(slots)
+    pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+    kp, vp = pk.kv_pool_ptrs(pool)
+    _fill(kp, torch.from_numpy(inp["pool_k"].view(np.int16)))
+    _fill(vp, torch.from_numpy(inp["pool_v"].view(np.int16)))
+    T = B * t_len
+    q = torch.from_numpy(inp["q"].view(np.int16)).cuda()
+    k_new = torch.from_numpy(inp["k_new"].view(np.int16)).cuda()
+    v_new = torch.from_numpy(inp["v_new"].view(np.int16)).cuda()
+    d_slots = torch.from_numpy(slots).cuda()
+    d_tables = torch.from_numpy(tables).cuda()
+    d_lens = torch.from_numpy(lens).cuda()
+    cu = torch.from_numpy(np.arange(0, T + 1, t_len, dtype=np.int32)).cuda()
+    out = torch.empty((T, hq, d), dtype=torch.int16, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    pairs = B * hq * (t_len * c_len + t_len * (t_len + 1) // 2)
+    flops = 4 * d * pairs
+
+    def append():
+        pk.kv_append(pool, k_new, v_new, d_slots, T)
+
+    def attend():
+        pk.paged_prefill_attention(pool, q, cu, T, t_len, d_tables, max_blocks, d_lens, B, hq,
+                                   scale, out, pk.KV_BF16, None)
+
+    for _ in range(args.warmup):
+        append()
+        attend()
+    torch.cuda.synchronize()
+    if pk.kv_get_device_error(pool):
+        raise RuntimeError("device error word set after warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        append()
+        ev[i][0].record()
+        attend()
+        ev[i][1].record()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    if pk.kv_get_device_error(pool):
+        raise RuntimeError("device error word set after the timed region")
+    peak, kind = read_tensor_peak()
+    achieved = flops / (attend_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(flops * K / (total_ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR["yi34b_prefill"], "name": "yi34b_prefill",
+                   "flop_per_step": flops, "append_tokens_per_step": T,
+                   "l2": "KV 168 MB + Q 117 MB per step, larger than L2; no flush"},
+        "prefill_tokens_per_s": round(T * K / (total_ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention (prefill_kernel)",
+                     "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": f"{kind} dense bf16 (cuBLAS burst)", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_flop_per_launch": flops, "avg_launch_ms": round(attend_ms, 4)},
+        "gpu_launches": 2 * K, "clocks": clk,
+    }
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -501,6 +615,10 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return  # the reference arm runs on rank 0 only
+        if args.workload == "yi34b_prefill":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the reference arm times the decode workloads only"}), flush=True)
+            return
         print(json.dumps(run_reference(args)), flush=True)
         return
 
@@ -510,7 +628,10 @@ def main():
 
         torch.cuda.set_device(local_rank)
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    line = run_ours(args, rank, world, local_rank)
+    if args.workload == "yi34b_prefill":
+        line = run_prefill(args, rank, world, local_rank)
+    else:
+        line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

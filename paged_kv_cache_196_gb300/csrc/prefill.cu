@@ -53,6 +53,14 @@ constexpr int kPfBarOff = kPfVOff + 2 * kPfTileBytes; // 160 KiB
 constexpr int kPfSmemBytes = kPfBarOff + 256 + 1024;  // barriers, slot, alignment slack
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
+// 2^x with the hardware approximation (relative error ~2^-22, far below the
+// bf16 rounding the weights get next); -inf gives 0.
+KV_DEVICE float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // TMEM column map
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
 
@@ -264,38 +272,43 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int s = j & 1;
             if (!mbar_wait(&bars->sfull[s], (j >> 1) & 1, p.err)) { ok = false; break; }
             tc::fence_after_sync();
-            float t[128];
+            // S row: four 32-column loads in flight, one wait.
+            uint32_t sv[128];
             {
-                uint32_t v[32];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    tc::tmem_ld32(tmem + lane_base + (s ? kColS1 : kColS0) + 32 * i, v);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) t[32 * i + k] = __uint_as_float(v[k]);
-                }
+                uint32_t (&a)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[0]);
+                uint32_t (&b2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[32]);
+                uint32_t (&c2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[64]);
+                uint32_t (&d2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[96]);
+                const uint32_t sc = tmem + lane_base + (s ? kColS1 : kColS0);
+                tc::tmem_ld32(sc, a);
+                tc::tmem_ld32(sc + 32, b2);
+                tc::tmem_ld32(sc + 64, c2);
+                tc::tmem_ld32(sc + 96, d2);
+                tc::tmem_wait_ld();
             }
             const long long key0 = (long long)j * kPfBN;
-            float mrow = -INFINITY;
-            if (key0 + kPfBN - 1 <= qpos) {
+            if (key0 + kPfBN - 1 > qpos) {
+                // diagonal tile: keys past this row's position get -inf
 #pragma unroll
-                for (int k = 0; k < 128; ++k) {
-                    t[k] *= p.scale_log2;
-                    mrow = fmaxf(mrow, t[k]);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 128; ++k) {
-                    t[k] = (key0 + k <= qpos) ? t[k] * p.scale_log2 : -INFINITY;
-                    mrow = fmaxf(mrow, t[k]);
-                }
+                for (int k = 0; k < 128; ++k)
+                    if (key0 + k > qpos) sv[k] = __float_as_uint(-INFINITY);
             }
+            // raw row maximum with eight independent chains (scale > 0, so
+            // max(scale * s) = scale * max(s))
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sv[k]);
+#pragma unroll
+            for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sv[k]));
+            const float mrow = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                               p.scale_log2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
                 m_used = mrow;
             } else if (mrow > m_used + kRescaleThreshold) {
-                alpha = exp2f(m_used - mrow);
+                alpha = ex2_approx(m_used - mrow);
                 m_used = mrow;
                 l_sum *= alpha;
                 rescale = true;
@@ -318,20 +331,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 tc::tmem_wait_st();
             }
-            float psum = 0.f;
+            // p = 2^(scale*s - m): packed fma, hardware exp2, bf16 pairs
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_used, -m_used);
+            float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t w[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const float p0 = exp2f(t[64 * half + 2 * k] - m_used);
-                    const float p1 = exp2f(t[64 * half + 2 * k + 1] - m_used);
-                    psum += p0 + p1;
-                    w[k] = tc::pack_bf16x2(p0, p1);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[64 * half + 2 * k]),
+                                                            __uint_as_float(sv[64 * half + 2 * k + 1])),
+                                                sc2, nm2);
+                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
+                    w[k] = tc::pack_bf16x2(e.x, e.y);
                 }
                 tc::tmem_st32(tmem + lane_base + (s ? kColP1 : kColP0) + 32 * half, w);
             }
-            l_sum += psum;
+            l_sum += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y) + (acc2[2].x + acc2[2].y) +
+                     (acc2[3].x + acc2[3].y);
             tc::tmem_wait_st();
             if (key0 + kPfBN > L) {
                 // Keys at or past L: the V rows there may hold anything; zero

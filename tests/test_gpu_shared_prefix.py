@@ -1,0 +1,163 @@
+"""Append + decode step with a shared prefix (copy-on-write) on the GPU.
+
+Groups of sequences share their common prefix as the same physical blocks
+("Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve Gerceklik": blocks are
+shared by pointer and copied on write).  One new token per sequence is
+appended; where it lands in a shared block, the block is copied first.  The
+result must equal the oracle on each sequence's logical content, and must be
+bit-identical to the same step on a layout where nobody shares anything.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_196_gb300 as pk
+import workloads as W
+from _gpu import assert_close_scaled, dev, host, require_cuda
+
+pytestmark = pytest.mark.gpu
+BS = 16
+
+
+def _append_tokens(pool, k, v, slots):
+    if len(slots):
+        pk.kv_append(pool, dev(k), dev(v), dev(np.asarray(slots, np.int64)), len(slots))
+
+
+def build_and_step(inp, share: bool, max_blocks: int, seed: int):
+    """Builds the cache (shared or private prefixes), runs the step; returns
+    (out, lse, tables, refcount checks, cow pair count)."""
+    lens = inp["lens"]
+    B, G, P = len(lens), inp["group_size"], inp["prefix_len"]
+    hkv, d = inp["new_k"].shape[1], inp["new_k"].shape[2]
+    hq = inp["q"].shape[1]
+    need = sum(-(-(int(L) + 1) // BS) for L in lens)
+    nb = int(math.ceil(1.2 * need)) + (B // G + 1) * (P // BS)
+    pool = pk.kv_pool_create(nb, BS, hkv, d, pk.KV_BF16)
+    alloc = pk.kv_pool_allocator(pool)
+    pk.kv_allocator_set_order(alloc, W.permutation(W.rng(seed), nb))
+    tables = np.full((B, max_blocks), -1, np.int32)
+    nblocks = np.zeros(B, np.int32)
+    none = np.zeros(0, np.int32)
+    templates = {}
+    for b in range(B):
+        g, L = b // G, int(lens[b])
+        n_pref = min(L, P)
+        if share:
+            if g not in templates:  # the group's prefix, written once
+                row = np.full(P // BS, -1, np.int32)
+                s = np.zeros(P, np.int64)
+                pk.kv_prepare_append(alloc, row, 0, 0, P, s, none, none)
+                _append_tokens(pool, inp["prefix_k"][g], inp["prefix_v"][g], s)
+                templates[g] = row
+            nbp = -(-n_pref // BS)
+            tables[b, :nbp] = templates[g][:nbp]
+            pk.kv_allocator_share(alloc, tables[b, :nbp])
+            nblocks[b] = nbp
+        else:
+            s = np.zeros(n_pref, np.int64)
+            nblocks[b], _ = pk.kv_prepare_append(alloc, tables[b], 0, 0, n_pref, s, none, none)
+            _append_tokens(pool, inp["prefix_k"][g][:n_pref], inp["prefix_v"][g][:n_pref], s)
+        if L > P:
+            s = np.zeros(L - P, np.int64)
+            nblocks[b], _ = pk.kv_prepare_append(alloc, tables[b], int(nblocks[b]), P, L - P, s,
+                                                 none, none)
+            _append_tokens(pool, inp["suffix_k"][b], inp["suffix_v"][b], s)
+    for row in templates.values():  # the templates were not sequences
+        pk.kv_allocator_free(alloc, row)
+    torch.cuda.synchronize()
+    # ---- the step: plan (host), copy shared blocks that get written, append, decode
+    slots = np.zeros(B, np.int64)
+    src, dst = [], []
+    cs, cd = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    for b in range(B):
+        s1 = np.zeros(1, np.int64)
+        nblocks[b], ncow = pk.kv_prepare_append(alloc, tables[b], int(nblocks[b]), int(lens[b]),
+                                                1, s1, cs, cd)
+        slots[b] = s1[0]
+        if ncow:
+            src.append(int(cs[0]))
+            dst.append(int(cd[0]))
+    if src:
+        pk.kv_copy_blocks(pool, dev(np.array(src, np.int32)), dev(np.array(dst, np.int32)), len(src))
+    pk.kv_append(pool, dev(inp["new_k"]), dev(inp["new_v"]), dev(slots), B)
+    new_lens = (lens + 1).astype(np.int32)
+    out = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+    wsb = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, 0)
+    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    pk.paged_decode_attention(pool, dev(inp["q"]), dev(tables), max_blocks, dev(new_lens), B, hq,
+                              1 / math.sqrt(d), out, pk.KV_F32, lse, 0, ws, wsb)
+    torch.cuda.synchronize()
+    assert pk.kv_get_device_error(pool) == 0
+    refs = {int(t): pk.kv_allocator_refcount(alloc, int(t)) for t in np.unique(tables[tables >= 0])}
+    res = host(out).astype(np.float64), host(lse).astype(np.float64), tables.copy(), refs, len(src)
+    pk.kv_pool_destroy(pool)
+    return res
+
+
+def oracle_step(inp):
+    """Oracle on each sequence's logical content after the step."""
+    lens = inp["lens"]
+    B, G, P = len(lens), inp["group_size"], inp["prefix_len"]
+    ks, vs = [], []
+    for b in range(B):
+        n_pref = min(int(lens[b]), P)
+        ks.append(np.concatenate([inp["prefix_k"][b // G][:n_pref], inp["suffix_k"][b],
+                                  inp["new_k"][b:b + 1]]))
+        vs.append(np.concatenate([inp["prefix_v"][b // G][:n_pref], inp["suffix_v"][b],
+                                  inp["new_v"][b:b + 1]]))
+    new_lens = (lens + 1).astype(np.int32)
+    hkv, d = ks[0].shape[1], ks[0].shape[2]
+    maxb = max(oracle.blocks_needed(int(L), BS) for L in new_lens)
+    nb = sum(oracle.blocks_needed(int(L), BS) for L in new_lens)
+    tables = oracle.build_block_tables(new_lens, BS, np.arange(nb, dtype=np.int32), maxb)
+    pk_, pv_ = W.empty_pool(nb, hkv, d, "bf16"), W.empty_pool(nb, hkv, d, "bf16")
+    for b in range(B):
+        j = np.arange(int(new_lens[b]))
+        oracle.append(pk_, pv_, ks[b], vs[b], tables[b, j // BS].astype(np.int64) * BS + j % BS)
+    return oracle.paged_decode(pk_, pv_, tables, new_lens, inp["q"], 1 / math.sqrt(d))
+
+
+def _check(inp, max_blocks, sample=None):
+    out_s, lse_s, tab_s, refs, ncow = build_and_step(inp, True, max_blocks, seed=91)
+    out_p, lse_p, _, _, ncow_p = build_and_step(inp, False, max_blocks, seed=92)
+    # shared blocks == private copies, bit for bit
+    np.testing.assert_array_equal(out_s, out_p)
+    np.testing.assert_array_equal(lse_s, lse_p)
+    assert ncow_p == 0
+    lens, G, P = inp["lens"], inp["group_size"], inp["prefix_len"]
+    # a write into a shared block copied it: exactly the sequences whose new
+    # token falls inside a partly used shared prefix block (L < prefix, L % 16 != 0)
+    expect_cow = 0
+    for g0 in range(0, len(lens), G):
+        grp = lens[g0:g0 + G]
+        for L in grp:
+            if L < P and L % BS:
+                sharers = np.sum(np.minimum(grp, P) > (L // BS) * BS)
+                expect_cow += int(sharers > 1)
+    assert ncow <= expect_cow and (expect_cow == 0 or ncow > 0)
+    # every block still in a table is referenced once per table that holds it
+    counts = {}
+    for t in tab_s[tab_s >= 0]:
+        counts[int(t)] = counts.get(int(t), 0) + 1
+    assert counts == refs
+    ref, ref_lse = oracle_step(inp)
+    assert_close_scaled(out_s, ref, 2e-3, "shared-prefix step")
+    np.testing.assert_allclose(lse_s, ref_lse, atol=1e-3)
+
+
+def test_shared_prefix_step_two_groups():
+    require_cuda()
+    inp = W.shared_prefix_inputs(batch=32)
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16)
+
+
+@pytest.mark.slow
+def test_shared_prefix_step_full_size():
+    require_cuda()
+    inp = W.shared_prefix_inputs()
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16)
