@@ -26,6 +26,7 @@
 // for the g heads are reduced across the 16 lanes with a reduce-scatter
 // (each exchange step halves the number of values carried), ending with lane c
 // holding the score of head c / (16/G).  Products use packed fp32x2 FMAs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -67,6 +68,7 @@ struct DecodeKParams {
     const unsigned long long *v_bases;
     const int32_t *req_ids;
     const long long *mapped_tokens;
+    const CUtensorMap *req_maps;
     long long head_stride;
     int max_requests;
     const int32_t *seq_lens;
@@ -458,6 +460,335 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core decode for large GQA groups (5..8 query heads per kv head,
+// bf16, head_dim 128).  With eight heads sharing every K/V element the
+// CUDA-core kernel above needs ~2x the instructions per byte of the four-head
+// case and becomes issue-bound; here the two small contractions of each
+// 16-token block run as warp-level mma.sync (the 16 tokens are M, the eight
+// heads N):
+//   S^T[16 tok][8 heads] = K[16][128] . Q^T        (8 k-steps of 16 dims)
+//   O^T[128][8] += V^T[128][16 tok] . P^T[16][8]    (8 m-tiles of 16 dims)
+// K/V tiles arrive by tiled TMA with 128-byte swizzle (two 16 x 64 boxes per
+// tile) so ldmatrix reads are bank-conflict-free.  P^T is formed from the S
+// fragment with movmatrix.trans and fed as bf16 hi + lo parts (two MMAs), so
+// the weights keep ~16 bits of precision.  Same CTA decomposition, pipeline,
+// split plan, masking and final merge as decode_kernel.
+// ---------------------------------------------------------------------------
+namespace mma {
+
+KV_DEVICE void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+KV_DEVICE void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+KV_DEVICE uint32_t movm_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+// d += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+KV_DEVICE void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+KV_DEVICE uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+KV_DEVICE float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+KV_DEVICE float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+KV_DEVICE void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                     uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+}  // namespace mma
+
+constexpr int kTcTile = 16 * 128 * 2;  // one (block, head) tile: 4 KiB, two 2 KiB swizzled halves
+
+template <bool LINEAR>
+__global__ void __launch_bounds__(kDecodeThreads, 3)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
+                     const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
+    constexpr int G = 8, D = 128;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    long long L = p.seq_lens[b];
+    const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
+    if constexpr (LINEAR) {
+        const int req = p.req_ids[b];
+        if (req < 0 || req >= p.max_requests || p.k_bases[req] == 0) {
+            if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+            L = 0;
+        } else {
+            const long long mapped = p.mapped_tokens[req];
+            if (L > mapped) {
+                if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+                L = mapped;
+            }
+            map_k = p.req_maps + 2 * req;
+            map_v = p.req_maps + 2 * req + 1;
+        }
+    }
+    if (L > (long long)p.max_blocks * kBS) {
+        if (tid == 0 && split == 0 && h == 0)
+            atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
+        L = (long long)p.max_blocks * kBS;
+    }
+    if (L < 0) L = 0;
+    const int nblk = (int)((L + kBS - 1) / kBS);
+    const int blk0 = split * p.part_blocks;
+    if (blk0 >= nblk && split > 0) return;
+    const int nloc = max(0, min(p.part_blocks, nblk - blk0));
+    const int nsplit = max(1, (nblk + p.part_blocks - 1) / p.part_blocks);
+
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    char *stages = smem;  // kNStage x (K tile, V tile), swizzled
+    constexpr size_t kRing = decode_ring_bytes<D, G, true>();
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
+    uint64_t *empty = full + kNStage;
+    int *stage_valid = reinterpret_cast<int *>(empty + kNStage);
+    int32_t *tbl = stage_valid + kNStage;  // [part_blocks]
+
+    if (warp == kNW) {
+        if constexpr (!LINEAR) {
+            const int32_t *row = p.tables + (size_t)b * p.max_blocks + blk0;
+            for (int i = lane; i < nloc; i += 32) tbl[i] = __ldg(row + i);
+        }
+        if (lane == 0) {
+            for (int st = 0; st < kNStage; ++st) {
+                mbar_init(&full[st], 1);
+                mbar_init(&empty[st], 32);
+            }
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+
+    if (warp == kNW) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(map_k) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
+            const uint64_t policy = l2_evict_first_policy();
+            int issued = 0;
+            for (int i = 0; i < nloc; ++i) {
+                const int st = i % kNStage, r = i / kNStage;
+                if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err)) break;
+                int y;
+                bool valid = true;
+                if constexpr (LINEAR) {
+                    y = (int)((long long)h * p.head_stride + (long long)(blk0 + i) * kBS);
+                } else {
+                    const int id = tbl[i];
+                    valid = id >= 0 && id < p.num_blocks;
+                    if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                    y = ((valid ? id : 0) * p.num_kv_heads + h) * kBS;
+                }
+                stage_valid[st] = valid ? 1 : 0;
+                char *dst = stages + st * 2 * kTcTile;
+                if (valid) {
+                    mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
+                    mma::tma2d(dst, map_k, 0, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
+                } else {
+                    mbar_arrive(&full[st]);
+                }
+                issued = i + 1;
+            }
+            for (int st = 0; st < kNStage && st < issued; ++st)
+                mbar_wait(&full[st], ((issued - 1 - st) / kNStage) & 1, p.err);
+        }
+        return;
+    }
+
+    // ---- consumer warps: lane = (g = lane / 4, t = lane % 4)
+    const int g = lane >> 2, t = lane & 3;
+    // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
+    uint32_t qf[8][2];
+    {
+        const bool live = g < p.g;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            reinterpret_cast<const uint16_t *>(p.q) + ((size_t)b * p.num_q_heads + h * p.g + (live ? g : 0)) * D);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
+            qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
+        }
+    }
+    // running state for heads 2t, 2t+1 (replicated over g)
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const uint32_t stage_base = smem_addr(stages);
+    // ldmatrix row / chunk selectors for this lane
+    const int mi = lane >> 3;
+    const int rowA = (lane & 7) + (mi & 1) * 8;      // K: token row (non-transposed A)
+    const int tokV = (lane & 7) + (mi >> 1) * 8;     // V: token row (transposed A)
+
+    for (int i = warp; i < nloc; i += kNW) {
+        const int st = i % kNStage, r = i / kNStage;
+        if (!mbar_wait(&full[st], r & 1, p.err)) break;
+        int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
+        if (!stage_valid[st]) ntok = 0;
+        const uint32_t kt = stage_base + st * 2 * kTcTile;
+        const uint32_t vt = kt + kTcTile;
+
+        // ---- S^T = K Q^T
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int chunk = 2 * (kk & 3) + (mi >> 1);
+            const uint32_t addr = kt + (kk >> 2) * (kTcTile / 2) + rowA * 128 + ((chunk ^ (rowA & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            mma::ldsm_x4(addr, a0, a1, a2, a3);
+            mma::mma_bf16(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        }
+        // c0,c1: token g, heads 2t,2t+1; c2,c3: token g+8
+        const bool v0 = g < ntok, v1 = g + 8 < ntok;
+        float s0 = v0 ? c[0] * p.scale_log2 : -INFINITY;
+        float s1 = v0 ? c[1] * p.scale_log2 : -INFINITY;
+        float s2 = v1 ? c[2] * p.scale_log2 : -INFINITY;
+        float s3 = v1 ? c[3] * p.scale_log2 : -INFINITY;
+        float mh0 = fmaxf(s0, s2), mh1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int x = 4; x <= 16; x <<= 1) {
+            mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, x));
+            mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, x));
+        }
+        const float mn0 = fmaxf(m_run[0], mh0), mn1 = fmaxf(m_run[1], mh1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
+        const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
+        l_run[0] = l_run[0] * al0 + (p0 + p2);
+        l_run[1] = l_run[1] * al1 + (p1 + p3);
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        // ---- P^T fragments (bf16 hi + lo), via transpose of the S layout
+        const uint32_t h01 = mma::pack_bf16(p0, p1), h23 = mma::pack_bf16(p2, p3);
+        const uint32_t l01 = mma::pack_bf16(p0 - mma::bf16_lo_f(h01), p1 - mma::bf16_hi_f(h01));
+        const uint32_t l23 = mma::pack_bf16(p2 - mma::bf16_lo_f(h23), p3 - mma::bf16_hi_f(h23));
+        const uint32_t bh0 = mma::movm_t(h01), bh1 = mma::movm_t(h23);
+        const uint32_t bl0 = mma::movm_t(l01), bl1 = mma::movm_t(l23);
+        // token masks for the V fragments (pairs 2t,2t+1 and 2t+8,2t+9)
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (ntok < kBS) {
+            mlo = (2 * t < ntok ? 0xffffu : 0u) | (2 * t + 1 < ntok ? 0xffff0000u : 0u);
+            mhi = (2 * t + 8 < ntok ? 0xffffu : 0u) | (2 * t + 9 < ntok ? 0xffff0000u : 0u);
+        }
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int cidx = 2 * mt + (mi & 1);
+            const uint32_t addr = vt + (cidx >> 3) * (kTcTile / 2) + tokV * 128 +
+                                  (((cidx & 7) ^ (tokV & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            mma::ldsm_x4_t(addr, a0, a1, a2, a3);
+            // a0/a1: tokens 2t,2t+1; a2/a3: tokens 2t+8,2t+9.  Unused slots may
+            // hold anything: their lanes are zeroed, never multiplied by 0.
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+            mma::mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma::mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+        }
+        __syncwarp();
+        mbar_arrive(&empty[st]);
+    }
+
+    // ---- per-warp totals over the 8 token lanes (g)
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
+    }
+    named_bar_sync(1, kNW * 32);
+    float *sm_o = reinterpret_cast<float *>(stages);  // [kNW][G][D]
+    float *sm_m = sm_o + kNW * G * D;
+    float *sm_l = sm_m + kNW * G;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        sm_o[(warp * G + 2 * t) * D + 16 * mt + g] = o[mt][0];
+        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g] = o[mt][1];
+        sm_o[(warp * G + 2 * t) * D + 16 * mt + g + 8] = o[mt][2];
+        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g + 8] = o[mt][3];
+    }
+    if (g == 0) {
+        sm_m[warp * G + 2 * t] = m_run[0];
+        sm_m[warp * G + 2 * t + 1] = m_run[1];
+        sm_l[warp * G + 2 * t] = l_run[0];
+        sm_l[warp * G + 2 * t + 1] = l_run[1];
+    }
+    named_bar_sync(1, kNW * 32);
+
+    constexpr float kLn2 = 0.6931471805599453f;
+    for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
+        const int j = idx / D, d = idx - j * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * G + j]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+                const float f = exp2f(sm_m[w * G + j] - M);
+                num += f * sm_o[(w * G + j) * D + d];
+                den += f * sm_l[w * G + j];
+            }
+        }
+        const float ov = den > 0.f ? num / den : 0.f;
+        const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
+        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
+        if (nsplit == 1) {
+            if (p.out_bf16)
+                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(ov);
+            else
+                reinterpret_cast<float *>(p.out)[row * D + d] = ov;
+            if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+        } else {
+            p.ws_o[(row * p.max_splits + split) * D + d] = ov;
+            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
+        }
+    }
+}
+
+static size_t decode_tc_smem_bytes(bool linear, int part_blocks) {
+    return 1024 + decode_ring_bytes<128, 8, true>() + 2 * kNStage * sizeof(uint64_t) +
+           kNStage * sizeof(int) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
+}
+
 // Merges the per-split results of sequences cut into more than one split:
 // o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), lse in the log2 domain.
 // One warp per (sequence, query head); lanes cover head_dim.
@@ -607,10 +938,26 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.ws_lse = need > 0 ? kp.ws_o + (size_t)a.batch * a.num_q_heads * ms * a.head_dim : nullptr;
     kp.err = a.err;
 
+    kp.req_maps = a.req_maps;
     const dim3 grid(ms, a.num_kv_heads, a.batch);
     kv_status st;
     const bool bf = a.dtype == KV_BF16;
-    if (a.head_dim == 128) {
+    // Large head groups on bf16 / d128 go to the tensor-core variant when the
+    // tiled-TMA maps of the K/V storage are available.
+    const bool use_tc = bf && a.head_dim == 128 && G == 8 &&
+                        (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
+    if (use_tc) {
+        const size_t smem = decode_tc_smem_bytes(linear, pb);
+        CUtensorMap dummy{};
+        const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
+        const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
+        auto fn = linear ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return KV_ERR_CUDA;
+        fn<<<grid, kDecodeThreads, smem, a.stream>>>(mk, mv, kp);
+        st = cuda_status(cudaGetLastError());
+    } else if (a.head_dim == 128) {
         st = bf ? (linear ? launch_g<128, true, true>(G, kp, grid, a.stream)
                           : launch_g<128, true, false>(G, kp, grid, a.stream))
                 : (linear ? launch_g<128, false, true>(G, kp, grid, a.stream)
@@ -682,6 +1029,10 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;
     a.stream = as_stream(stream);
+    if (p->dtype == KV_BF16 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
+        a.pool_map_k = &p->tmap_k;
+        a.pool_map_v = &p->tmap_v;
+    }
     return launch_decode(a, false);
 }
 

@@ -44,6 +44,11 @@ inline kv_status device_error_status(int code) {
 
 int sm_count();
 
+// tiled-TMA maps (tmap.cu): bf16 rows of 128 values, boxes 16 x 64, 128B swizzle
+bool encode_rows_map(CUtensorMap *m, void *base, long long rows);
+bool encode_q_map(CUtensorMap *m, const void *q, int rows, int hq);
+kv_status pool_tensor_maps(kv_pool *p);
+
 // ---- decode (shared by the paged and contiguous paths) ----
 struct DecodeArgs {
     const void *q;
@@ -58,8 +63,12 @@ struct DecodeArgs {
     const unsigned long long *v_bases;
     const int32_t *req_ids;
     const long long *mapped_tokens;  // per request
+    const CUtensorMap *req_maps;     // per request: K map, V map (contiguous, bf16 d128)
     long long head_stride;           // tokens per head region
     int max_requests;
+    // paged: tiled-TMA maps of the pools (bf16 d128 only; else null)
+    const CUtensorMap *pool_map_k;
+    const CUtensorMap *pool_map_v;
     // common
     const int32_t *seq_lens;
     int batch;

@@ -32,7 +32,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -416,53 +415,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// Pool as a 2-D bf16 tensor [rows = num_blocks*Hkv*16][head_dim]; boxes of
-// 16 rows x 64 columns with 128-byte swizzle.
-static bool encode_pool_map(CUtensorMap *m, void *base, long long rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kPfD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kPfD * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// q as a 3-D tensor [rows][Hq][head_dim]; boxes of 128 rows x 1 head x 64 dims.
-static bool encode_q_map(CUtensorMap *m, const void *q, int rows, int hq) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kPfD, (cuuint64_t)hq, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)kPfD * 2, (cuuint64_t)hq * kPfD * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)kPfBM};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace pkv
 
 using namespace pkv;
@@ -482,12 +434,7 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     if (reinterpret_cast<uintptr_t>(q) & 15) return KV_ERR_ARG;
     const long long pool_rows = (long long)p->num_blocks * p->num_kv_heads * 16;
     if (pool_rows > INT32_MAX || batch > 65535) return KV_ERR_UNSUPPORTED;
-    if (!p->tmaps_ready) {
-        if (!encode_pool_map(&p->tmap_k, p->k, pool_rows) ||
-            !encode_pool_map(&p->tmap_v, p->v, pool_rows))
-            return KV_ERR_CUDA;
-        p->tmaps_ready = true;
-    }
+    if (pool_tensor_maps(p) != KV_OK) return KV_ERR_CUDA;
     // The q map covers exactly total_q rows: a tile reaching past them reads
     // zeros, and rows past a chunk or past total_q are never stored.
     CUtensorMap tm_q;

@@ -116,6 +116,9 @@ struct kv_contig {
     unsigned long long *d_vbase = nullptr;
     long long *d_mapped = nullptr;
     int *err = nullptr;
+    // tiled-TMA maps of each request's K and V region (bf16, head_dim 128 only)
+    CUtensorMap *d_maps = nullptr;  // [max_requests][2]
+    bool maps = false;
 };
 
 static kv_status sync_request(kv_contig *c, int req) {
@@ -126,6 +129,16 @@ static kv_status sync_request(kv_contig *c, int req) {
         cudaMemcpy(c->d_vbase + req, &vb, sizeof(vb), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(c->d_mapped + req, &mt, sizeof(mt), cudaMemcpyHostToDevice) != cudaSuccess)
         return KV_ERR_CUDA;
+    if (c->maps && r.base) {
+        // The maps describe the whole reserved region; kernels only read rows
+        // below the mapped length.
+        CUtensorMap m[2];
+        const long long rows = (long long)c->hkv * c->head_stride;
+        if (!encode_rows_map(&m[0], reinterpret_cast<void *>(kb), rows) ||
+            !encode_rows_map(&m[1], reinterpret_cast<void *>(vb), rows) ||
+            cudaMemcpy(c->d_maps + 2 * req, m, sizeof(m), cudaMemcpyHostToDevice) != cudaSuccess)
+            return KV_ERR_CUDA;
+    }
     return KV_OK;
 }
 
@@ -184,6 +197,14 @@ kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, i
         cudaGetLastError();
         kv_contig_destroy(c);
         return KV_ERR_OOM;
+    }
+    if (dtype == KV_BF16 && head_dim == 128 && (long long)num_kv_heads * c->head_stride <= INT32_MAX) {
+        if (cudaMalloc(&c->d_maps, sizeof(CUtensorMap) * 2 * max_requests) != cudaSuccess) {
+            cudaGetLastError();
+            kv_contig_destroy(c);
+            return KV_ERR_OOM;
+        }
+        c->maps = true;
     }
     *out = c;
     return KV_OK;
@@ -305,6 +326,7 @@ kv_status kv_contig_destroy(kv_contig_t c) {
     if (c->d_vbase) cudaFree(c->d_vbase);
     if (c->d_mapped) cudaFree(c->d_mapped);
     if (c->err) cudaFree(c->err);
+    if (c->d_maps) cudaFree(c->d_maps);
     delete c;
     return KV_OK;
 }
@@ -358,6 +380,7 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
     a.v_bases = c->d_vbase;
     a.req_ids = req_ids;
     a.mapped_tokens = c->d_mapped;
+    a.req_maps = c->maps ? c->d_maps : nullptr;
     a.head_stride = c->head_stride;
     a.max_requests = c->max_requests;
     a.seq_lens = seq_lens;

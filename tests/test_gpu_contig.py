@@ -94,9 +94,10 @@ def test_contig_decode_matches_oracle(dtype):
     c.close()
 
 
-def test_contig_equals_paged_bit_for_bit():
+@pytest.mark.parametrize("hq", [16, 32])  # g = 4 (CUDA cores) and g = 8 (tensor cores)
+def test_contig_equals_paged_bit_for_bit(hq):
     lens = [35, 17, 1, 300, 777, 64]
-    c = ContigCase(lens, 800, hq=16, hkv=4, d=128, dtype="bf16", seed=42)
+    c = ContigCase(lens, 800, hq=hq, hkv=4, d=128, dtype="bf16", seed=42)
     # the same logical data in a shuffled paged pool
     need = sum(oracle.blocks_needed(L, 16) for L in lens)
     perm = W.permutation(W.rng(43), need + 5)
@@ -111,12 +112,12 @@ def test_contig_equals_paged_bit_for_bit():
         pk.kv_append(pool, dev(c.K[b]), dev(c.V[b]), dev(slots), L)
     for splits in (1, 4, 0):
         out_c, lse_c = c.run(splits)
-        out_p = torch.empty((len(lens), 16, 128), dtype=torch.float32, device="cuda")
-        lse_p = torch.empty((len(lens), 16), dtype=torch.float32, device="cuda")
-        wsb = pk.kv_decode_workspace_size(len(lens), 16, 4, 128, maxb, splits)
+        out_p = torch.empty((len(lens), hq, 128), dtype=torch.float32, device="cuda")
+        lse_p = torch.empty((len(lens), hq), dtype=torch.float32, device="cuda")
+        wsb = pk.kv_decode_workspace_size(len(lens), hq, 4, 128, maxb, splits)
         ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
         pk.paged_decode_attention(pool, dev(c.q), dev(tables), maxb, dev(np.array(lens, np.int32)),
-                                  len(lens), 16, 1 / math.sqrt(128), out_p, pk.KV_F32, lse_p,
+                                  len(lens), hq, 1 / math.sqrt(128), out_p, pk.KV_F32, lse_p,
                                   splits, ws, wsb)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(host(out_p), out_c.astype(np.float32))
