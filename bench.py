@@ -225,7 +225,8 @@ def run_ours(args, rank, world, local_rank):
     k_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
     v_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
     out = torch.empty((B, hq, d), dtype=torch.int16, device="cuda")
-    splits = args.splits
+    # the split plan: from the host-known lengths unless forced on the command line
+    splits = args.splits if args.splits > 0 else pk.kv_decode_plan(lens, hkv, max_blocks)
     ws_bytes = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, splits)
     ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
     part_blocks, max_splits = pk.kv_decode_split_plan(B, hkv, max_blocks, splits)
@@ -601,7 +602,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="llama3_8b_decode", choices=sorted(DESCR))
-    ap.add_argument("--splits", type=int, default=0, help="0 = the library's automatic plan")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="0 = plan from the host-known lengths (kv_decode_plan)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -178,6 +178,16 @@ kv_status kv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
 kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits,
                                int *part_blocks, int *max_splits);
 
+/* Chooses num_splits for paged_decode_attention / contig_decode_attention
+ * from the sequence lengths as the host knows them (a serving host keeps its
+ * own block tables, so it has them).  host_seq_lens: host int32[batch].
+ * Prefers the smallest partitions whose CTAs all fit in one wave of at most
+ * 2.4 CTAs per SM on this GPU (measured to stream fastest); when no split
+ * fits, the largest partitions that still give at least three full waves.  The result depends only on the lengths, the batch
+ * shape and the SM count.  Host only; *num_splits >= 1. */
+kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_heads,
+                         int max_blocks, int *num_splits);
+
 /* Paged decode attention: one query token per sequence attends all
  * seq_lens[b] tokens of its cache, reading K/V blocks through the block
  * table ("PagedAttention Nedir?", "Nasil Calisir?" step 4), with

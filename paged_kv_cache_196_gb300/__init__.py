@@ -20,7 +20,7 @@ __all__ = [
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
     "kv_allocator_num_free", "kv_prepare_append", "kv_pool_create", "kv_pool_destroy",
     "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks",
-    "kv_decode_workspace_size", "kv_decode_split_plan", "paged_decode_attention",
+    "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_append", "contig_decode_attention",
@@ -65,6 +65,7 @@ _SIGS = {
     "kv_copy_blocks": [_vp, _vp, _vp, _i32, _vp],
     "kv_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
     "kv_decode_split_plan": [_i32, _i32, _i32, _i32, _P(_i32), _P(_i32)],
+    "kv_decode_plan": [_vp, _i32, _i32, _i32, _P(_i32)],
     "paged_decode_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32,
                                _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
@@ -248,6 +249,16 @@ def kv_decode_split_plan(batch, num_kv_heads, max_blocks, num_splits=0):
     _check(lib().kv_decode_split_plan(batch, num_kv_heads, max_blocks, num_splits,
                                       ctypes.byref(pb), ctypes.byref(ms)), "kv_decode_split_plan")
     return pb.value, ms.value
+
+
+def kv_decode_plan(host_seq_lens, num_kv_heads: int, max_blocks: int) -> int:
+    """num_splits for a decode over sequences of these (host, int32) lengths."""
+    import numpy as _np
+    lens = _np.ascontiguousarray(host_seq_lens, dtype=_np.int32)
+    r = _i32()
+    _check(lib().kv_decode_plan(_ptr(lens), len(lens), num_kv_heads, max_blocks, ctypes.byref(r)),
+           "kv_decode_plan")
+    return r.value
 
 
 def paged_decode_attention(p: int, q, block_tables, max_blocks: int, seq_lens, batch: int,

@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -50,11 +51,17 @@ namespace pkv {
 #ifndef PKV_DECODE_HS8
 #define PKV_DECODE_HS8 2
 #endif
+#ifndef PKV_TC_MIN_G
+#define PKV_TC_MIN_G 3   // smallest head group routed to the tensor-core decode
+#endif
 constexpr int kNW = PKV_DECODE_WARPS;    // consumer warps per CTA
 constexpr int kDecodeThreads = (kNW + 1) * 32;
 constexpr int kBS = 16;                  // tokens per block
 constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
 constexpr int kNStage = PKV_DECODE_STAGES;  // pipeline depth (a multiple of kNW)
+// Splits per (sequence, kv head) merged inside the decode kernel by the last
+// CTA of that pair; longer plans leave the merge to merge_kernel.
+constexpr int kFuseMaxSplits = 32;
 static_assert(kNStage % kNW == 0, "each stage must belong to one consumer warp");
 
 struct DecodeKParams {
@@ -83,6 +90,7 @@ struct DecodeKParams {
     float *lse;
     float *ws_o;
     float *ws_lse;
+    int *counters;  // per (sequence, kv head) arrival counters for the fused merge, or null
     int *err;
 };
 
@@ -147,8 +155,104 @@ KV_DEVICE void reduce_scatter16(float *v, int lane) {
 template <int D, int G, bool BF16>
 constexpr size_t decode_ring_bytes() {
     constexpr size_t ring = (size_t)kNStage * 2 * TileShape<D, BF16>::kBytes;
-    constexpr size_t merge = (size_t)kNW * (G * D + 2 * G) * sizeof(float);
+    constexpr size_t merge =
+        (size_t)kNW * (G * D + 2 * G) * sizeof(float) + (G * kFuseMaxSplits + 4) * sizeof(float);
     return ((ring > merge ? ring : merge) + 127) / 128 * 128;
+}
+
+// End of a partition: combine the kNW warp states (running max m, sum l,
+// unnormalised output o, all in the log2 domain) into this partition's
+// result.  With one partition the result is final.  Otherwise it is written
+// to the workspace; the CTA that finishes last for its (sequence, kv head)
+// -- found with an arrival counter that it resets afterwards -- merges all
+// partitions: o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
+template <int G, int D>
+KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const float *sm_m,
+                                const float *sm_l, int b, int h, int split, int nsplit, int tid) {
+    constexpr float kLn2 = 0.6931471805599453f;
+    for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
+        const int j = idx / D, d = idx - j * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * G + j]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+                const float f = exp2f(sm_m[w * G + j] - M);
+                num += f * sm_o[(w * G + j) * D + d];
+                den += f * sm_l[w * G + j];
+            }
+        }
+        const float o = den > 0.f ? num / den : 0.f;
+        const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
+        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
+        if (nsplit == 1) {
+            if (p.out_bf16)
+                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(o);
+            else
+                reinterpret_cast<float *>(p.out)[row * D + d] = o;
+            if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+        } else {
+            p.ws_o[(row * p.max_splits + split) * D + d] = o;
+            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
+        }
+    }
+    if (nsplit == 1 || !p.counters || nsplit > kFuseMaxSplits) return;
+
+    // ---- fused merge by the last-arriving CTA of this (sequence, kv head)
+    float *w = const_cast<float *>(sm_l) + kNW * G;  // [G][kFuseMaxSplits] weights, then a flag
+    int *flag = reinterpret_cast<int *>(w + G * kFuseMaxSplits);
+    __threadfence();  // partial results visible device-wide before the arrival
+    named_bar_sync(1, kNW * 32);
+    if (tid == 0) {
+        const int old = atomicAdd(p.counters + (size_t)b * p.num_kv_heads + h, 1);
+        *flag = old == nsplit - 1;
+    }
+    named_bar_sync(1, kNW * 32);
+    if (!*flag) return;
+    __threadfence();
+    // split weights per head: 2^(lse_s - M) / sum
+    for (int j = tid; j < p.g; j += kNW * 32) {
+        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
+        const float *ls = p.ws_lse + row * p.max_splits;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(ls + s2));
+        float den = 0.f;
+        for (int s2 = 0; s2 < nsplit; ++s2) {
+            const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(ls + s2) - M);
+            w[j * kFuseMaxSplits + s2] = e;
+            den += e;
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        for (int s2 = 0; s2 < nsplit; ++s2) w[j * kFuseMaxSplits + s2] *= inv;
+        if (p.lse) p.lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+    }
+    named_bar_sync(1, kNW * 32);
+    for (int idx = tid; idx < p.g * (D / 4); idx += kNW * 32) {
+        const int j = idx / (D / 4), d4 = idx - j * (D / 4);
+        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
+        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * p.max_splits * D) + d4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < nsplit; ++s2) {
+            const float ws = w[j * kFuseMaxSplits + s2];
+            const float4 v = __ldcg(src + (size_t)s2 * (D / 4));
+            acc.x += ws * v.x;
+            acc.y += ws * v.y;
+            acc.z += ws * v.z;
+            acc.w += ws * v.w;
+        }
+        if (p.out_bf16) {
+            uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + row * D + 4 * d4;
+            o[0] = float_to_bf16_rn(acc.x);
+            o[1] = float_to_bf16_rn(acc.y);
+            o[2] = float_to_bf16_rn(acc.z);
+            o[3] = float_to_bf16_rn(acc.w);
+        } else {
+            reinterpret_cast<float4 *>(p.out)[(row * D) / 4 + d4] = acc;
+        }
+    }
+    if (tid == 0) p.counters[(size_t)b * p.num_kv_heads + h] = 0;  // ready for the next call
 }
 
 // HS = 1: the two half-warps take different tokens (2 per pass) and every
@@ -429,42 +533,15 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     }
     named_bar_sync(1, kNW * 32);
 
-    constexpr float kLn2 = 0.6931471805599453f;
-    for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
-        const int j = idx / D, d = idx - j * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * G + j]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const float f = exp2f(sm_m[w * G + j] - M);
-                num += f * sm_o[(w * G + j) * D + d];
-                den += f * sm_l[w * G + j];
-            }
-        }
-        const float o = den > 0.f ? num / den : 0.f;
-        const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
-        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
-        if (nsplit == 1) {
-            if (p.out_bf16)
-                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(o);
-            else
-                reinterpret_cast<float *>(p.out)[row * D + d] = o;
-            if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
-        } else {
-            p.ws_o[(row * p.max_splits + split) * D + d] = o;
-            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
-        }
-    }
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, tid);
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core decode for large GQA groups (5..8 query heads per kv head,
-// bf16, head_dim 128).  With eight heads sharing every K/V element the
-// CUDA-core kernel above needs ~2x the instructions per byte of the four-head
-// case and becomes issue-bound; here the two small contractions of each
+// Tensor-core decode for GQA groups of 3..8 query heads per kv head (bf16,
+// head_dim 128).  With g heads sharing every K/V element the CUDA-core kernel
+// above is issue-bound (ncu: ~55% issue-active at g = 4, about half the HBM
+// rate at g = 8, where it needs ~2x the instructions per byte); here the two
+// small contractions of each
 // 16-token block run as warp-level mma.sync (the 16 tokens are M, the eight
 // heads N):
 //   S^T[16 tok][8 heads] = K[16][128] . Q^T        (8 k-steps of 16 dims)
@@ -753,35 +830,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     named_bar_sync(1, kNW * 32);
 
-    constexpr float kLn2 = 0.6931471805599453f;
-    for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
-        const int j = idx / D, d = idx - j * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * G + j]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const float f = exp2f(sm_m[w * G + j] - M);
-                num += f * sm_o[(w * G + j) * D + d];
-                den += f * sm_l[w * G + j];
-            }
-        }
-        const float ov = den > 0.f ? num / den : 0.f;
-        const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
-        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
-        if (nsplit == 1) {
-            if (p.out_bf16)
-                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(ov);
-            else
-                reinterpret_cast<float *>(p.out)[row * D + d] = ov;
-            if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
-        } else {
-            p.ws_o[(row * p.max_splits + split) * D + d] = ov;
-            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
-        }
-    }
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, tid);
 }
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks) {
@@ -800,7 +849,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
                                                     int max_len_tokens, int batch,
                                                     int num_q_heads, int head_dim,
                                                     int part_blocks, int max_splits, void *out,
-                                                    int out_bf16, float *lse) {
+                                                    int out_bf16, float *lse, int min_splits) {
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= batch * num_q_heads) return;
@@ -814,7 +863,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
     if (L < 0) L = 0;
     const int nblk = (int)((L + kBS - 1) / kBS);
     const int nsplit = max(1, (nblk + part_blocks - 1) / part_blocks);
-    if (nsplit == 1) return;  // the decode kernel wrote the final result
+    if (nsplit < min_splits) return;  // the decode kernel wrote the final result
     const float *ls = ws_lse + (size_t)row * max_splits;
     float M = -INFINITY;
     for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ls[s]);
@@ -843,11 +892,11 @@ void split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits, int
     } else if (num_splits > 0) {
         pb = (max_blocks + num_splits - 1) / num_splits;
     } else {
-        // Partitions sized so the widest possible tables would give about 16
+        // Partitions sized so the widest possible tables would give about 12
         // CTAs per SM: real lengths are shorter, and small partitions keep
         // the last wave short.  At least 32 blocks (512 tokens) each.
         const long long work = (long long)batch * num_kv_heads * max_blocks;
-        const long long target = 16LL * sm_count();
+        const long long target = 12LL * sm_count();
         pb = (int)((work + target - 1) / target);
         if (pb < 32) pb = 32;
     }
@@ -939,12 +988,14 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.err = a.err;
 
     kp.req_maps = a.req_maps;
+    kp.counters = (a.counters && (long long)a.batch * a.num_kv_heads <= a.counter_slots) ? a.counters
+                                                                                       : nullptr;
     const dim3 grid(ms, a.num_kv_heads, a.batch);
     kv_status st;
     const bool bf = a.dtype == KV_BF16;
     // Large head groups on bf16 / d128 go to the tensor-core variant when the
     // tiled-TMA maps of the K/V storage are available.
-    const bool use_tc = bf && a.head_dim == 128 && G == 8 &&
+    const bool use_tc = bf && a.head_dim == 128 && g >= PKV_TC_MIN_G &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
     if (use_tc) {
         const size_t smem = decode_tc_smem_bytes(linear, pb);
@@ -969,11 +1020,13 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
                           : launch_g<64, false, false>(G, kp, grid, a.stream));
     }
     if (st != KV_OK || ms <= 1) return st;
+    const int min_splits = kp.counters ? kFuseMaxSplits + 1 : 2;
+    if (ms < min_splits) return st;  // every merge happens inside the decode kernel
     const int rows = a.batch * a.num_q_heads;
     merge_kernel<<<(rows + 3) / 4, 128, 0, a.stream>>>(
         kp.ws_o, kp.ws_lse, a.seq_lens, linear ? a.mapped_tokens : nullptr, a.req_ids,
         a.max_requests, a.max_blocks * kBS, a.batch, a.num_q_heads, a.head_dim, pb, ms, a.out,
-        kp.out_bf16, a.lse);
+        kp.out_bf16, a.lse, min_splits);
     return cuda_status(cudaGetLastError());
 }
 
@@ -988,6 +1041,64 @@ kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int 
     if (!part_blocks || !max_splits || batch < 0 || num_kv_heads <= 0 || max_blocks < 0)
         return KV_ERR_ARG;
     split_plan(batch, num_kv_heads, max_blocks, num_splits, part_blocks, max_splits);
+    return KV_OK;
+}
+
+kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_heads,
+                         int max_blocks, int *num_splits) {
+    if (!num_splits || batch < 0 || num_kv_heads <= 0 || max_blocks < 0 ||
+        (batch > 0 && !host_seq_lens))
+        return KV_ERR_ARG;
+    if (batch == 0 || max_blocks == 0) {
+        *num_splits = 1;
+        return KV_OK;
+    }
+    // Both decode kernels keep up to three CTAs resident per SM, but a single
+    // wave streams fastest at about two to two and a half CTAs per SM (sweeps
+    // of the Yi-6B-shaped workload on GB300: 2.0-2.3 per SM reach ~0.95 of the
+    // copy bandwidth, 2.7-3.0 per SM drop to ~0.65).
+    const long long slots = (long long)(2.4 * sm_count());
+    const long long resident = 3LL * sm_count();
+    std::vector<int> nblk(batch);
+    int longest = 1;
+    for (int b = 0; b < batch; ++b) {
+        long long L = host_seq_lens[b];
+        if (L < 0) L = 0;
+        if (L > (long long)max_blocks * kBS) L = (long long)max_blocks * kBS;
+        nblk[b] = (int)((L + kBS - 1) / kBS);
+        if (nblk[b] > longest) longest = nblk[b];
+    }
+    auto ctas = [&](int pb) {
+        long long n = 0;
+        for (int b = 0; b < batch; ++b) n += nblk[b] > pb ? (nblk[b] + pb - 1) / pb : 1;
+        return n * num_kv_heads;
+    };
+    // The partition size a given split count turns into inside the kernel.
+    auto plan_pb = [&](int splits) {
+        int pb, ms;
+        split_plan(batch, num_kv_heads, max_blocks, splits, &pb, &ms);
+        return pb;
+    };
+    // 1) One wave if it fits: the smallest partitions whose CTAs all run at
+    //    once (every CTA streams at the same time, none waits for a slot),
+    //    at most `slots` of them.
+    // 2) Otherwise at least three waves of smaller partitions, so the last,
+    //    partly filled wave is a small share of the time.
+    int best = 0;
+    for (int s = 1; s <= 4096; ++s) {
+        const int pb = plan_pb(s);
+        if (ctas(pb) <= slots) best = s;  // more splits -> smaller partitions
+        if (pb <= kNW) break;
+    }
+    if (best == 0) {
+        best = 1;
+        for (int s = 1; s <= 4096; ++s) {
+            const int pb = plan_pb(s);
+            best = s;
+            if (ctas(pb) >= 3 * resident || pb <= 32) break;
+        }
+    }
+    *num_splits = best;
     return KV_OK;
 }
 
@@ -1028,6 +1139,8 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;
+    a.counters = p->counters;
+    a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
     if (p->dtype == KV_BF16 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
         a.pool_map_k = &p->tmap_k;

@@ -16,6 +16,10 @@ struct kv_pool {
     void *k = nullptr;  // [num_blocks][num_kv_heads][block_size][head_dim]
     void *v = nullptr;
     int *err = nullptr;  // device error word
+    // arrival counters of the fused split merge, one per (sequence, kv head),
+    // zero between calls (each merging CTA resets its own)
+    static constexpr int kCounterSlots = 65536;
+    int *counters = nullptr;
     kv_allocator_t alloc = nullptr;
     // tiled-TMA descriptors of the K and V pools (built on first prefill)
     CUtensorMap tmap_k;
@@ -81,6 +85,8 @@ struct DecodeArgs {
     kv_dtype out_dtype;
     float *lse;
     int num_splits;
+    int *counters;
+    long long counter_slots;
     void *workspace;
     size_t workspace_bytes;
     int *err;

@@ -109,10 +109,12 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
     const size_t bytes = (size_t)num_blocks * num_kv_heads * block_size * head_dim * dtype_bytes(dtype);
     kv_status st = KV_OK;
     if (cudaMalloc(&p->k, bytes) != cudaSuccess || cudaMalloc(&p->v, bytes) != cudaSuccess ||
-        cudaMalloc(&p->err, sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&p->err, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&p->counters, sizeof(int) * kv_pool::kCounterSlots) != cudaSuccess) {
         cudaGetLastError();
         st = KV_ERR_OOM;
-    } else if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess) {
+    } else if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
+               cudaMemset(p->counters, 0, sizeof(int) * kv_pool::kCounterSlots) != cudaSuccess) {
         st = KV_ERR_CUDA;
     } else {
         st = kv_allocator_create(num_blocks, &p->alloc);
@@ -130,6 +132,7 @@ kv_status kv_pool_destroy(kv_pool_t p) {
     if (p->k) cudaFree(p->k);
     if (p->v) cudaFree(p->v);
     if (p->err) cudaFree(p->err);
+    if (p->counters) cudaFree(p->counters);
     if (p->alloc) kv_allocator_destroy(p->alloc);
     delete p;
     return KV_OK;
@@ -182,7 +185,12 @@ kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream) {
     if (cudaMemcpyAsync(&h, p->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return KV_ERR_CUDA;
-    if (h != 0 && cudaMemsetAsync(p->err, 0, sizeof(int), s) != cudaSuccess) return KV_ERR_CUDA;
+    // After a device error a merge may have been left half counted: clear the
+    // arrival counters along with the error word.
+    if (h != 0 && (cudaMemsetAsync(p->err, 0, sizeof(int), s) != cudaSuccess ||
+                   cudaMemsetAsync(p->counters, 0, sizeof(int) * kv_pool::kCounterSlots, s) !=
+                       cudaSuccess))
+        return KV_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
     *code = h;
     return device_error_status(h);

@@ -116,6 +116,7 @@ struct kv_contig {
     unsigned long long *d_vbase = nullptr;
     long long *d_mapped = nullptr;
     int *err = nullptr;
+    int *counters = nullptr;  // fused split-merge arrival counters (see kv_pool)
     // tiled-TMA maps of each request's K and V region (bf16, head_dim 128 only)
     CUtensorMap *d_maps = nullptr;  // [max_requests][2]
     bool maps = false;
@@ -190,6 +191,8 @@ kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, i
         cudaMalloc(&c->d_vbase, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
         cudaMalloc(&c->d_mapped, sizeof(long long) * max_requests) != cudaSuccess ||
         cudaMalloc(&c->err, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&c->counters, sizeof(int) * kv_pool::kCounterSlots) != cudaSuccess ||
+        cudaMemset(c->counters, 0, sizeof(int) * kv_pool::kCounterSlots) != cudaSuccess ||
         cudaMemset(c->d_kbase, 0, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
         cudaMemset(c->d_vbase, 0, sizeof(unsigned long long) * max_requests) != cudaSuccess ||
         cudaMemset(c->d_mapped, 0, sizeof(long long) * max_requests) != cudaSuccess ||
@@ -326,6 +329,7 @@ kv_status kv_contig_destroy(kv_contig_t c) {
     if (c->d_vbase) cudaFree(c->d_vbase);
     if (c->d_mapped) cudaFree(c->d_mapped);
     if (c->err) cudaFree(c->err);
+    if (c->counters) cudaFree(c->counters);
     if (c->d_maps) cudaFree(c->d_maps);
     delete c;
     return KV_OK;
@@ -397,6 +401,8 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = c->err;
+    a.counters = c->counters;
+    a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
     return launch_decode(a, true);
 }
@@ -408,7 +414,10 @@ kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream) {
     if (cudaMemcpyAsync(&h, c->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return KV_ERR_CUDA;
-    if (h != 0 && cudaMemsetAsync(c->err, 0, sizeof(int), s) != cudaSuccess) return KV_ERR_CUDA;
+    if (h != 0 && (cudaMemsetAsync(c->err, 0, sizeof(int), s) != cudaSuccess ||
+                   cudaMemsetAsync(c->counters, 0, sizeof(int) * kv_pool::kCounterSlots, s) !=
+                       cudaSuccess))
+        return KV_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
     *code = h;
     return device_error_status(h);
