@@ -67,6 +67,10 @@ typedef enum { KV_F32 = 0, KV_BF16 = 1 } kv_dtype;
 
 const char *kv_status_string(kv_status s);
 
+/* Text of the last CUDA runtime error a call of this library met on the
+ * calling thread (after a KV_ERR_CUDA or KV_ERR_OOM).  Owned by the library. */
+const char *kv_last_cuda_error(void);
+
 /* Number of blocks a sequence of n_tokens needs and the slots left unused in
  * its last block ("PagedAttention Nedir?", "Nasil Calisir?": 35 tokens at 16
  * per block need 3 blocks and leave 13 slots unused).  Host only. */

@@ -15,7 +15,7 @@ import os
 from . import build as _build
 
 __all__ = [
-    "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_blocks_for_tokens",
+    "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_last_cuda_error", "kv_blocks_for_tokens",
     "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
     "kv_allocator_num_free", "kv_prepare_append", "kv_pool_create", "kv_pool_destroy",
@@ -37,7 +37,10 @@ STATUS = {0: "KV_OK", -1: "KV_ERR_ARG", -2: "KV_ERR_OOM", -3: "KV_ERR_UNSUPPORTE
 class KVError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({kv_status_string(status)})")
+        msg = f"{where}: {STATUS.get(status, status)} ({kv_status_string(status)})"
+        if status in (-2, -4):
+            msg += f" [{kv_last_cuda_error()}]"
+        super().__init__(msg)
 
 
 _lib = None
@@ -47,6 +50,7 @@ _P = ctypes.POINTER
 # name -> argtypes (every function returns kv_status unless listed in _RESTYPE)
 _SIGS = {
     "kv_status_string": [_i32],
+    "kv_last_cuda_error": [],
     "kv_blocks_for_tokens": [_i64, _i32, _P(_i64), _P(_i64)],
     "kv_allocator_create": [_i32, _P(_vp)],
     "kv_allocator_destroy": [_vp],
@@ -86,7 +90,7 @@ _SIGS = {
                                 _sz, _vp],
     "kv_contig_get_device_error": [_vp, _P(_i32), _vp],
 }
-_RESTYPE = {"kv_status_string": ctypes.c_char_p}
+_RESTYPE = {"kv_status_string": ctypes.c_char_p, "kv_last_cuda_error": ctypes.c_char_p}
 
 
 def lib_path() -> str:
@@ -138,6 +142,10 @@ def _check(st: int, where: str):
 
 def kv_status_string(status: int) -> str:
     return lib().kv_status_string(status).decode()
+
+
+def kv_last_cuda_error() -> str:
+    return lib().kv_last_cuda_error().decode()
 
 
 def kv_blocks_for_tokens(n_tokens: int, block_size: int = 16):

@@ -925,9 +925,9 @@ static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
     // Large head groups split their heads across the two half-warps (register pressure).
     constexpr int HS = (G >= 8 && D == 128) ? PKV_DECODE_HS8 : 1;
     auto fn = decode_kernel<D, G, HS, BF16, LINEAR>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return KV_ERR_CUDA;
+    if (kv_status st0 = cuda_status(
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return st0;
     fn<<<grid, kDecodeThreads, smem, s>>>(kp);
     return cuda_status(cudaGetLastError());
 }
@@ -1003,9 +1003,9 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
         auto fn = linear ? decode_tc_kernel<true> : decode_tc_kernel<false>;
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return KV_ERR_CUDA;
+        if (kv_status st0 = cuda_status(
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return st0;
         fn<<<grid, kDecodeThreads, smem, a.stream>>>(mk, mv, kp);
         st = cuda_status(cudaGetLastError());
     } else if (a.head_dim == 128) {

@@ -33,9 +33,13 @@ inline int dtype_bytes(kv_dtype t) { return t == KV_BF16 ? 2 : 4; }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Maps a CUDA runtime error to a status (and clears sticky-free errors).
+// Remembers the text of the last CUDA error seen by this thread.
+void note_cuda_error(cudaError_t e);
+
+// Maps a CUDA runtime error to a status.
 inline kv_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return KV_OK;
+    note_cuda_error(e);
     if (e == cudaErrorMemoryAllocation) return KV_ERR_OOM;
     return KV_ERR_CUDA;
 }

@@ -10,12 +10,20 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <new>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace pkv {
+
+static thread_local char g_last_error[256] = "no CUDA error recorded";
+
+void note_cuda_error(cudaError_t e) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+}
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -91,6 +99,8 @@ static int grid_for(long long work, int threads) {
 using namespace pkv;
 
 extern "C" {
+
+const char *kv_last_cuda_error(void) { return g_last_error; }
 
 kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
                          kv_dtype dtype, kv_pool_t *out) {

@@ -14,15 +14,22 @@
 // The score matrix is never written to memory ("PagedAttention Nedir?",
 // "FlashAttention ile Ayni mi?").
 //
-// One CTA = one 128-query tile of one query head of one sequence, 192 threads:
-//   warps 0-3  softmax: thread r owns query row r (tensor-memory lane r);
-//   warp 4     TMA producer: Q once, then K and V tiles of 128 keys (8 blocks)
-//              into a 2-deep ring per operand;
-//   warp 5     MMA issuer: S = Q K^T and O += P V with tcgen05.mma
-//              (M=128, N=128, K=16 steps), fp32 accumulators in tensor memory.
-// Tensor memory (512 columns): S ping-pong [0,128) and [128,256), O
-// [256,384), P ping-pong (bf16 pairs) [384,448) and [448,512).  While the
-// softmax warps turn S_j into P_j the tensor core already computes S_{j+1}.
+// One CTA = two 128-query tiles (A: rows 0-127, B: rows 128-255 of a 256-query
+// slice) of one query head of one sequence; every K/V tile of 128 keys (8
+// blocks) is loaded once and used by both.  320 threads:
+//   warps 0-3  softmax of tile A (thread = query row = tensor-memory lane)
+//   warps 4-7  softmax of tile B
+//   warp 8     TMA producer: Q once, K and V into 2-deep rings
+//   warp 9     MMA issuer (tcgen05.mma, M=128, N=128, K=16 steps, fp32 in TMEM)
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512); each tile's bf16 weights P overwrite the first 64 columns of
+// its S once read.  MMA issue order per key tile j:
+//   ... PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) ...
+// so while one softmax group turns S into P the tensor core works for the
+// other.  tcgen05.mma operations of one thread run in issue order, which
+// orders PV_X(j)'s read of P before S_X(j+1) overwrites it, and makes the
+// completion of S_X(j+1) imply that of PV_X(j) (so O_X is stable when the
+// softmax warps see S_X(j+1)).
 //
 // Online softmax keeps a per-row reference maximum m and rescales O and the
 // row sum only when the running maximum exceeds m by more than 2^8, so the
@@ -39,18 +46,18 @@
 
 namespace pkv {
 
-constexpr int kPfBM = 128;           // queries per CTA
+constexpr int kPfBM = 256;           // queries per CTA (two tensor-core tiles)
 constexpr int kPfBN = 128;           // keys per tile
 constexpr int kPfD = 128;            // head dim (only size supported)
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;
 constexpr int kPfHalfBytes = 128 * 128;         // 128 rows x 64 bf16 (one half of D)
 constexpr int kPfTileBytes = 2 * kPfHalfBytes;  // 128 rows x 128 bf16
-constexpr int kPfQOff = 0;
-constexpr int kPfKOff = kPfTileBytes;                 // 2 stages
-constexpr int kPfVOff = kPfKOff + 2 * kPfTileBytes;   // 2 stages
-constexpr int kPfBarOff = kPfVOff + 2 * kPfTileBytes; // 160 KiB
-constexpr int kPfSmemBytes = kPfBarOff + 256 + 1024;  // barriers, slot, alignment slack
-constexpr float kRescaleThreshold = 8.0f;             // log2 units
+constexpr int kPfQOff = 0;                             // Q_A, Q_B
+constexpr int kPfKOff = 2 * kPfTileBytes;              // 2 stages
+constexpr int kPfVOff = kPfKOff + 2 * kPfTileBytes;    // 2 stages
+constexpr int kPfBarOff = kPfVOff + 2 * kPfTileBytes;  // 192 KiB
+constexpr int kPfSmemBytes = kPfBarOff + 256 + 1024;   // barriers, slot, alignment slack
+constexpr float kRescaleThreshold = 8.0f;              // log2 units
 
 // 2^x with the hardware approximation (relative error ~2^-22, far below the
 // bf16 rounding the weights get next); -inf gives 0.
@@ -60,8 +67,9 @@ KV_DEVICE float ex2_approx(float x) {
     return y;
 }
 
-// TMEM column map
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
+// TMEM column map: S of tile x at colS(x), O of tile x at colO(x)
+KV_DEVICE constexpr uint32_t colS(int x) { return x ? 128u : 0u; }
+KV_DEVICE constexpr uint32_t colO(int x) { return x ? 384u : 256u; }
 
 struct PrefillParams {
     const int32_t *cu_q;
@@ -83,7 +91,8 @@ struct PrefillParams {
 struct PfBars {
     uint64_t qfull;
     uint64_t kfull[2], vfull[2], kempty[2], vempty[2];
-    uint64_t sfull[2], pfull[2], pfree[2];
+    uint64_t sfull[2], pfull[2];  // per query tile
+    uint64_t done;                // all MMAs complete
     uint32_t tmem_slot;
     int abort;
 };
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         return;
     }
     const int h = hq / p.g;
-    const long long kv_end = c + min(q0 + kPfBM, T);  // keys any row of this tile can see
+    const long long kv_end = c + min(q0 + kPfBM, T);  // keys any row of this CTA can see
     const int n = (int)((kv_end + kPfBN - 1) / kPfBN);
     const int nblk = (int)((L + 15) / 16);
 
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     char *sV = smem + kPfVOff;
     PfBars *bars = reinterpret_cast<PfBars *>(smem + kPfBarOff);
 
-    if (warp == 5) {
+    if (warp == 9) {
         tc::tmem_alloc(&bars->tmem_slot, 512);
         tc::tmem_relinquish();
     }
@@ -128,8 +137,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&bars->vempty[s], 1);
             mbar_init(&bars->sfull[s], 1);
             mbar_init(&bars->pfull[s], 128);
-            mbar_init(&bars->pfree[s], 1);
         }
+        mbar_init(&bars->done, 1);
         bars->abort = 0;
         mbar_init_fence();
     }
@@ -139,15 +148,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort_flag = &bars->abort;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ================================================== TMA producer
         if (lane == 0) {
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
             tc::prefetch_tensormap(&tm_v);
-            mbar_arrive_expect_tx(&bars->qfull, kPfTileBytes);
-            tc::tma_load_3d(sQ, &tm_q, 0, hq, q_begin + q0, &bars->qfull);
-            tc::tma_load_3d(sQ + kPfHalfBytes, &tm_q, 64, hq, q_begin + q0, &bars->qfull);
+            mbar_arrive_expect_tx(&bars->qfull, 2 * kPfTileBytes);
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                tc::tma_load_3d(sQ + x * kPfTileBytes, &tm_q, 0, hq, q_begin + q0 + 128 * x, &bars->qfull);
+                tc::tma_load_3d(sQ + x * kPfTileBytes + kPfHalfBytes, &tm_q, 64, hq,
+                                q_begin + q0 + 128 * x, &bars->qfull);
+            }
             const int32_t *row = p.tables + (size_t)b * p.max_blocks;
             int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n && !*abort_flag; ++j) {
@@ -198,107 +211,114 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
                 mbar_wait(&bars->vfull[j & 1], (j >> 1) & 1, p.err);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, false, true);
             const uint32_t q_addr = smem_addr(sQ), k_addr = smem_addr(sK), v_addr = smem_addr(sV);
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint32_t d = tmem + (s ? kColS1 : kColS0);
-                const uint32_t kb = k_addr + s * kPfTileBytes;
+            auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
+                const uint32_t kb = k_addr + (j & 1) * kPfTileBytes;
+                const uint32_t qb = q_addr + x * kPfTileBytes;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t da = tc::smem_desc_sw128(q_addr + hh * kPfHalfBytes + kk * 32, 16, 1024);
+                        const uint64_t da = tc::smem_desc_sw128(qb + hh * kPfHalfBytes + kk * 32, 16, 1024);
                         const uint64_t db = tc::smem_desc_sw128(kb + hh * kPfHalfBytes + kk * 32, 16, 1024);
-                        tc::mma_ss(d, da, db, idesc_qk, (hh | kk) != 0);
+                        tc::mma_ss(tmem + colS(x), da, db, idesc_qk, (hh | kk) != 0);
                     }
-                tc::mma_commit(&bars->sfull[s]);
-                tc::mma_commit(&bars->kempty[s]);
+                tc::mma_commit(&bars->sfull[x]);
             };
-            bool ok = mbar_wait(&bars->qfull, 0, p.err);
-            for (int j = 0; ok && j < 2 && j < n; ++j) {
-                ok = mbar_wait(&bars->kfull[j], 0, p.err);
-                if (ok) {
-                    tc::fence_after_sync();
-                    issue_s(j);
-                }
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&bars->pfull[s], (j >> 1) & 1, p.err) ||
-                    !mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint32_t pcol = tmem + (s ? kColP1 : kColP0);
-                const uint32_t vb = v_addr + s * kPfTileBytes;
+            auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j
+                const uint32_t vb = v_addr + (j & 1) * kPfTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     // B = V tile, keys 16kk..16kk+15 x all 128 dims (MN-major):
                     // the two 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
                     const uint64_t db = tc::smem_desc_sw128(vb + kk * 2048, kPfHalfBytes, 1024);
-                    tc::mma_ts(tmem + kColO, pcol + kk * 8, db, idesc_pv, (j | kk) != 0);
+                    tc::mma_ts(tmem + colO(x), tmem + colS(x) + kk * 8, db, idesc_pv, (j | kk) != 0);
                 }
-                tc::mma_commit(&bars->pfree[s]);
-                tc::mma_commit(&bars->vempty[s]);
-                if (j + 2 < n) {
-                    if (!mbar_wait(&bars->kfull[s], ((j + 2) >> 1) & 1, p.err)) {
+            };
+            bool ok = mbar_wait(&bars->qfull, 0, p.err) && mbar_wait(&bars->kfull[0], 0, p.err);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc::mma_commit(&bars->kempty[0]);
+            }
+            for (int j = 0; ok && j < n; ++j) {
+                const int s = j & 1;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (!mbar_wait(&bars->pfull[x], j & 1, p.err) ||
+                        (x == 0 && !mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err))) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    issue_s(j + 2);
+                    issue_pv(x, j);
+                    if (x == 1) tc::mma_commit(&bars->vempty[s]);
+                    if (j + 1 < n) {
+                        if (x == 0 && !mbar_wait(&bars->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        issue_s(x, j + 1);
+                        if (x == 1) tc::mma_commit(&bars->kempty[(j + 1) & 1]);
+                    }
                 }
             }
+            tc::mma_commit(&bars->done);
             if (!ok) *abort_flag = 1;
         }
     } else {
         // ================================================== softmax warps
-        const int r = tid;  // query row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const bool row_valid = q0 + r < T;
+        const int x = warp >> 2;       // query tile
+        const int r = tid & 127;       // query row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int qrow = q0 + 128 * x + r;
+        const bool row_valid = qrow < T;
         // Invalid rows (past the chunk) see every key; they are never stored.
-        const long long qpos = row_valid ? c + q0 + r : L - 1;
+        const long long qpos = row_valid ? c + qrow : L - 1;
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             if (*abort_flag) { ok = false; break; }
-            const int s = j & 1;
-            if (!mbar_wait(&bars->sfull[s], (j >> 1) & 1, p.err)) { ok = false; break; }
+            if (!mbar_wait(&bars->sfull[x], j & 1, p.err)) { ok = false; break; }
             tc::fence_after_sync();
-            // S row: four 32-column loads in flight, one wait.
-            uint32_t sv[128];
-            {
-                uint32_t (&a)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[0]);
-                uint32_t (&b2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[32]);
-                uint32_t (&c2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[64]);
-                uint32_t (&d2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sv[96]);
-                const uint32_t sc = tmem + lane_base + (s ? kColS1 : kColS0);
-                tc::tmem_ld32(sc, a);
-                tc::tmem_ld32(sc + 32, b2);
-                tc::tmem_ld32(sc + 64, c2);
-                tc::tmem_ld32(sc + 96, d2);
-                tc::tmem_wait_ld();
-            }
             const long long key0 = (long long)j * kPfBN;
-            if (key0 + kPfBN - 1 > qpos) {
-                // diagonal tile: keys past this row's position get -inf
-#pragma unroll
-                for (int k = 0; k < 128; ++k)
-                    if (key0 + k > qpos) sv[k] = __float_as_uint(-INFINITY);
-            }
-            // raw row maximum with eight independent chains (scale > 0, so
-            // max(scale * s) = scale * max(s))
+            // Keys past this row's position are masked: column k is kept iff
+            // k <= lim.  Only tiles on the diagonal need it; the branch is
+            // warp-uniform so interior tiles pay nothing.
+            const int lim = (int)max(-1LL, min(127LL, qpos - key0));
+            const bool diag = __any_sync(0xffffffffu, lim < 127);
+            const uint32_t scol = tmem + lane_base + colS(x);
+            // pass 1: raw row maximum (scale > 0, so max(scale*s) = scale*max(s)),
+            // 64 columns per round, eight independent chains
             float mx[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sv[k]);
+            for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-            for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sv[k]));
+            for (int half = 0; half < 2; ++half) {
+                uint32_t a[32], b2[32];
+                tc::tmem_ld32(scol + 64 * half, a);
+                tc::tmem_ld32(scol + 64 * half + 32, b2);
+                tc::tmem_wait_ld();
+                if (diag) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const float va = 64 * half + k <= lim ? __uint_as_float(a[k]) : -INFINITY;
+                        const float vb = 64 * half + 32 + k <= lim ? __uint_as_float(b2[k]) : -INFINITY;
+                        mx[k & 7] = fmaxf(mx[k & 7], fmaxf(va, vb));
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        mx[k & 7] = fmaxf(mx[k & 7], fmaxf(__uint_as_float(a[k]), __uint_as_float(b2[k])));
+                }
+            }
             const float mrow = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
                                p.scale_log2;
@@ -312,75 +332,81 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 l_sum *= alpha;
                 rescale = true;
             }
-            // P_j goes into buffer s: PV_{j-2} must have consumed it.
-            if (j >= 2 && !mbar_wait(&bars->pfree[s], ((j - 2) >> 1) & 1, p.err)) { ok = false; break; }
             if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold PV_{j-1} before it is rescaled.
-                const int sp = (j - 1) & 1;
-                if (!mbar_wait(&bars->pfree[sp], ((j - 1) >> 1) & 1, p.err)) { ok = false; break; }
-                tc::fence_after_sync();
+                // O_x holds PV_x(j-1): its completion precedes S_x(j)'s.
                 uint32_t v[32];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    tc::tmem_ld32(tmem + lane_base + kColO + 32 * i, v);
+                    tc::tmem_ld32(tmem + lane_base + colO(x) + 32 * i, v);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-                    tc::tmem_st32(tmem + lane_base + kColO + 32 * i, v);
+                    tc::tmem_st32(tmem + lane_base + colO(x) + 32 * i, v);
                 }
-                tc::tmem_wait_st();
             }
-            // p = 2^(scale*s - m): packed fma, hardware exp2, bf16 pairs
+            // pass 2: p = 2^(scale*s - m) with a packed fma and the hardware
+            // exp2, bf16 pairs written over the first 64 columns of this S
+            // (columns 64h..64h+63 of S are read before P half h is stored)
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_used, -m_used);
             float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                               make_float2(0.f, 0.f)};
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                uint32_t w[32];
+                uint32_t a[32], b2[32], w[32];
+                tc::tmem_ld32(scol + 64 * half, a);
+                tc::tmem_ld32(scol + 64 * half + 32, b2);
+                tc::tmem_wait_ld();
+                if (diag) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        if (64 * half + k > lim) a[k] = __float_as_uint(-INFINITY);
+                        if (64 * half + 32 + k > lim) b2[k] = __float_as_uint(-INFINITY);
+                    }
+                }
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[64 * half + 2 * k]),
-                                                            __uint_as_float(sv[64 * half + 2 * k + 1])),
-                                                sc2, nm2);
-                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    const uint32_t *src = k < 16 ? a : b2;
+                    const int kk = 2 * (k & 15);
+                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(src[kk]), __uint_as_float(src[kk + 1])),
+                                                 sc2, nm2);
+                    const float2 e = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
                     acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
                     w[k] = tc::pack_bf16x2(e.x, e.y);
                 }
-                tc::tmem_st32(tmem + lane_base + (s ? kColP1 : kColP0) + 32 * half, w);
+                tc::tmem_st32(scol + 32 * half, w);
             }
             l_sum += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y) + (acc2[2].x + acc2[2].y) +
                      (acc2[3].x + acc2[3].y);
             tc::tmem_wait_st();
-            if (key0 + kPfBN > L) {
+            if (x == 0 && key0 + kPfBN > L) {
                 // Keys at or past L: the V rows there may hold anything; zero
                 // them so the zero weights cannot meet a NaN in the tensor core.
+                // Tile A's PV runs first, so A's warps do it for both tiles.
+                const int s = j & 1;
                 if (!mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err)) { ok = false; break; }
                 const int first = (int)(L - key0);
                 char *vt = sV + s * kPfTileBytes;
                 for (int idx = r; idx < (kPfBN - first) * 16; idx += 128) {
-                    const int row = first + idx / 16, chunk = idx % 16;
-                    *reinterpret_cast<uint4 *>(vt + (chunk >> 3) * kPfHalfBytes + row * 128 +
+                    const int rw = first + idx / 16, chunk = idx % 16;
+                    *reinterpret_cast<uint4 *>(vt + (chunk >> 3) * kPfHalfBytes + rw * 128 +
                                                (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
                 tc::fence_proxy_async_smem();
             }
             tc::fence_before_sync();
-            mbar_arrive(&bars->pfull[s]);
+            mbar_arrive(&bars->pfull[x]);
         }
         // ---- epilogue: O / l for this row
-        if (ok && n > 0) {
-            const int sl = (n - 1) & 1;
-            ok = mbar_wait(&bars->pfree[sl], ((n - 1) >> 1) & 1, p.err);
-        }
+        if (ok) ok = mbar_wait(&bars->done, 0, p.err);
         if (!ok) *abort_flag = 1;
         tc::fence_after_sync();
         const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        const size_t orow = ((size_t)(q_begin + q0 + r) * p.num_q_heads + hq) * kPfD;
+        const size_t orow = ((size_t)(q_begin + qrow) * p.num_q_heads + hq) * kPfD;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             uint32_t v[32];
-            tc::tmem_ld32(tmem + lane_base + kColO + 32 * i, v);
+            tc::tmem_ld32(tmem + lane_base + colO(x) + 32 * i, v);
             tc::tmem_wait_ld();
             if (row_valid && ok) {
                 if (p.out_bf16) {
@@ -404,12 +430,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
         }
         if (row_valid && ok && p.lse)
-            p.lse[(size_t)(q_begin + q0 + r) * p.num_q_heads + hq] =
+            p.lse[(size_t)(q_begin + qrow) * p.num_q_heads + hq] =
                 l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, 512);
     }
@@ -454,9 +480,9 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     pp.out_bf16 = out_dtype == KV_BF16;
     pp.lse = lse_out;
     pp.err = p->err;
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kPfSmemBytes) != cudaSuccess)
-        return KV_ERR_CUDA;
+    if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
+            prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes)))
+        return st0;
     const dim3 grid(num_q_heads, (max_q_len + kPfBM - 1) / kPfBM, batch);
     prefill_kernel<<<grid, kPfThreads, kPfSmemBytes, as_stream(stream)>>>(tm_q, p->tmap_k,
                                                                          p->tmap_v, pp);
