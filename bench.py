@@ -341,7 +341,9 @@ def run_ours(args, rank, world, local_rank):
     achieved = kv_bytes / (attend_ms * 1e-3) / 1e9
     src = source_hash("paged_kv_cache_196_gb300/csrc/decode.cu",
                       "paged_kv_cache_196_gb300/csrc/common.cuh")
-    traffic = recorded_traffic("decode_kernel", args.workload, src)
+    # bf16 / head_dim 128 with >= 3 query heads per kv head runs the tensor-core kernel
+    kname = "decode_tc_kernel" if (hq // hkv >= 3 and d == 128) else "decode_kernel"
+    traffic = recorded_traffic(kname, args.workload, src)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -372,7 +374,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {
             "bound": "hbm",
             "kernel": ("contig_decode_attention" if contig else "paged_decode_attention")
-                      + " (decode kernel" + (" + split merge kernel)" if max_splits > 1 else ")"),
+                      + f" ({kname}" + (" + split merge kernel)" if max_splits > 32 else ")"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
@@ -589,7 +591,11 @@ def run_prefill(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention (prefill_kernel)",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": f"{kind} dense bf16 (cuBLAS burst)", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("prefill_kernel", "yi34b_prefill", source_hash(
+                         "paged_kv_cache_196_gb300/csrc/prefill.cu",
+                         "paged_kv_cache_196_gb300/csrc/tc.cuh",
+                         "paged_kv_cache_196_gb300/csrc/common.cuh")),
                      "algorithmic_flop_per_launch": flops, "avg_launch_ms": round(attend_ms, 4)},
         "gpu_launches": 2 * K, "clocks": clk,
     }
