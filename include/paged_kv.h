@@ -133,6 +133,21 @@ kv_status kv_prepare_append(kv_allocator_t a, int block_size, int32_t *table_row
                             int64_t *slots_out, int32_t *cow_src, int32_t *cow_dst,
                             int *n_cow);
 
+/* The host step of a whole batch in one call: kv_prepare_append for every
+ * sequence b in order, with
+ *   tables      host int32[batch][max_blocks] (rows updated in place);
+ *   num_blocks  host int32[batch] (in/out);
+ *   cur_lens    host int64[batch]; n_new host int32[batch];
+ *   slots_out   host int64[sum n_new], sequence b's slots after those of b-1;
+ *   cow_src/cow_dst host int32[*n_cow] capacity, *n_cow pairs on return.
+ * The whole batch is planned before anything changes: on KV_ERR_OOM or
+ * KV_ERR_ARG no table, count or refcount is modified.  A block shared by
+ * several sequences of the batch is copied for every writer but the last. */
+kv_status kv_prepare_append_batch(kv_allocator_t a, int block_size, int batch, int32_t *tables,
+                                  int max_blocks, int32_t *num_blocks, const int64_t *cur_lens,
+                                  const int32_t *n_new, int64_t *slots_out, int32_t *cow_src,
+                                  int32_t *cow_dst, int *n_cow);
+
 /* ======================================================================
  * Device pool.
  * ==================================================================== */

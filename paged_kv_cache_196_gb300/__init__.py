@@ -18,7 +18,7 @@ __all__ = [
     "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_last_cuda_error", "kv_blocks_for_tokens",
     "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
-    "kv_allocator_num_free", "kv_prepare_append", "kv_pool_create", "kv_pool_destroy",
+    "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch", "kv_pool_create", "kv_pool_destroy",
     "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
@@ -61,6 +61,7 @@ _SIGS = {
     "kv_allocator_refcount": [_vp, ctypes.c_int32, _P(_i32)],
     "kv_allocator_num_free": [_vp, _P(_i32)],
     "kv_prepare_append": [_vp, _i32, _vp, _i32, _P(_i32), _i64, _i32, _vp, _vp, _vp, _P(_i32)],
+    "kv_prepare_append_batch": [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _P(_i32)],
     "kv_pool_create": [_i32, _i32, _i32, _i32, _i32, _P(_vp)],
     "kv_pool_destroy": [_vp],
     "kv_pool_ptrs": [_vp, _P(_vp), _P(_vp)],
@@ -208,6 +209,20 @@ def kv_prepare_append(a: int, table_row, num_blocks: int, cur_len: int, n_new: i
                                    _ptr(cow_src), _ptr(cow_dst), ctypes.byref(ncow)),
            "kv_prepare_append")
     return nb.value, ncow.value
+
+
+def kv_prepare_append_batch(a: int, tables, num_blocks, cur_lens, n_new, slots_out, cow_src,
+                            cow_dst, block_size: int = 16) -> int:
+    """Batched host step.  tables int32 [B][max_blocks], num_blocks int32 [B] (updated in
+    place), cur_lens int64 [B], n_new int32 [B], slots_out int64 [sum n_new], cow_src /
+    cow_dst int32 (capacity = their length).  Returns the number of copy pairs."""
+    ncow = _i32(len(cow_src))
+    _check(lib().kv_prepare_append_batch(a, block_size, tables.shape[0], _ptr(tables),
+                                         tables.shape[1], _ptr(num_blocks), _ptr(cur_lens),
+                                         _ptr(n_new), _ptr(slots_out), _ptr(cow_src),
+                                         _ptr(cow_dst), ctypes.byref(ncow)),
+           "kv_prepare_append_batch")
+    return ncow.value
 
 
 # ---------------------------------------------------------------- pool

@@ -195,4 +195,65 @@ kv_status kv_prepare_append(kv_allocator_t a, int block_size, int32_t *table_row
     return KV_OK;
 }
 
+kv_status kv_prepare_append_batch(kv_allocator_t a, int block_size, int batch, int32_t *tables,
+                                  int max_blocks, int32_t *num_blocks, const int64_t *cur_lens,
+                                  const int32_t *n_new, int64_t *slots_out, int32_t *cow_src,
+                                  int32_t *cow_dst, int *n_cow) {
+    if (!a || block_size <= 0 || batch < 0 || max_blocks < 0 || !n_cow || *n_cow < 0) return KV_ERR_ARG;
+    if (batch > 0 && (!tables || !num_blocks || !cur_lens || !n_new)) return KV_ERR_ARG;
+    // Plan first, change nothing: blocks to take and copies to make for the
+    // whole batch.  A block shared by several sequences of this batch is
+    // copied by all but the last writer (whose write finds it private).
+    std::vector<int> pending;  // refcount drops planned per block
+    long long need_new = 0, need_cow = 0, total_slots = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int32_t *row = tables + (size_t)b * max_blocks;
+        const int nb = num_blocks[b];
+        const int64_t len = cur_lens[b];
+        if (nb < 0 || nb > max_blocks || len < 0 || n_new[b] < 0) return KV_ERR_ARG;
+        if ((len + block_size - 1) / block_size > nb) return KV_ERR_ARG;
+        for (int i = 0; i < nb; ++i)
+            if (row[i] < 0 || row[i] >= a->num_blocks || a->refcount[row[i]] <= 0) return KV_ERR_ARG;
+        total_slots += n_new[b];
+        if (n_new[b] == 0) continue;
+        const int64_t first = len / block_size, last = (len + n_new[b] - 1) / block_size;
+        if (last >= max_blocks) return KV_ERR_ARG;
+        for (int64_t bi = first; bi <= last; ++bi) {
+            if (bi >= nb) {
+                need_new += 1;
+                continue;
+            }
+            const int32_t id = row[bi];
+            if (pending.empty()) pending.assign(a->num_blocks, 0);
+            const int left = a->refcount[id] - pending[id];
+            if (left > 1) {  // still shared when this sequence writes: copy
+                need_cow += 1;
+                pending[id] += 1;
+            }
+        }
+    }
+    if (total_slots > 0 && !slots_out) return KV_ERR_ARG;
+    if (need_cow > *n_cow || (need_cow > 0 && (!cow_src || !cow_dst))) return KV_ERR_ARG;
+    if (need_new + need_cow > a->count) return KV_ERR_OOM;
+    // Apply, sequence by sequence (the single-sequence planner makes the same
+    // decisions in the same order).
+    int k = 0;
+    long long off = 0;
+    for (int b = 0; b < batch; ++b) {
+        int cap = *n_cow - k;
+        int nb = num_blocks[b];
+        const kv_status st = kv_prepare_append(a, block_size, tables + (size_t)b * max_blocks,
+                                               max_blocks, &nb, cur_lens[b], n_new[b],
+                                               slots_out ? slots_out + off : nullptr,
+                                               cow_src ? cow_src + k : nullptr,
+                                               cow_dst ? cow_dst + k : nullptr, &cap);
+        if (st != KV_OK) return st;  // not reached: the plan above checked every condition
+        num_blocks[b] = nb;
+        k += cap;
+        off += n_new[b];
+    }
+    *n_cow = k;
+    return KV_OK;
+}
+
 }  // extern "C"

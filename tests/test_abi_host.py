@@ -200,3 +200,61 @@ def test_split_plan_and_workspace():
     assert pk.kv_decode_workspace_size(64, 32, 8, 128, 256, 1) == 0
     ws = pk.kv_decode_workspace_size(64, 32, 8, 128, 256, 4)
     assert ws == 64 * 32 * ms * 129 * 4
+
+
+def _shared_layout(n_blocks=64):
+    """Two sequences sharing a 40-token prefix (3 blocks, the last partly used),
+    plus one private sequence."""
+    a = pk.kv_allocator_create(n_blocks)
+    none = np.zeros(0, np.int32)
+    tables = np.full((3, 8), -1, np.int32)
+    nb = np.zeros(3, np.int32)
+    nb[0], _ = pk.kv_prepare_append(a, tables[0], 0, 0, 40, np.zeros(40, np.int64), none, none)
+    tables[1, :3] = tables[0, :3]
+    pk.kv_allocator_share(a, tables[1, :3])
+    nb[1] = 3
+    nb[2], _ = pk.kv_prepare_append(a, tables[2], 0, 0, 20, np.zeros(20, np.int64), none, none)
+    return a, tables, nb
+
+
+def test_batched_planner_matches_sequential_planner():
+    a1, t1, nb1 = _shared_layout()
+    a2, t2, nb2 = _shared_layout()
+    lens = np.array([40, 40, 20], np.int64)
+    n_new = np.array([1, 30, 5], np.int32)
+    # sequential
+    slots_seq, pairs_seq = [], []
+    cs, cd = np.zeros(4, np.int32), np.zeros(4, np.int32)
+    for b in range(3):
+        s = np.zeros(n_new[b], np.int64)
+        nb1[b], nc = pk.kv_prepare_append(a1, t1[b], int(nb1[b]), int(lens[b]), int(n_new[b]), s,
+                                          cs, cd)
+        slots_seq.append(s)
+        pairs_seq += list(zip(cs[:nc], cd[:nc]))
+    # batched
+    slots = np.zeros(int(n_new.sum()), np.int64)
+    src, dst = np.zeros(8, np.int32), np.zeros(8, np.int32)
+    nc = pk.kv_prepare_append_batch(a2, t2, nb2, lens, n_new, slots, src, dst)
+    np.testing.assert_array_equal(t1, t2)
+    np.testing.assert_array_equal(nb1, nb2)
+    np.testing.assert_array_equal(slots, np.concatenate(slots_seq))
+    assert list(zip(src[:nc], dst[:nc])) == pairs_seq
+    # the shared, partly used block 2 was copied once, for the first writer
+    # (sequence 0); the second writer (sequence 1) then found it private
+    assert nc == 1 and pairs_seq[0] == (t1[1, 2], t1[0, 2])
+
+
+def test_batched_planner_changes_nothing_on_failure():
+    a, t, nb = _shared_layout(n_blocks=7)  # 5 used, 2 free
+    before = (t.copy(), nb.copy(), pk.kv_allocator_num_free(a))
+    lens = np.array([40, 40, 20], np.int64)
+    n_new = np.array([1, 60, 1], np.int32)  # needs more blocks than are free
+    with pytest.raises(pk.KVError) as e:
+        pk.kv_prepare_append_batch(a, t, nb, lens, n_new, np.zeros(62, np.int64),
+                                   np.zeros(8, np.int32), np.zeros(8, np.int32))
+    assert e.value.status == -2
+    np.testing.assert_array_equal(t, before[0])
+    np.testing.assert_array_equal(nb, before[1])
+    assert pk.kv_allocator_num_free(a) == before[2]
+    for blk in t[0, :3]:
+        assert pk.kv_allocator_refcount(a, int(blk)) == 2
