@@ -49,6 +49,9 @@ DESCR = {
                                "(cuMemMap-backed) KV path, same inputs as yi6b_long_decode",
     "yi34b_prefill": "Yi-34B-shaped chunked causal paged prefill: 4 seqs x (8192 cached + 2048 "
                      "new) tokens in shuffled 16-token blocks, 56q/8kv heads, head_dim 128, bf16",
+    "shared_prefix_step": "append + decode step with shared prefix: 256 seqs, ctx U[128,2048], groups "
+                          "of 16 share a 1024-token prefix (refcounted blocks, copy-on-write), "
+                          "32q/8kv heads, head_dim 128, bf16",
 }
 PREFILL_METRIC = "chunked causal paged prefill tensor TFLOP/s (fraction of dense bf16 peak)"
 
@@ -558,6 +561,7 @@ def run_prefill(args, rank, world, local_rank):
         raise RuntimeError("device error word set after warm-up")
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -566,6 +570,7 @@ def run_prefill(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(K):
+        ea[i].record()
         append()
         ev[i][0].record()
         attend()
@@ -575,6 +580,8 @@ def run_prefill(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = e0.elapsed_time(e1)
     attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    append_ms = float(np.mean([a.elapsed_time(b[0]) for a, b in zip(ea, ev)]))
+    append_bytes = 2 * 2 * T * hkv * d * 2 + 8 * T  # read k/v_new, write the pool, slots
     if pk.kv_get_device_error(pool):
         raise RuntimeError("device error word set after the timed region")
     peak, kind = read_tensor_peak()
@@ -588,6 +595,9 @@ def run_prefill(args, rank, world, local_rank):
                    "flop_per_step": flops, "append_tokens_per_step": T,
                    "l2": "KV 168 MB + Q 117 MB per step, larger than L2; no flush"},
         "prefill_tokens_per_s": round(T * K / (total_ms * 1e-3), 1),
+        "append": {"tokens": T, "bytes": append_bytes, "avg_ms": round(append_ms, 5),
+                   "gbs": round(append_bytes / (append_ms * 1e-3) / 1e9, 1),
+                   "frac_of_hbm_peak": round(append_bytes / (append_ms * 1e-3) / 1e9 / read_peaks()[0], 4)},
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention (prefill_kernel)",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": f"{kind} dense bf16 (cuBLAS burst)", "unit": "TFLOP/s",
@@ -600,6 +610,145 @@ def run_prefill(args, rank, world, local_rank):
         "gpu_launches": 2 * K, "clocks": clk,
     }
     return line
+
+
+def run_shared_prefix(args, rank, world, local_rank):
+    """One decode step over sequences that share prefix blocks: the planned
+    copy-on-write block copies, the append of every sequence's new token and
+    paged decode attention over the L+1 tokens."""
+    import torch
+
+    import paged_kv_cache_196_gb300 as pk
+
+    torch.cuda.set_device(local_rank)
+    inp = W.shared_prefix_inputs()
+    lens = inp["lens"]
+    B, G, P = len(lens), inp["group_size"], inp["prefix_len"]
+    hkv, d = inp["new_k"].shape[1], inp["new_k"].shape[2]
+    hq = inp["q"].shape[1]
+    max_blocks = (int(lens.max()) + 1 + 15) // 16
+    need = sum(-(-(int(L) + 1) // 16) for L in lens)
+    nb = int(math.ceil(1.2 * need)) + (B // G + 1) * (P // 16)
+    pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+    alloc = pk.kv_pool_allocator(pool)
+    pk.kv_allocator_set_order(alloc, W.permutation(W.rng(W.CONFIGS["shared_prefix_step"]["seed"] + 7), nb))
+    none = np.zeros(0, np.int32)
+    tables = np.full((B, max_blocks), -1, np.int32)
+    nblocks = np.zeros(B, np.int32)
+    templates = {}
+
+    def put(k, v, slots):
+        if len(slots):
+            pk.kv_append(pool, torch.from_numpy(np.ascontiguousarray(k).view(np.int16)).cuda(),
+                         torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).cuda(),
+                         torch.from_numpy(np.asarray(slots, np.int64)).cuda(), len(slots))
+
+    for b in range(B):  # the cache as it stands before the step (shared prefixes)
+        g, L = b // G, int(lens[b])
+        if g not in templates:
+            row = np.full(P // 16, -1, np.int32)
+            s = np.zeros(P, np.int64)
+            pk.kv_prepare_append(alloc, row, 0, 0, P, s, none, none)
+            put(inp["prefix_k"][g], inp["prefix_v"][g], s)
+            templates[g] = row
+        nbp = -(-min(L, P) // 16)
+        tables[b, :nbp] = templates[g][:nbp]
+        pk.kv_allocator_share(alloc, tables[b, :nbp])
+        nblocks[b] = nbp
+        if L > P:
+            s = np.zeros(L - P, np.int64)
+            nblocks[b], _ = pk.kv_prepare_append(alloc, tables[b], int(nblocks[b]), P, L - P, s,
+                                                 none, none)
+            put(inp["suffix_k"][b], inp["suffix_v"][b], s)
+    for row in templates.values():
+        pk.kv_allocator_free(alloc, row)
+    # ---- host step: plan the whole batch's appends (new blocks, copy-on-write)
+    slots = np.zeros(B, np.int64)
+    cow_src, cow_dst = np.zeros(B, np.int32), np.zeros(B, np.int32)
+    t0 = time.perf_counter()
+    n_cow = pk.kv_prepare_append_batch(alloc, tables, nblocks, lens.astype(np.int64),
+                                       np.ones(B, np.int32), slots, cow_src, cow_dst)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    new_lens = (lens + 1).astype(np.int32)
+    logical_bytes = int(new_lens.sum()) * 2 * hkv * d * 2
+    held = {}  # tokens each distinct physical block holds for its longest user
+    for b in range(B):
+        for i in range(int(nblocks[b])):
+            blk = int(tables[b, i])
+            held[blk] = max(held.get(blk, 0), min(16, int(new_lens[b]) - 16 * i))
+    unique_tokens = sum(held.values())
+    unique_bytes = unique_tokens * 2 * hkv * d * 2
+    d_src = torch.from_numpy(cow_src[:max(n_cow, 1)]).cuda()
+    d_dst = torch.from_numpy(cow_dst[:max(n_cow, 1)]).cuda()
+    d_slots = torch.from_numpy(slots).cuda()
+    d_tables = torch.from_numpy(tables).cuda()
+    d_lens = torch.from_numpy(new_lens).cuda()
+    k_new = torch.from_numpy(inp["new_k"].view(np.int16)).cuda()
+    v_new = torch.from_numpy(inp["new_v"].view(np.int16)).cuda()
+    q = torch.from_numpy(inp["q"].view(np.int16)).cuda()
+    out = torch.empty((B, hq, d), dtype=torch.int16, device="cuda")
+    splits = args.splits if args.splits > 0 else pk.kv_decode_plan(new_lens, hkv, max_blocks)
+    ws_bytes = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, splits)
+    ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+
+    def step(ev=None):
+        if n_cow:
+            pk.kv_copy_blocks(pool, d_src, d_dst, n_cow)
+        pk.kv_append(pool, k_new, v_new, d_slots, B)
+        if ev is not None:
+            ev[0].record()
+        pk.paged_decode_attention(pool, q, d_tables, max_blocks, d_lens, B, hq, scale, out,
+                                  pk.KV_BF16, None, splits, ws, ws_bytes)
+        if ev is not None:
+            ev[1].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pk.kv_get_device_error(pool):
+        raise RuntimeError("device error word set after warm-up")
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        step(evs[i])
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    if pk.kv_get_device_error(pool):
+        raise RuntimeError("device error word set after the timed region")
+    peak, peak_kind = read_peaks()
+    achieved = logical_bytes / (dec_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": round(logical_bytes * K / (total_ms * 1e-3) / 1e9, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR["shared_prefix_step"], "name": "shared_prefix_step",
+                   "batch": B, "logical_kv_bytes_per_step": logical_bytes,
+                   "unique_kv_bytes_per_step": unique_bytes, "cow_copies_per_step": n_cow,
+                   "cow_bytes_per_step": n_cow * 2 * hkv * 16 * d * 2 * 2,
+                   "host_plan_ms": round(plan_ms, 3), "num_splits": splits,
+                   "l2": "logical KV read per step larger than L2; shared prefix blocks are re-read "
+                         "by every sequence of a group (L2 hits possible)"},
+        "decode_tokens_per_s": round(B * K / (total_ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (decode_tc_kernel)",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (logical bytes; shared blocks "
+                                  "re-read from L2 can exceed it)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": logical_bytes, "avg_launch_ms": round(dec_ms, 5)},
+        "gpu_launches": (3 if n_cow else 2) * K, "clocks": clk,
+    }
 
 
 def main():
@@ -623,7 +772,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return  # the reference arm runs on rank 0 only
-        if args.workload == "yi34b_prefill":
+        if args.workload in ("yi34b_prefill", "shared_prefix_step"):
             print(json.dumps({"impl": "reference", "unavailable":
                               "the reference arm times the decode workloads only"}), flush=True)
             return
@@ -638,6 +787,8 @@ def main():
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.workload == "yi34b_prefill":
         line = run_prefill(args, rank, world, local_rank)
+    elif args.workload == "shared_prefix_step":
+        line = run_shared_prefix(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0:
