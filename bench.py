@@ -92,6 +92,25 @@ def recorded_traffic(kernel: str, workload: str, src_hash: str):
     return None
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time (ms).  All ranks call it; with one process it
+    returns ms unchanged."""
+    import torch
+    import torch.distributed as tdist
+
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job rate: every rank processed units_per_rank per step (weak
+    scaling), the job took the slowest rank's time."""
+    return world * units_per_rank * steps / (slowest_ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
 
@@ -288,13 +307,10 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device="cuda")
     ms_per_step = total_ms / K
-    value = world * kv_bytes * K / (total_ms * 1e-3) / 1e9
-    tokens_per_s = world * B * K / (total_ms * 1e-3)
+    value = job_throughput(kv_bytes, K, world, total_ms) / 1e9
+    tokens_per_s = job_throughput(B, K, world, total_ms)
 
     # ---- end to end through the public API with host buffers
     Ke = min(K, 2000)
@@ -330,11 +346,8 @@ def run_ours(args, rank, world, local_rank):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * kv_bytes * Ke / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, device="cuda")
+    e2e_value = job_throughput(kv_bytes, Ke, world, e2e_ms) / 1e9
 
     err = pk.kv_contig_get_device_error(ctx) if contig else pk.kv_get_device_error(pool)
     if err:

@@ -22,10 +22,13 @@ _lib = None
 
 
 def lib():
-    """Load (building if needed) the oracle shared library."""
+    """Load (building if needed) the oracle shared library.
+
+    ORACLE_LIB, if set, names another build of oracle.c to load instead; the
+    mutation tests use it to check that the pins catch planted mistakes."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = os.environ.get("ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         L.oracle_blocks_needed.restype = i64
