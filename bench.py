@@ -49,6 +49,8 @@ DESCR = {
                                "(cuMemMap-backed) KV path, same inputs as yi6b_long_decode",
     "yi34b_prefill": "Yi-34B-shaped chunked causal paged prefill: 4 seqs x (8192 cached + 2048 "
                      "new) tokens in shuffled 16-token blocks, 56q/8kv heads, head_dim 128, bf16",
+    "swap_blocks": "swap 2048 shuffled 64 KiB blocks (Llama-3-8B-shaped pool, 8 kv heads, d128, "
+                   "bf16) out to pinned host memory and back in",
     "shared_prefix_step": "append + decode step with shared prefix: 256 seqs, ctx U[128,2048], groups "
                           "of 16 share a 1024-token prefix (refcounted blocks, copy-on-write), "
                           "32q/8kv heads, head_dim 128, bf16",
@@ -764,6 +766,61 @@ def run_shared_prefix(args, rank, world, local_rank):
     }
 
 
+def run_swap(args, rank, world, local_rank):
+    """Swap-out then swap-in of 2048 blocks between the pool and pinned host
+    memory (kernels that store to / load from the host buffer directly),
+    against one copy-engine transfer of the same bytes each way."""
+    import torch
+
+    import paged_kv_cache_196_gb300 as pk
+
+    torch.cuda.set_device(local_rank)
+    cfg = W.CONFIGS["llama3_8b_decode"]
+    hkv, d, nb, n = cfg["num_kv_heads"], cfg["head_dim"], 8192, 2048
+    pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+    ids = torch.from_numpy(W.permutation(W.rng(cfg["seed"]), nb)[:n]).cuda()
+    nbytes = pk.kv_swap_bytes(pool, n)
+    buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def time_it(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    t_out = time_it(lambda: pk.kv_swap_out(pool, ids, n, buf))
+    t_in = time_it(lambda: pk.kv_swap_in(pool, ids, n, buf))
+    t_d2h = time_it(lambda: buf.copy_(dbuf, non_blocking=True))
+    t_h2d = time_it(lambda: dbuf.copy_(buf, non_blocking=True))
+    if pk.kv_get_device_error(pool):
+        raise RuntimeError("device error word set")
+    gbs = lambda ms: round(nbytes / (ms * 1e-3) / 1e9, 1)
+    total_ms = t_out + t_in
+    return {
+        "metric": "swap block-copy GB/s (pool <-> pinned host)", "value": round(2 * nbytes / (total_ms * 1e-3) / 1e9, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR["swap_blocks"], "name": "swap_blocks", "blocks": n,
+                   "bytes_each_way": nbytes},
+        "swap_out_gbs": gbs(t_out), "swap_in_gbs": gbs(t_in),
+        "roofline": {"bound": "host link", "kernel": "swap_blocks_kernel",
+                     "achieved": round(nbytes / (min(t_out, t_in) * 1e-3) / 1e9, 1),
+                     "peak": max(gbs(t_d2h), gbs(t_h2d)),
+                     "peak_kind": "copy-engine transfer of the same bytes measured in this run",
+                     "unit": "GB/s", "frac": round(min(t_d2h, t_h2d) / min(t_out, t_in), 4),
+                     "traffic": None, "copy_engine_d2h_gbs": gbs(t_d2h), "copy_engine_h2d_gbs": gbs(t_h2d)},
+        "gpu_launches": 2 * args.steps, "clocks": None,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -785,7 +842,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return  # the reference arm runs on rank 0 only
-        if args.workload in ("yi34b_prefill", "shared_prefix_step"):
+        if args.workload in ("yi34b_prefill", "shared_prefix_step", "swap_blocks"):
             print(json.dumps({"impl": "reference", "unavailable":
                               "the reference arm times the decode workloads only"}), flush=True)
             return
@@ -802,6 +859,8 @@ def main():
         line = run_prefill(args, rank, world, local_rank)
     elif args.workload == "shared_prefix_step":
         line = run_shared_prefix(args, rank, world, local_rank)
+    elif args.workload == "swap_blocks":
+        line = run_swap(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0:

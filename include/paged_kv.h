@@ -184,6 +184,22 @@ kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
 kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, int n,
                          void *stream);
 
+/* Swap / preemption ("Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve
+ * Gerceklik": when GPU memory is full, blocks are moved to CPU memory).
+ * kv_swap_out copies every head and slot of K and V of the listed blocks
+ * (device int32[n]) into host_buf, laid out [n][K then V][num_kv_heads][16]
+ * [head_dim]; kv_swap_in copies them back into the listed blocks (which may
+ * differ from the ones swapped out).  host_buf must be addressable by the GPU
+ * (pinned host memory: cudaHostAlloc / cudaHostRegister, or a torch pinned
+ * tensor), 16-byte aligned, kv_swap_bytes(n) long; a kernel reads / writes it
+ * directly, so on this machine the bytes cross NVLink-C2C.  Out-of-range ids
+ * are skipped and set KV_DEVERR_BLOCK_RANGE.  The refcounts are the caller's
+ * business: swap out, kv_allocator_free; later alloc + swap in. */
+kv_status kv_swap_out(kv_pool_t p, const int32_t *block_ids, int n, void *host_buf, void *stream);
+kv_status kv_swap_in(kv_pool_t p, const int32_t *block_ids, int n, const void *host_buf,
+                     void *stream);
+kv_status kv_swap_bytes(kv_pool_t p, int n, size_t *bytes);
+
 /* Scratch memory the decode call needs for a split plan: partial outputs
  * fp32 [batch][num_q_heads][splits][head_dim] and their log-sum-exp
  * [batch][num_q_heads][splits].  num_splits as in paged_decode_attention

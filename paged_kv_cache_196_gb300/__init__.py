@@ -19,7 +19,8 @@ __all__ = [
     "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
     "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch", "kv_pool_create", "kv_pool_destroy",
-    "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks",
+    "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks", "kv_swap_out",
+    "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
@@ -68,6 +69,9 @@ _SIGS = {
     "kv_pool_allocator": [_vp, _P(_vp)],
     "kv_append": [_vp, _vp, _vp, _vp, _i32, _vp],
     "kv_copy_blocks": [_vp, _vp, _vp, _i32, _vp],
+    "kv_swap_out": [_vp, _vp, _i32, _vp, _vp],
+    "kv_swap_in": [_vp, _vp, _i32, _vp, _vp],
+    "kv_swap_bytes": [_vp, _i32, _P(_sz)],
     "kv_decode_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
     "kv_decode_split_plan": [_i32, _i32, _i32, _i32, _P(_i32), _P(_i32)],
     "kv_decode_plan": [_vp, _i32, _i32, _i32, _P(_i32)],
@@ -257,6 +261,20 @@ def kv_append(p: int, k_new, v_new, slot_mapping, num_tokens: int, stream=None):
 
 def kv_copy_blocks(p: int, src, dst, n: int, stream=None):
     _check(lib().kv_copy_blocks(p, _ptr(src), _ptr(dst), n, _stream(stream)), "kv_copy_blocks")
+
+
+def kv_swap_out(p: int, block_ids, n: int, host_buf, stream=None):
+    _check(lib().kv_swap_out(p, _ptr(block_ids), n, _ptr(host_buf), _stream(stream)), "kv_swap_out")
+
+
+def kv_swap_in(p: int, block_ids, n: int, host_buf, stream=None):
+    _check(lib().kv_swap_in(p, _ptr(block_ids), n, _ptr(host_buf), _stream(stream)), "kv_swap_in")
+
+
+def kv_swap_bytes(p: int, n: int) -> int:
+    r = _sz()
+    _check(lib().kv_swap_bytes(p, n, ctypes.byref(r)), "kv_swap_bytes")
+    return r.value
 
 
 def kv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,

@@ -87,6 +87,39 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
     }
 }
 
+// Swap: whole blocks (K and V, all heads) between the pool and a buffer the
+// GPU can address directly (pinned host memory on this system: the stores /
+// loads cross NVLink-C2C or PCIe).  Host layout: [n][K|V][block chunks].
+// dir = 0: pool -> host (swap out); dir = 1: host -> pool (swap in).
+__global__ void __launch_bounds__(256) swap_blocks_kernel(uint4 *__restrict__ k_pool,
+                                                          uint4 *__restrict__ v_pool,
+                                                          uint4 *__restrict__ host,
+                                                          const int32_t *__restrict__ ids, int n,
+                                                          int block_chunks, int num_blocks, int dir,
+                                                          int *err) {
+    const long long total = (long long)n * block_chunks;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int p = (int)(i / block_chunks);
+        const int c = (int)(i - (long long)p * block_chunks);
+        const int id = __ldg(ids + p);
+        if (id < 0 || id >= num_blocks) {
+            if (c == 0) atomicOr(err, KV_DEVERR_BLOCK_RANGE);
+            continue;
+        }
+        uint4 *hk = host + (2LL * p) * block_chunks + c;
+        uint4 *hv = hk + block_chunks;
+        const long long pc = (long long)id * block_chunks + c;
+        if (dir == 0) {
+            *hk = k_pool[pc];
+            *hv = v_pool[pc];
+        } else {
+            k_pool[pc] = *hk;
+            v_pool[pc] = *hv;
+        }
+    }
+}
+
 static int grid_for(long long work, int threads) {
     long long blocks = (work + threads - 1) / threads;
     long long cap = (long long)sm_count() * 16;
@@ -186,6 +219,33 @@ kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, in
     copy_blocks_kernel<<<grid_for((long long)n * block_chunks, 256), 256, 0, as_stream(stream)>>>(
         (uint4 *)p->k, (uint4 *)p->v, src, dst, n, block_chunks, p->num_blocks, p->err);
     return cuda_status(cudaGetLastError());
+}
+
+static kv_status swap(kv_pool_t p, const int32_t *ids, int n, void *host, int dir, void *stream) {
+    if (!p || n < 0) return KV_ERR_ARG;
+    if (n == 0) return KV_OK;
+    if (!ids || !host || (reinterpret_cast<uintptr_t>(host) & 15)) return KV_ERR_ARG;
+    const int block_chunks = p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype) / 16;
+    const long long total = (long long)n * block_chunks;
+    swap_blocks_kernel<<<grid_for(total, 256), 256, 0, as_stream(stream)>>>(
+        (uint4 *)p->k, (uint4 *)p->v, (uint4 *)host, ids, n, block_chunks, p->num_blocks, dir,
+        p->err);
+    return cuda_status(cudaGetLastError());
+}
+
+kv_status kv_swap_out(kv_pool_t p, const int32_t *block_ids, int n, void *host_buf, void *stream) {
+    return swap(p, block_ids, n, host_buf, 0, stream);
+}
+
+kv_status kv_swap_in(kv_pool_t p, const int32_t *block_ids, int n, const void *host_buf,
+                     void *stream) {
+    return swap(p, block_ids, n, const_cast<void *>(host_buf), 1, stream);
+}
+
+kv_status kv_swap_bytes(kv_pool_t p, int n, size_t *bytes) {
+    if (!p || n < 0 || !bytes) return KV_ERR_ARG;
+    *bytes = (size_t)n * 2 * p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype);
+    return KV_OK;
 }
 
 kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream) {
