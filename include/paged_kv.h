@@ -149,6 +149,49 @@ kv_status kv_prepare_append_batch(kv_allocator_t a, int block_size, int batch, i
                                   int32_t *cow_dst, int *n_cow);
 
 /* ======================================================================
+ * Prefix cache ("PagedAttention Nedir?", "Prefix Sharing Nasil Calisir?":
+ * the KV of a common prompt prefix is reused when the tokens and the context
+ * before them match exactly; blocks are keyed by their contents plus the
+ * preceding context).  Host only.
+ *
+ * Full blocks only.  Block i's key mixes block i-1's key with block i's token
+ * ids; each entry also keeps its tokens and parent key and a lookup compares
+ * them, so hash collisions cannot cause a false match.  The cache holds one
+ * allocator reference on every block it lists; a match takes one more for
+ * the caller (who frees it with kv_allocator_free like any block of its
+ * table).  Not thread-safe.
+ * ==================================================================== */
+typedef struct kv_prefix_cache *kv_prefix_cache_t;
+
+/* A cache listing at most capacity_blocks blocks of allocator a. */
+kv_status kv_prefix_cache_create(kv_allocator_t a, int block_size, int capacity_blocks,
+                                 kv_prefix_cache_t *out);
+/* Drops the cache's references and frees the cache. */
+kv_status kv_prefix_cache_destroy(kv_prefix_cache_t c);
+
+/* Longest run of leading full blocks of tokens (host int32[n_tokens]) that
+ * is cached: their ids go to blocks_out (host, up to max_blocks), each with
+ * one more reference for the caller; *n_matched blocks. */
+kv_status kv_prefix_cache_match(kv_prefix_cache_t c, const int32_t *tokens, int64_t n_tokens,
+                                int32_t *blocks_out, int max_blocks, int *n_matched);
+
+/* Lists the full blocks of a sequence (tokens host int32[n_tokens], blocks =
+ * its table row, host int32[n_blocks]) for later matches, taking one
+ * reference on each newly listed block.  Blocks already listed for the same
+ * key keep the older copy.  At capacity, least recently used blocks that only
+ * the cache holds are evicted first; if none can be, insertion stops.
+ * *n_inserted (may be NULL) counts the new entries. */
+kv_status kv_prefix_cache_insert(kv_prefix_cache_t c, const int32_t *tokens, int64_t n_tokens,
+                                 const int32_t *blocks, int n_blocks, int *n_inserted);
+
+/* Frees up to n_blocks listed blocks that nobody but the cache holds,
+ * least recently used first. */
+kv_status kv_prefix_cache_evict(kv_prefix_cache_t c, int n_blocks, int *n_freed);
+
+kv_status kv_prefix_cache_stats(kv_prefix_cache_t c, int *cached_blocks, int64_t *lookups,
+                                int64_t *hits);
+
+/* ======================================================================
  * Device pool.
  * ==================================================================== */
 typedef struct kv_pool *kv_pool_t;

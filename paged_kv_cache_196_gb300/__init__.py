@@ -18,7 +18,9 @@ __all__ = [
     "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_last_cuda_error", "kv_blocks_for_tokens",
     "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
-    "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch", "kv_pool_create", "kv_pool_destroy",
+    "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch",
+    "kv_prefix_cache_create", "kv_prefix_cache_destroy", "kv_prefix_cache_match",
+    "kv_prefix_cache_insert", "kv_prefix_cache_evict", "kv_prefix_cache_stats", "kv_pool_create", "kv_pool_destroy",
     "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks", "kv_swap_out",
     "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
@@ -63,6 +65,12 @@ _SIGS = {
     "kv_allocator_num_free": [_vp, _P(_i32)],
     "kv_prepare_append": [_vp, _i32, _vp, _i32, _P(_i32), _i64, _i32, _vp, _vp, _vp, _P(_i32)],
     "kv_prepare_append_batch": [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _P(_i32)],
+    "kv_prefix_cache_create": [_vp, _i32, _i32, _P(_vp)],
+    "kv_prefix_cache_destroy": [_vp],
+    "kv_prefix_cache_match": [_vp, _vp, _i64, _vp, _i32, _P(_i32)],
+    "kv_prefix_cache_insert": [_vp, _vp, _i64, _vp, _i32, _P(_i32)],
+    "kv_prefix_cache_evict": [_vp, _i32, _P(_i32)],
+    "kv_prefix_cache_stats": [_vp, _P(_i32), _P(_i64), _P(_i64)],
     "kv_pool_create": [_i32, _i32, _i32, _i32, _i32, _P(_vp)],
     "kv_pool_destroy": [_vp],
     "kv_pool_ptrs": [_vp, _P(_vp), _P(_vp)],
@@ -227,6 +235,46 @@ def kv_prepare_append_batch(a: int, tables, num_blocks, cur_lens, n_new, slots_o
                                          _ptr(cow_dst), ctypes.byref(ncow)),
            "kv_prepare_append_batch")
     return ncow.value
+
+
+# ---------------------------------------------------------------- prefix cache
+def kv_prefix_cache_create(a: int, capacity_blocks: int, block_size: int = 16) -> int:
+    h = _vp()
+    _check(lib().kv_prefix_cache_create(a, block_size, capacity_blocks, ctypes.byref(h)),
+           "kv_prefix_cache_create")
+    return h.value
+
+
+def kv_prefix_cache_destroy(c: int):
+    _check(lib().kv_prefix_cache_destroy(c), "kv_prefix_cache_destroy")
+
+
+def kv_prefix_cache_match(c: int, tokens, blocks_out) -> int:
+    """tokens int32 numpy; blocks_out int32 numpy (capacity = its length)."""
+    n = _i32()
+    _check(lib().kv_prefix_cache_match(c, _ptr(tokens), len(tokens), _ptr(blocks_out),
+                                       len(blocks_out), ctypes.byref(n)), "kv_prefix_cache_match")
+    return n.value
+
+
+def kv_prefix_cache_insert(c: int, tokens, blocks) -> int:
+    n = _i32()
+    _check(lib().kv_prefix_cache_insert(c, _ptr(tokens), len(tokens), _ptr(blocks), len(blocks),
+                                        ctypes.byref(n)), "kv_prefix_cache_insert")
+    return n.value
+
+
+def kv_prefix_cache_evict(c: int, n_blocks: int) -> int:
+    n = _i32()
+    _check(lib().kv_prefix_cache_evict(c, n_blocks, ctypes.byref(n)), "kv_prefix_cache_evict")
+    return n.value
+
+
+def kv_prefix_cache_stats(c: int):
+    cb, lk, ht = _i32(), _i64(), _i64()
+    _check(lib().kv_prefix_cache_stats(c, ctypes.byref(cb), ctypes.byref(lk), ctypes.byref(ht)),
+           "kv_prefix_cache_stats")
+    return cb.value, lk.value, ht.value
 
 
 # ---------------------------------------------------------------- pool
