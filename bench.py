@@ -49,6 +49,9 @@ DESCR = {
                                "(cuMemMap-backed) KV path, same inputs as yi6b_long_decode",
     "yi34b_prefill": "Yi-34B-shaped chunked causal paged prefill: 4 seqs x (8192 cached + 2048 "
                      "new) tokens in shuffled 16-token blocks, 56q/8kv heads, head_dim 128, bf16",
+    "vmm_pages": "vAttention page mapping: 8 requests reserved for 196608 tokens (4 kv heads, d128, "
+                 "bf16) mapped to their lengths page by page, with and without the background page "
+                 "pool",
     "swap_blocks": "swap 2048 shuffled 64 KiB blocks (Llama-3-8B-shaped pool, 8 kv heads, d128, "
                    "bf16) out to pinned host memory and back in",
     "shared_prefix_step": "append + decode step with shared prefix: 256 seqs, ctx U[128,2048], groups "
@@ -821,6 +824,52 @@ def run_swap(args, rank, world, local_rank):
     }
 
 
+def run_vmm(args, rank, world, local_rank):
+    """Host latency of the contiguous path's page mapping: kv_contig_ensure
+    (cuMemCreate + cuMemMap + cuMemSetAccess per 2 MiB page) against the same
+    with pages pre-created by the background pool, and kv_contig_release
+    (unmap + release) against unmap + recycle."""
+    import torch
+
+    import paged_kv_cache_196_gb300 as pk
+
+    torch.cuda.set_device(local_rank)
+    cfg = W.CONFIGS["yi6b_long_decode"]
+    lens = W.decode_lengths("yi6b_long_decode")
+    res = {}
+    for mode in ("cold", "pool"):
+        ctx = pk.kv_contig_create(len(lens), cfg["len_hi"], cfg["num_kv_heads"], cfg["head_dim"],
+                                  pk.KV_BF16)
+        if mode == "pool":
+            pk.kv_contig_page_pool(ctx, 512, 1024)
+            t0 = time.time()
+            while pk.kv_contig_page_stats(ctx)["spare"] < 512 and time.time() - t0 < 30:
+                time.sleep(0.01)
+        t0 = time.perf_counter()
+        for b, L in enumerate(lens):
+            pk.kv_contig_reserve(ctx, b)
+            pk.kv_contig_ensure(ctx, b, int(L))
+        t_map = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        for b in range(len(lens)):
+            pk.kv_contig_release(ctx, b)
+        t_rel = time.perf_counter() - t0
+        st = pk.kv_contig_page_stats(ctx)
+        res[mode] = {"map_us_per_page": round(st["map_us"], 2), "unmap_us_per_page": round(st["unmap_us"], 2),
+                     "ensure_total_ms": round(t_map * 1e3, 2), "release_total_ms": round(t_rel * 1e3, 2),
+                     "pages_created": st["created"], "pages_reused": st["reused"]}
+        pk.kv_contig_destroy(ctx)
+    pages = res["cold"]["pages_created"]
+    return {
+        "metric": "contiguous-path page mapping latency (host, per 2 MiB page)",
+        "value": res["pool"]["map_us_per_page"], "unit": "us/page", "n_gpus": world, "steps": 1,
+        "warmup": 0, "ms_per_step": res["pool"]["ensure_total_ms"], "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR["vmm_pages"], "name": "vmm_pages", "pages": pages},
+        "cold": res["cold"], "pool": res["pool"], "gpu_launches": 0, "clocks": None,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -842,7 +891,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return  # the reference arm runs on rank 0 only
-        if args.workload in ("yi34b_prefill", "shared_prefix_step", "swap_blocks"):
+        if args.workload in ("yi34b_prefill", "shared_prefix_step", "swap_blocks", "vmm_pages"):
             print(json.dumps({"impl": "reference", "unavailable":
                               "the reference arm times the decode workloads only"}), flush=True)
             return
@@ -861,6 +910,8 @@ def main():
         line = run_shared_prefix(args, rank, world, local_rank)
     elif args.workload == "swap_blocks":
         line = run_swap(args, rank, world, local_rank)
+    elif args.workload == "vmm_pages":
+        line = run_vmm(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
     if rank == 0:

@@ -384,6 +384,22 @@ kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens);
  * virtual range.  The caller must have finished all work that uses it. */
 kv_status kv_contig_release(kv_contig_t c, int req);
 
+/* Keeps physical pages ready off the request path ("Makale Bulteni --
+ * vAttention", "Iddia ve Gerceklik": background pre-allocation and deferred
+ * reclamation hide the VMM-call latency).  With low > 0 a background thread
+ * creates pages (cuMemCreate) whenever fewer than `low` are spare, up to
+ * `high`; kv_contig_ensure then only maps.  kv_contig_release hands its
+ * pages back to the spare set (up to `high`) instead of releasing them.
+ * (0, 0) stops the thread and releases every spare page.  Spare pages count
+ * as used device memory. */
+kv_status kv_contig_page_pool(kv_contig_t c, int low, int high);
+
+/* Spare pages now, pages created and spare pages reused so far, and the mean
+ * host time per page of mapping (kv_contig_ensure) and unmapping
+ * (kv_contig_release). */
+kv_status kv_contig_page_stats(kv_contig_t c, int *spare_pages, int64_t *created, int64_t *reused,
+                               double *map_us_per_page, double *unmap_us_per_page);
+
 /* Device base addresses of request req's K and V regions. */
 kv_status kv_contig_ptrs(kv_contig_t c, int req, void **k_base, void **v_base);
 

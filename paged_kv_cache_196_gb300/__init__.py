@@ -26,7 +26,7 @@ __all__ = [
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
-    "kv_contig_ptrs", "kv_contig_stats", "kv_contig_append", "contig_decode_attention",
+    "kv_contig_ptrs", "kv_contig_stats", "kv_contig_page_pool", "kv_contig_page_stats", "kv_contig_append", "contig_decode_attention",
     "kv_contig_get_device_error",
 ]
 
@@ -97,6 +97,9 @@ _SIGS = {
     "kv_contig_ensure": [_vp, _i32, _i64],
     "kv_contig_release": [_vp, _i32],
     "kv_contig_ptrs": [_vp, _i32, _P(_vp), _P(_vp)],
+    "kv_contig_page_pool": [_vp, _i32, _i32],
+    "kv_contig_page_stats": [_vp, _P(_i32), _P(_i64), _P(_i64), _P(ctypes.c_double),
+                             _P(ctypes.c_double)],
     "kv_contig_stats": [_vp, _i32, _P(_i64), _P(_i64)],
     "kv_contig_append": [_vp, _vp, _vp, _vp, _vp, _i32, _vp],
     "contig_decode_attention": [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32, _vp,
@@ -428,6 +431,18 @@ def kv_contig_ptrs(c: int, req: int):
     k, v = _vp(), _vp()
     _check(lib().kv_contig_ptrs(c, req, ctypes.byref(k), ctypes.byref(v)), "kv_contig_ptrs")
     return k.value, v.value
+
+
+def kv_contig_page_pool(c: int, low: int, high: int):
+    _check(lib().kv_contig_page_pool(c, low, high), "kv_contig_page_pool")
+
+
+def kv_contig_page_stats(c: int):
+    sp, cr, ru = _i32(), _i64(), _i64()
+    mu, uu = ctypes.c_double(), ctypes.c_double()
+    _check(lib().kv_contig_page_stats(c, ctypes.byref(sp), ctypes.byref(cr), ctypes.byref(ru),
+                                      ctypes.byref(mu), ctypes.byref(uu)), "kv_contig_page_stats")
+    return dict(spare=sp.value, created=cr.value, reused=ru.value, map_us=mu.value, unmap_us=uu.value)
 
 
 def kv_contig_stats(c: int, req: int):

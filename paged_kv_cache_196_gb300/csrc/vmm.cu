@@ -18,9 +18,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <chrono>
+#include <condition_variable>
 #include <cstdint>
+#include <deque>
 #include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "common.cuh"
@@ -120,7 +124,93 @@ struct kv_contig {
     // tiled-TMA maps of each request's K and V region (bf16, head_dim 128 only)
     CUtensorMap *d_maps = nullptr;  // [max_requests][2]
     bool maps = false;
+    // Physical pages kept ready off the request path ("Makale Bulteni --
+    // vAttention", "Iddia ve Gerceklik": background pre-allocation threads and
+    // deferred reclamation hide the latency of the VMM calls).  A worker
+    // thread creates pages while fewer than `low` are spare; released
+    // requests hand their pages back instead of releasing them, up to `high`.
+    struct PagePool {
+        std::mutex mu;
+        std::condition_variable cv;
+        std::deque<CUmemGenericAllocationHandle> spare;
+        std::thread worker;
+        bool running = false, stop = false;
+        int low = 0, high = 0;
+        long long created = 0, reused = 0;
+        double map_ns = 0, unmap_ns = 0;
+        long long maps = 0, unmaps = 0;
+    } pp;
 };
+
+static CUmemAllocationProp page_prop(int device) {
+    CUmemAllocationProp prop{};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = device;
+    return prop;
+}
+
+// A physical page for a mapping: a spare one if the pool has it, else a new one.
+static bool take_page(kv_contig *c, CUmemGenericAllocationHandle *h) {
+    {
+        std::lock_guard<std::mutex> lk(c->pp.mu);
+        if (!c->pp.spare.empty()) {
+            *h = c->pp.spare.front();
+            c->pp.spare.pop_front();
+            c->pp.reused += 1;
+            if (c->pp.running && (int)c->pp.spare.size() < c->pp.low) c->pp.cv.notify_one();
+            return true;
+        }
+        c->pp.created += 1;
+    }
+    const CUmemAllocationProp prop = page_prop(c->device);
+    return driver().create(h, c->page, &prop, 0) == CUDA_SUCCESS;
+}
+
+// An unmapped page: kept for reuse while the pool wants it, else released.
+static void give_page(kv_contig *c, CUmemGenericAllocationHandle h) {
+    {
+        std::lock_guard<std::mutex> lk(c->pp.mu);
+        if ((int)c->pp.spare.size() < c->pp.high) {
+            c->pp.spare.push_back(h);
+            return;
+        }
+    }
+    driver().release(h);
+}
+
+static void page_worker(kv_contig *c) {
+    cudaSetDevice(c->device);
+    const CUmemAllocationProp prop = page_prop(c->device);
+    std::unique_lock<std::mutex> lk(c->pp.mu);
+    while (true) {
+        c->pp.cv.wait(lk, [&] { return c->pp.stop || (int)c->pp.spare.size() < c->pp.low; });
+        if (c->pp.stop) break;
+        const int want = c->pp.high - (int)c->pp.spare.size();
+        lk.unlock();
+        std::vector<CUmemGenericAllocationHandle> made;
+        for (int i = 0; i < want; ++i) {
+            CUmemGenericAllocationHandle h = 0;
+            if (driver().create(&h, c->page, &prop, 0) != CUDA_SUCCESS) break;
+            made.push_back(h);
+        }
+        lk.lock();
+        for (auto h : made) c->pp.spare.push_back(h);
+        c->pp.created += (long long)made.size();
+        if (made.empty()) c->pp.cv.wait_for(lk, std::chrono::milliseconds(50));  // out of memory: back off
+    }
+}
+
+static void stop_page_worker(kv_contig *c) {
+    {
+        std::lock_guard<std::mutex> lk(c->pp.mu);
+        c->pp.stop = true;
+    }
+    c->pp.cv.notify_all();
+    if (c->pp.worker.joinable()) c->pp.worker.join();
+    c->pp.running = false;
+    c->pp.stop = false;
+}
 
 static kv_status sync_request(kv_contig *c, int req) {
     const kv_contig::Req &r = c->reqs[req];
@@ -263,12 +353,13 @@ kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
                 const size_t slot = ((size_t)kv * c->hkv + h) * c->pages_per_head + k;
                 const CUdeviceptr va = r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page;
                 CUmemGenericAllocationHandle hdl = 0;
-                if (d.create(&hdl, c->page, &prop, 0) != CUDA_SUCCESS) {
+                const auto t0 = std::chrono::steady_clock::now();
+                if (!take_page(c, &hdl)) {
                     st = KV_ERR_OOM;
                     break;
                 }
                 if (d.map(va, c->page, 0, hdl, 0) != CUDA_SUCCESS) {
-                    d.release(hdl);
+                    give_page(c, hdl);
                     st = KV_ERR_CUDA;
                     break;
                 }
@@ -278,6 +369,8 @@ kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
                     st = KV_ERR_CUDA;
                     break;
                 }
+                c->pp.map_ns += std::chrono::duration<double, std::nano>(std::chrono::steady_clock::now() - t0).count();
+                c->pp.maps += 1;
             }
     if (st != KV_OK) {
         for (size_t slot : made) {
@@ -285,7 +378,7 @@ kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
             const size_t rem = slot % ((size_t)c->hkv * c->pages_per_head);
             const size_t h = rem / c->pages_per_head, k = rem % c->pages_per_head;
             d.unmap(r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page, c->page);
-            d.release(r.pages[slot]);
+            give_page(c, r.pages[slot]);
             r.pages[slot] = 0;
         }
         return st;
@@ -306,10 +399,14 @@ kv_status kv_contig_release(kv_contig_t c, int req) {
         const size_t kv = slot / ((size_t)c->hkv * c->pages_per_head);
         const size_t rem = slot % ((size_t)c->hkv * c->pages_per_head);
         const size_t h = rem / c->pages_per_head, k = rem % c->pages_per_head;
+        const auto t0 = std::chrono::steady_clock::now();
         if (d.unmap(r.base + kv * c->region_bytes + h * c->head_bytes + k * c->page, c->page) !=
-                CUDA_SUCCESS ||
-            d.release(r.pages[slot]) != CUDA_SUCCESS)
+            CUDA_SUCCESS)
             st = KV_ERR_CUDA;
+        else
+            give_page(c, r.pages[slot]);  // deferred reclamation: kept for reuse while wanted
+        c->pp.unmap_ns += std::chrono::duration<double, std::nano>(std::chrono::steady_clock::now() - t0).count();
+        c->pp.unmaps += 1;
         r.pages[slot] = 0;
         c->mapped_bytes -= (long long)c->page;
     }
@@ -323,8 +420,12 @@ kv_status kv_contig_release(kv_contig_t c, int req) {
 
 kv_status kv_contig_destroy(kv_contig_t c) {
     if (!c) return KV_ERR_ARG;
+    stop_page_worker(c);
+    c->pp.high = 0;  // released pages are not kept any more
     for (int r = 0; r < c->max_requests; ++r)
         if (c->reqs[r].base && c->d_kbase) kv_contig_release(c, r);
+    for (auto h : c->pp.spare) driver().release(h);
+    c->pp.spare.clear();
     if (c->d_kbase) cudaFree(c->d_kbase);
     if (c->d_vbase) cudaFree(c->d_vbase);
     if (c->d_mapped) cudaFree(c->d_mapped);
@@ -332,6 +433,43 @@ kv_status kv_contig_destroy(kv_contig_t c) {
     if (c->counters) cudaFree(c->counters);
     if (c->d_maps) cudaFree(c->d_maps);
     delete c;
+    return KV_OK;
+}
+
+kv_status kv_contig_page_pool(kv_contig_t c, int low, int high) {
+    if (!c || low < 0 || high < low) return KV_ERR_ARG;
+    stop_page_worker(c);
+    std::vector<CUmemGenericAllocationHandle> drop;
+    {
+        std::lock_guard<std::mutex> lk(c->pp.mu);
+        c->pp.low = low;
+        c->pp.high = high;
+        while ((int)c->pp.spare.size() > high) {
+            drop.push_back(c->pp.spare.back());
+            c->pp.spare.pop_back();
+        }
+    }
+    for (auto h : drop) driver().release(h);
+    if (low > 0) {
+        try {
+            c->pp.worker = std::thread(page_worker, c);
+        } catch (...) {
+            return KV_ERR_OOM;
+        }
+        c->pp.running = true;
+    }
+    return KV_OK;
+}
+
+kv_status kv_contig_page_stats(kv_contig_t c, int *spare_pages, int64_t *created, int64_t *reused,
+                               double *map_us_per_page, double *unmap_us_per_page) {
+    if (!c) return KV_ERR_ARG;
+    std::lock_guard<std::mutex> lk(c->pp.mu);
+    if (spare_pages) *spare_pages = (int)c->pp.spare.size();
+    if (created) *created = c->pp.created;
+    if (reused) *reused = c->pp.reused;
+    if (map_us_per_page) *map_us_per_page = c->pp.maps ? c->pp.map_ns / c->pp.maps / 1e3 : 0.0;
+    if (unmap_us_per_page) *unmap_us_per_page = c->pp.unmaps ? c->pp.unmap_ns / c->pp.unmaps / 1e3 : 0.0;
     return KV_OK;
 }
 

@@ -157,3 +157,42 @@ def test_pages_are_mapped_on_demand_and_released():
     assert pk.kv_contig_stats(ctx, 1) == (0, 0)
     pk.kv_contig_reserve(ctx, 1)                             # reusable after release
     pk.kv_contig_destroy(ctx)
+
+
+def test_page_pool_prefetches_and_recycles_pages():
+    import time
+    require_cuda()
+    ctx = pk.kv_contig_create(4, 100000, 4, 128, pk.KV_BF16)
+    _, page, _ = pk.kv_contig_layout(ctx)
+    pages_per_req = 2 * 4 * -(-30000 * 128 * 2 // page)   # K and V regions of 4 heads
+    pk.kv_contig_page_pool(ctx, pages_per_req, 2 * pages_per_req)
+    t0 = time.time()
+    while pk.kv_contig_page_stats(ctx)["spare"] < pages_per_req and time.time() - t0 < 10:
+        time.sleep(0.01)
+    st0 = pk.kv_contig_page_stats(ctx)
+    assert st0["spare"] >= pages_per_req                  # created ahead, off the request path
+    pk.kv_contig_reserve(ctx, 0)
+    pk.kv_contig_ensure(ctx, 0, 30000)
+    st1 = pk.kv_contig_page_stats(ctx)
+    assert st1["reused"] - st0["reused"] == pages_per_req    # every mapped page came from the pool
+    # the request works as usual: write and read back through the mapping
+    k = W.normal(W.rng(5), (3, 4, 128), "bf16")
+    pk.kv_contig_append(ctx, dev(k), dev(k), dev(np.zeros(3, np.int32)),
+                        dev(np.array([0, 1, 29999], np.int32)), 3)
+    torch.cuda.synchronize()
+    assert pk.kv_contig_get_device_error(ctx) == 0
+    k_ptr, _ = pk.kv_contig_ptrs(ctx, 0)
+    hs, _, _ = pk.kv_contig_layout(ctx)
+    got = read_linear(k_ptr, 4, hs, 30000, 128, True)
+    np.testing.assert_array_equal(got[:, [0, 1, 29999]], k.transpose(1, 0, 2))
+    # deferred reclamation: released pages stay spare and serve the next request
+    pk.kv_contig_release(ctx, 0)
+    created = pk.kv_contig_page_stats(ctx)["created"]
+    pk.kv_contig_reserve(ctx, 1)
+    pk.kv_contig_ensure(ctx, 1, 30000)
+    st2 = pk.kv_contig_page_stats(ctx)
+    assert st2["created"] == created or st2["created"] - created <= pages_per_req
+    assert st2["reused"] - st1["reused"] == pages_per_req
+    pk.kv_contig_page_pool(ctx, 0, 0)                      # stop the thread, drop spare pages
+    assert pk.kv_contig_page_stats(ctx)["spare"] == 0
+    pk.kv_contig_destroy(ctx)
