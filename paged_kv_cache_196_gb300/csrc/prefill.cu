@@ -49,7 +49,8 @@ namespace pkv {
 constexpr int kPfBM = 256;           // queries per CTA (two tensor-core tiles)
 constexpr int kPfBN = 128;           // keys per tile
 constexpr int kPfD = 128;            // head dim (only size supported)
-constexpr int kPfThreads = 320;
+constexpr int kPfThreads = 320;  // 8 softmax warps + producer + MMA issuer
+constexpr int kPfProducerWarp = 8, kPfMmaWarp = 9;
 constexpr int kPfHalfBytes = 128 * 128;         // 128 rows x 64 bf16 (one half of D)
 constexpr int kPfTileBytes = 2 * kPfHalfBytes;  // 128 rows x 128 bf16
 constexpr int kPfQOff = 0;                             // Q_A, Q_B
@@ -65,6 +66,13 @@ KV_DEVICE float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// max(a, b, c) in one instruction
+KV_DEVICE float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // TMEM column map: S of tile x at colS(x), O of tile x at colO(x)
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     char *sV = smem + kPfVOff;
     PfBars *bars = reinterpret_cast<PfBars *>(smem + kPfBarOff);
 
-    if (warp == 9) {
+    if (warp == kPfMmaWarp) {
         tc::tmem_alloc(&bars->tmem_slot, 512);
         tc::tmem_relinquish();
     }
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&bars->kempty[s], 1);
             mbar_init(&bars->vempty[s], 1);
             mbar_init(&bars->sfull[s], 1);
-            mbar_init(&bars->pfull[s], 128);
+            mbar_init(&bars->pfull[s], 4);
         }
         mbar_init(&bars->done, 1);
         bars->abort = 0;
@@ -148,8 +156,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort_flag = &bars->abort;
 
-    if (warp == 8) {
+    if (warp == kPfProducerWarp) {
         // ================================================== TMA producer
+        // The whole warp runs the loop: lanes 0-7 hold the block-table
+        // entries (as tensor rows) of the next two key tiles, loaded two tiles
+        // ahead so their latency never stalls a copy; lane 0 waits on the
+        // ring barriers and issues the copies.  K runs one tile ahead of V:
+        // S_X(j+1) needs K(j+1) as soon as PV_X(j) is issued.
         if (lane == 0) {
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
@@ -161,49 +174,62 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc::tma_load_3d(sQ + x * kPfTileBytes + kPfHalfBytes, &tm_q, 64, hq,
                                 q_begin + q0 + 128 * x, &bars->qfull);
             }
-            const int32_t *row = p.tables + (size_t)b * p.max_blocks;
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n && !*abort_flag; ++j) {
-                const int s = j & 1;
-                int ys[8];
-#pragma unroll
-                for (int bi = 0; bi < 8; ++bi) {
-                    const int ib = j * 8 + bi;
-                    int y = -16;  // rows -16..-1: outside the tensor, read as zeros
-                    if (ib < nblk) {
-                        const int id = __ldg(row + ib);
-                        if (id >= 0 && id < p.num_blocks)
-                            y = (id * p.num_kv_heads + h) * 16;
-                        else
-                            atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                    }
-                    ys[bi] = y;
-                }
-                if (j >= 2 && !mbar_wait(&bars->kempty[s], ((j - 2) >> 1) & 1, p.err)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                char *dk = sK + s * kPfTileBytes;
-                mbar_arrive_expect_tx(&bars->kfull[s], kPfTileBytes);
-#pragma unroll
-                for (int bi = 0; bi < 8; ++bi) {
-                    tc::tma_load_2d(dk + bi * 2048, &tm_k, 0, ys[bi], &bars->kfull[s]);
-                    tc::tma_load_2d(dk + kPfHalfBytes + bi * 2048, &tm_k, 64, ys[bi], &bars->kfull[s]);
-                }
-                k_issued = j + 1;
-                if (j >= 2 && !mbar_wait(&bars->vempty[s], ((j - 2) >> 1) & 1, p.err)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                char *dv = sV + s * kPfTileBytes;
-                mbar_arrive_expect_tx(&bars->vfull[s], kPfTileBytes);
-#pragma unroll
-                for (int bi = 0; bi < 8; ++bi) {
-                    tc::tma_load_2d(dv + bi * 2048, &tm_v, 0, ys[bi], &bars->vfull[s]);
-                    tc::tma_load_2d(dv + kPfHalfBytes + bi * 2048, &tm_v, 64, ys[bi], &bars->vfull[s]);
-                }
-                v_issued = j + 1;
+        }
+        const int32_t *row = p.tables + (size_t)b * p.max_blocks;
+        // Tensor row of block (8*jj + lane) of this sequence and head; rows
+        // -16..-1 lie outside the tensor and read as zeros.
+        auto fetch = [&](int jj) {
+            int y = -16;
+            const int ib = jj * 8 + lane;
+            if (lane < 8 && jj < n && ib < nblk) {
+                const int id = __ldg(row + ib);
+                if (id >= 0 && id < p.num_blocks)
+                    y = (id * p.num_kv_heads + h) * 16;
+                else
+                    atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
             }
+            return y;
+        };
+        auto issue = [&](const CUtensorMap *map, char *dst, uint64_t *bar, int y_lane) {
+            int ys[8];
+#pragma unroll
+            for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_lane, bi);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, kPfTileBytes);
+#pragma unroll
+                for (int bi = 0; bi < 8; ++bi) {
+                    tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], bar);
+                    tc::tma_load_2d(dst + kPfHalfBytes + bi * 2048, map, 64, ys[bi], bar);
+                }
+            }
+        };
+        int k_issued, v_issued = 0;
+        int y_v = fetch(0), y_k = fetch(1);  // entries of tiles t and t+1
+        issue(&tm_k, sK, &bars->kfull[0], y_v);
+        k_issued = 1;
+        for (int t = 0; t < n; ++t) {
+            const int y_next = fetch(t + 2);  // in flight during this iteration
+            bool stop = false;
+            if (t + 1 < n) {
+                const int s = (t + 1) & 1;
+                if (lane == 0)
+                    stop = *abort_flag ||
+                           (t + 1 >= 2 && !mbar_wait(&bars->kempty[s], ((t - 1) >> 1) & 1, p.err));
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                issue(&tm_k, sK + s * kPfTileBytes, &bars->kfull[s], y_k);
+                k_issued = t + 2;
+            }
+            const int s = t & 1;
+            if (lane == 0)
+                stop = *abort_flag || (t >= 2 && !mbar_wait(&bars->vempty[s], ((t - 2) >> 1) & 1, p.err));
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            issue(&tm_v, sV + s * kPfTileBytes, &bars->vfull[s], y_v);
+            v_issued = t + 1;
+            y_v = y_k;
+            y_k = y_next;
+        }
+        if (lane == 0) {
+            if (v_issued < n) *abort_flag = 1;
             // Never leave copies in flight into this CTA's shared memory.
             mbar_wait(&bars->qfull, 0, p.err);
             for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
@@ -211,7 +237,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
                 mbar_wait(&bars->vfull[j & 1], (j >> 1) & 1, p.err);
         }
-    } else if (warp == 9) {
+    } else if (warp == kPfMmaWarp) {
         // ================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
@@ -285,42 +311,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            if (*abort_flag) { ok = false; break; }
-            if (!mbar_wait(&bars->sfull[x], j & 1, p.err)) { ok = false; break; }
+            // Exits are warp-uniform: the warp arrives on pfull as one.
+            bool bad = *abort_flag != 0;
+            if (!bad) bad = !mbar_wait(&bars->sfull[x], j & 1, p.err);
+            if (__any_sync(0xffffffffu, bad)) { ok = false; break; }
             tc::fence_after_sync();
             const long long key0 = (long long)j * kPfBN;
+            // The row's 128 scores are read from tensor memory once and kept
+            // in registers for both the maximum and the exponentials.
+            uint32_t sv[4][32];
+            const uint32_t scol = tmem + lane_base + colS(x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tc::tmem_ld32(scol + 32 * i, sv[i]);
+            tc::tmem_wait_ld();
             // Keys past this row's position are masked: column k is kept iff
             // k <= lim.  Only tiles on the diagonal need it; the branch is
             // warp-uniform so interior tiles pay nothing.
             const int lim = (int)max(-1LL, min(127LL, qpos - key0));
-            const bool diag = __any_sync(0xffffffffu, lim < 127);
-            const uint32_t scol = tmem + lane_base + colS(x);
-            // pass 1: raw row maximum (scale > 0, so max(scale*s) = scale*max(s)),
-            // 64 columns per round, eight independent chains
-            float mx[8];
+            if (__any_sync(0xffffffffu, lim < 127)) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t a[32], b2[32];
-                tc::tmem_ld32(scol + 64 * half, a);
-                tc::tmem_ld32(scol + 64 * half + 32, b2);
-                tc::tmem_wait_ld();
-                if (diag) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float va = 64 * half + k <= lim ? __uint_as_float(a[k]) : -INFINITY;
-                        const float vb = 64 * half + 32 + k <= lim ? __uint_as_float(b2[k]) : -INFINITY;
-                        mx[k & 7] = fmaxf(mx[k & 7], fmaxf(va, vb));
-                    }
-                } else {
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
-                        mx[k & 7] = fmaxf(mx[k & 7], fmaxf(__uint_as_float(a[k]), __uint_as_float(b2[k])));
-                }
+                        if (32 * i + k > lim) sv[i][k] = __float_as_uint(-INFINITY);
             }
-            const float mrow = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+            // raw row maximum (scale > 0, so max(scale*s) = scale*max(s)),
+            // eight independent chains of three-input maxima
+            float mx[8];
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint32_t *v = &sv[c8 >> 1][16 * (c8 & 1)];
+                float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                for (int k = 3; k < 15; k += 2)
+                    m = fmax3(m, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+                mx[c8] = fmaxf(m, __uint_as_float(v[15]));
+            }
+            const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                                     fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) *
                                p.scale_log2;
             float alpha = 1.f;
             bool rescale = false;
@@ -332,59 +360,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 l_sum *= alpha;
                 rescale = true;
             }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O_x holds PV_x(j-1): its completion precedes S_x(j)'s.
-                uint32_t v[32];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    tc::tmem_ld32(tmem + lane_base + colO(x) + 32 * i, v);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-                    tc::tmem_st32(tmem + lane_base + colO(x) + 32 * i, v);
-                }
-            }
-            // pass 2: p = 2^(scale*s - m) with a packed fma and the hardware
-            // exp2, bf16 pairs written over the first 64 columns of this S
-            // (columns 64h..64h+63 of S are read before P half h is stored)
+            // p = 2^(scale*s - m) with a packed fma and the hardware exp2; bf16
+            // pairs written over the first 64 columns of this S, 32 keys at a time
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_used, -m_used);
             float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                               make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t a[32], b2[32], w[32];
-                tc::tmem_ld32(scol + 64 * half, a);
-                tc::tmem_ld32(scol + 64 * half + 32, b2);
-                tc::tmem_wait_ld();
-                if (diag) {
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w[16];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        if (64 * half + k > lim) a[k] = __float_as_uint(-INFINITY);
-                        if (64 * half + 32 + k > lim) b2[k] = __float_as_uint(-INFINITY);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const uint32_t *src = k < 16 ? a : b2;
-                    const int kk = 2 * (k & 15);
-                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(src[kk]), __uint_as_float(src[kk + 1])),
+                for (int k = 0; k < 16; ++k) {
+                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[i][2 * k]),
+                                                             __uint_as_float(sv[i][2 * k + 1])),
                                                  sc2, nm2);
                     const float2 e = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
                     acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
                     w[k] = tc::pack_bf16x2(e.x, e.y);
                 }
-                tc::tmem_st32(scol + 32 * half, w);
+                tc::tmem_st16(scol + 16 * i, w);
             }
             l_sum += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y) + (acc2[2].x + acc2[2].y) +
                      (acc2[3].x + acc2[3].y);
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O_x holds PV_x(j-1): its completion precedes S_x(j)'s.  Done after
+                // the exponentials, when the scores no longer occupy registers.
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t v[16];
+                    const uint32_t oc = tmem + lane_base + colO(x) + 16 * i;
+                    tc::tmem_ld16(oc, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+                    tc::tmem_st16(oc, v);
+                }
+            }
             tc::tmem_wait_st();
             if (x == 0 && key0 + kPfBN > L) {
                 // Keys at or past L: the V rows there may hold anything; zero
                 // them so the zero weights cannot meet a NaN in the tensor core.
                 // Tile A's PV runs first, so A's warps do it for both tiles.
                 const int s = j & 1;
-                if (!mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err)) { ok = false; break; }
+                if (__any_sync(0xffffffffu, !mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err))) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
                 const int first = (int)(L - key0);
                 char *vt = sV + s * kPfTileBytes;
                 for (int idx = r; idx < (kPfBN - first) * 16; idx += 128) {
@@ -395,7 +417,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc::fence_proxy_async_smem();
             }
             tc::fence_before_sync();
-            mbar_arrive(&bars->pfull[x]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->pfull[x]);  // one arrival per warp
         }
         // ---- epilogue: O / l for this row
         if (ok) ok = mbar_wait(&bars->done, 0, p.err);
@@ -435,7 +458,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kPfMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, 512);
     }
