@@ -16,11 +16,12 @@
 //
 // One CTA = two 128-query tiles (A: rows 0-127, B: rows 128-255 of a 256-query
 // slice) of one query head of one sequence; every K/V tile of 128 keys (8
-// blocks) is loaded once and used by both.  320 threads:
+// blocks) is loaded once and used by both.  352 threads:
 //   warps 0-3  softmax of tile A (thread = query row = tensor-memory lane)
 //   warps 4-7  softmax of tile B
-//   warp 8     TMA producer: Q once, K and V into 2-deep rings
+//   warp 8     TMA producer: Q once, K into a 2-deep ring
 //   warp 9     MMA issuer (tcgen05.mma, M=128, N=128, K=16 steps, fp32 in TMEM)
+//   warp 10    TMA producer: V into a 2-deep ring
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
 // O_B [384,512); each tile's bf16 weights P overwrite the first 64 columns of
 // its S once read.  MMA issue order per key tile j:
@@ -49,8 +50,8 @@ namespace pkv {
 constexpr int kPfBM = 256;           // queries per CTA (two tensor-core tiles)
 constexpr int kPfBN = 128;           // keys per tile
 constexpr int kPfD = 128;            // head dim (only size supported)
-constexpr int kPfThreads = 320;  // 8 softmax warps + producer + MMA issuer
-constexpr int kPfProducerWarp = 8, kPfMmaWarp = 9;
+constexpr int kPfThreads = 352;  // 8 softmax warps, MMA issuer, K and V producers
+constexpr int kPfProducerWarp = 8, kPfMmaWarp = 9, kPfVProducerWarp = 10;
 constexpr int kPfHalfBytes = 128 * 128;         // 128 rows x 64 bf16 (one half of D)
 constexpr int kPfTileBytes = 2 * kPfHalfBytes;  // 128 rows x 128 bf16
 constexpr int kPfQOff = 0;                             // Q_A, Q_B
@@ -156,17 +157,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem = bars->tmem_slot;
     volatile int *abort_flag = &bars->abort;
 
-    if (warp == kPfProducerWarp) {
-        // ================================================== TMA producer
-        // The whole warp runs the loop: lanes 0-7 hold the block-table
-        // entries (as tensor rows) of the next two key tiles, loaded two tiles
-        // ahead so their latency never stalls a copy; lane 0 waits on the
-        // ring barriers and issues the copies.  K runs one tile ahead of V:
-        // S_X(j+1) needs K(j+1) as soon as PV_X(j) is issued.
-        if (lane == 0) {
+    if (warp == kPfProducerWarp || warp == kPfVProducerWarp) {
+        // ================================================== TMA producers
+        // One warp fills the K ring (and loads Q), another the V ring, so the
+        // two streams of copies are issued independently.  In each warp lanes
+        // 0-7 hold the block-table entries (as tensor rows) of the next two
+        // key tiles, loaded two tiles ahead so their latency never stalls a
+        // copy; lane 0 waits on the ring barriers and issues the copies.
+        const bool is_v = warp == kPfVProducerWarp;
+        if (!is_v && lane == 0) {
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
-            tc::prefetch_tensormap(&tm_v);
             mbar_arrive_expect_tx(&bars->qfull, 2 * kPfTileBytes);
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
@@ -175,6 +176,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                 q_begin + q0 + 128 * x, &bars->qfull);
             }
         }
+        if (is_v && lane == 0) tc::prefetch_tensormap(&tm_v);
+        const CUtensorMap *map = is_v ? &tm_v : &tm_k;
+        char *ring = is_v ? sV : sK;
+        uint64_t *full = is_v ? bars->vfull : bars->kfull;
+        uint64_t *empty = is_v ? bars->vempty : bars->kempty;
         const int32_t *row = p.tables + (size_t)b * p.max_blocks;
         // Tensor row of block (8*jj + lane) of this sequence and head; rows
         // -16..-1 lie outside the tensor and read as zeros.
@@ -185,57 +191,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int id = __ldg(row + ib);
                 if (id >= 0 && id < p.num_blocks)
                     y = (id * p.num_kv_heads + h) * 16;
-                else
+                else if (!is_v)
                     atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
             }
             return y;
         };
-        auto issue = [&](const CUtensorMap *map, char *dst, uint64_t *bar, int y_lane) {
+        int issued = 0;
+        int y_cur = fetch(0), y_nxt = fetch(1);  // entries of tiles t and t+1
+        for (int t = 0; t < n; ++t) {
+            const int y_later = fetch(t + 2);  // in flight during this iteration
+            const int s = t & 1;
+            bool stop = false;
+            if (lane == 0)
+                stop = *abort_flag || (t >= 2 && !mbar_wait(&empty[s], ((t - 2) >> 1) & 1, p.err));
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
             int ys[8];
 #pragma unroll
-            for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_lane, bi);
+            for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar, kPfTileBytes);
+                char *dst = ring + s * kPfTileBytes;
+                mbar_arrive_expect_tx(&full[s], kPfTileBytes);
 #pragma unroll
                 for (int bi = 0; bi < 8; ++bi) {
-                    tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], bar);
-                    tc::tma_load_2d(dst + kPfHalfBytes + bi * 2048, map, 64, ys[bi], bar);
+                    tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
+                    tc::tma_load_2d(dst + kPfHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
                 }
             }
-        };
-        int k_issued, v_issued = 0;
-        int y_v = fetch(0), y_k = fetch(1);  // entries of tiles t and t+1
-        issue(&tm_k, sK, &bars->kfull[0], y_v);
-        k_issued = 1;
-        for (int t = 0; t < n; ++t) {
-            const int y_next = fetch(t + 2);  // in flight during this iteration
-            bool stop = false;
-            if (t + 1 < n) {
-                const int s = (t + 1) & 1;
-                if (lane == 0)
-                    stop = *abort_flag ||
-                           (t + 1 >= 2 && !mbar_wait(&bars->kempty[s], ((t - 1) >> 1) & 1, p.err));
-                if (__shfl_sync(0xffffffffu, stop, 0)) break;
-                issue(&tm_k, sK + s * kPfTileBytes, &bars->kfull[s], y_k);
-                k_issued = t + 2;
-            }
-            const int s = t & 1;
-            if (lane == 0)
-                stop = *abort_flag || (t >= 2 && !mbar_wait(&bars->vempty[s], ((t - 2) >> 1) & 1, p.err));
-            if (__shfl_sync(0xffffffffu, stop, 0)) break;
-            issue(&tm_v, sV + s * kPfTileBytes, &bars->vfull[s], y_v);
-            v_issued = t + 1;
-            y_v = y_k;
-            y_k = y_next;
+            issued = t + 1;
+            y_cur = y_nxt;
+            y_nxt = y_later;
         }
         if (lane == 0) {
-            if (v_issued < n) *abort_flag = 1;
+            if (issued < n) *abort_flag = 1;
             // Never leave copies in flight into this CTA's shared memory.
-            mbar_wait(&bars->qfull, 0, p.err);
-            for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
-                mbar_wait(&bars->kfull[j & 1], (j >> 1) & 1, p.err);
-            for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
-                mbar_wait(&bars->vfull[j & 1], (j >> 1) & 1, p.err);
+            if (!is_v) mbar_wait(&bars->qfull, 0, p.err);
+            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+                mbar_wait(&full[j & 1], (j >> 1) & 1, p.err);
         }
     } else if (warp == kPfMmaWarp) {
         // ================================================== MMA issuer
