@@ -310,6 +310,48 @@ kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32
                                          kv_dtype out_dtype, float *lse_out, int num_splits,
                                          void *stream);
 
+/* Cascade decode over shared prefixes ("PagedAttention Nedir?", "Prefix
+ * Sharing Nasil Calisir?"; "Makale Bulteni -- PagedAttention ve vLLM",
+ * "Ticari Etki": sequences that start alike hold that part of the cache once,
+ * as the same physical blocks).  Same result as paged_decode_attention (exact
+ * maths; rounding differs), but each group's shared blocks are read once for
+ * all its sequences instead of once per sequence.
+ *
+ *   group_seqs     device int32[num_groups][group_size]: the sequences of
+ *                  each group (batch indices), -1 for an empty slot; a
+ *                  sequence belongs to at most one group;
+ *   shared_tokens  device int32[batch]: tokens at the start of sequence b that
+ *                  it reads through its group's shared blocks, rounded down to
+ *                  whole blocks and clamped to seq_lens[b]; 0 for a sequence
+ *                  in no group.  The blocks are read from the table row of the
+ *                  member with the most shared tokens; every member's row must
+ *                  hold the same block ids for its own shared blocks;
+ *   max_prefix_blocks  upper bound of any group's shared blocks (host-known;
+ *                  <= max_blocks).  A group with more sets
+ *                  KV_DEVERR_BLOCK_RANGE and its excess is not attended;
+ *   prefix_splits  0 = automatic (kv_cascade_plan), else the number of
+ *                  key-range partitions of each group's prefix;
+ *   num_splits, workspace: as paged_decode_attention, for the suffix (the
+ *                  blocks after each sequence's shared part); the workspace
+ *                  must hold kv_cascade_workspace_size bytes.
+ * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16,
+ * head_dim 128 and group_size * (num_q_heads / num_kv_heads) <= 128, else
+ * KV_ERR_UNSUPPORTED.  Two kernels run in stream order: the prefix kernel
+ * (tcgen05; rows = a group's sequences x the query heads of one kv head) and
+ * the decode kernel over the suffixes, whose split-KV merge also takes the
+ * prefix's partial results. */
+kv_status kv_cascade_plan(int num_groups, int num_kv_heads, int max_prefix_blocks, int requested,
+                          int *prefix_splits);
+kv_status kv_cascade_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int max_blocks, int num_splits, int prefix_splits,
+                                    size_t *bytes);
+kv_status paged_decode_attention_cascade(
+    kv_pool_t p, const void *q, const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
+    int batch, int num_q_heads, float scale, const int32_t *group_seqs, int num_groups,
+    int group_size, const int32_t *shared_tokens, int max_prefix_blocks, int prefix_splits,
+    void *out, kv_dtype out_dtype, float *lse_out, int num_splits, void *workspace,
+    size_t workspace_bytes, void *stream);
+
 /* Chunked causal paged prefill ("Makale Bulteni -- vAttention", "Iddia ve
  * Gerceklik": the prefill kernels are where paging costs most).  Sequence b
  * holds seq_lens[b] tokens in the cache, the last T_b = cu_q[b+1] - cu_q[b]

@@ -24,7 +24,8 @@ __all__ = [
     "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks", "kv_swap_out",
     "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
-    "paged_decode_attention_noalloc", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
+    "paged_decode_attention_noalloc", "kv_cascade_plan", "kv_cascade_workspace_size",
+    "paged_decode_attention_cascade", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_page_pool", "kv_contig_page_stats", "kv_contig_append", "contig_decode_attention",
     "kv_contig_get_device_error",
@@ -87,6 +88,11 @@ _SIGS = {
                                _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _vp, _i32, _vp],
+    "kv_cascade_plan": [_i32, _i32, _i32, _i32, _P(_i32)],
+    "kv_cascade_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
+    "paged_decode_attention_cascade": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
+                                       _i32, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _sz,
+                                       _vp],
     "paged_prefill_attention": [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
                                 _i32, _vp, _vp],
     "kv_get_device_error": [_vp, _P(_i32), _vp],
@@ -375,6 +381,37 @@ def paged_decode_attention_noalloc(p: int, q, block_tables, max_blocks: int, seq
                                                 _ptr(out), out_dtype, _ptr(lse_out), num_splits,
                                                 _stream(stream)),
            "paged_decode_attention_noalloc")
+
+
+def kv_cascade_plan(num_groups: int, num_kv_heads: int, max_prefix_blocks: int,
+                    requested: int = 0) -> int:
+    r = _i32()
+    _check(lib().kv_cascade_plan(num_groups, num_kv_heads, max_prefix_blocks, requested,
+                                 ctypes.byref(r)), "kv_cascade_plan")
+    return r.value
+
+
+def kv_cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, num_splits,
+                              prefix_splits) -> int:
+    r = _sz()
+    _check(lib().kv_cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                           num_splits, prefix_splits, ctypes.byref(r)),
+           "kv_cascade_workspace_size")
+    return r.value
+
+
+def paged_decode_attention_cascade(p: int, q, block_tables, max_blocks: int, seq_lens, batch: int,
+                                   num_q_heads: int, scale: float, group_seqs, num_groups: int,
+                                   group_size: int, shared_tokens, max_prefix_blocks: int,
+                                   prefix_splits: int, out, out_dtype: int, lse_out=None,
+                                   num_splits: int = 0, workspace=None, workspace_bytes: int = 0,
+                                   stream=None):
+    """Decode with each group's shared prefix blocks read once; see the C header."""
+    _check(lib().paged_decode_attention_cascade(
+        p, _ptr(q), _ptr(block_tables), max_blocks, _ptr(seq_lens), batch, num_q_heads, scale,
+        _ptr(group_seqs), num_groups, group_size, _ptr(shared_tokens), max_prefix_blocks,
+        prefix_splits, _ptr(out), out_dtype, _ptr(lse_out), num_splits, _ptr(workspace),
+        workspace_bytes, _stream(stream)), "paged_decode_attention_cascade")
 
 
 def paged_prefill_attention(p: int, q, cu_q, total_q: int, max_q_len: int, block_tables,

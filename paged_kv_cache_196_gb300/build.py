@@ -21,7 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
 SOURCES = ["allocator.cpp", "prefix_cache.cpp", "pool.cu", "decode.cu", "vmm.cu", "prefill.cu",
-           "tmap.cu"]
+           "cascade.cu", "tmap.cu"]
 
 
 def nvcc() -> str:

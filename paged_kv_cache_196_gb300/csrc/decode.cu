@@ -85,6 +85,8 @@ struct DecodeKParams {
     float scale_log2;  // scale * log2(e): scores are kept in the log2 domain
     int part_blocks;
     int max_splits;
+    const int32_t *start_tokens;  // cascade: tokens of each sequence attended elsewhere, or null
+    int part_base;                // cascade: workspace slots [0, part_base) hold those results
     void *out;
     int out_bf16;
     float *lse;
@@ -160,6 +162,16 @@ constexpr size_t decode_ring_bytes() {
     return ((ring > merge ? ring : merge) + 127) / 128 * 128;
 }
 
+// Blocks of sequence b before this call's part of it: its first
+// start_tokens[b] tokens (clamped to [0, L], whole blocks) were attended by
+// the cascade's prefix kernel.
+KV_DEVICE int start_block(const DecodeKParams &p, int b, long long L) {
+    if (!p.start_tokens) return 0;
+    long long st = p.start_tokens[b];
+    st = st < 0 ? 0 : (st > L ? L : st);
+    return (int)(st / kBS);
+}
+
 // End of a partition: combine the kNW warp states (running max m, sum l,
 // unnormalised output o, all in the log2 domain) into this partition's
 // result.  With one partition the result is final.  Otherwise it is written
@@ -167,8 +179,14 @@ constexpr size_t decode_ring_bytes() {
 // -- found with an arrival counter that it resets afterwards -- merges all
 // partitions: o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).
 template <int G, int D>
+//
+// Cascade: a sequence whose prefix was attended by the prefix kernel (pre > 0)
+// has pre more partial results in workspace slots [0, pre); this call's
+// partitions use slots part_base + split, and the merge takes both.
 KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const float *sm_m,
-                                const float *sm_l, int b, int h, int split, int nsplit, int tid) {
+                                const float *sm_l, int b, int h, int split, int nsplit, int pre,
+                                int tid) {
+    const int ntot = pre + nsplit;
     constexpr float kLn2 = 0.6931471805599453f;
     for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
         const int j = idx / D, d = idx - j * D;
@@ -187,18 +205,18 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
         const float o = den > 0.f ? num / den : 0.f;
         const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
         const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
-        if (nsplit == 1) {
+        if (ntot == 1) {
             if (p.out_bf16)
                 reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(o);
             else
                 reinterpret_cast<float *>(p.out)[row * D + d] = o;
             if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
         } else {
-            p.ws_o[(row * p.max_splits + split) * D + d] = o;
-            if (d == 0) p.ws_lse[row * p.max_splits + split] = lse2;
+            p.ws_o[(row * p.max_splits + p.part_base + split) * D + d] = o;
+            if (d == 0) p.ws_lse[row * p.max_splits + p.part_base + split] = lse2;
         }
     }
-    if (nsplit == 1 || !p.counters || nsplit > kFuseMaxSplits) return;
+    if (ntot == 1 || !p.counters || ntot > kFuseMaxSplits) return;
 
     // ---- fused merge by the last-arriving CTA of this (sequence, kv head)
     float *w = const_cast<float *>(sm_l) + kNW * G;  // [G][kFuseMaxSplits] weights, then a flag
@@ -217,15 +235,16 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
         const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
         const float *ls = p.ws_lse + row * p.max_splits;
         float M = -INFINITY;
-        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(ls + s2));
+        for (int s2 = 0; s2 < ntot; ++s2) M = fmaxf(M, __ldcg(ls + (s2 < pre ? s2 : p.part_base + s2 - pre)));
         float den = 0.f;
-        for (int s2 = 0; s2 < nsplit; ++s2) {
-            const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(ls + s2) - M);
+        for (int s2 = 0; s2 < ntot; ++s2) {
+            const float e =
+                M == -INFINITY ? 0.f : exp2f(__ldcg(ls + (s2 < pre ? s2 : p.part_base + s2 - pre)) - M);
             w[j * kFuseMaxSplits + s2] = e;
             den += e;
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        for (int s2 = 0; s2 < nsplit; ++s2) w[j * kFuseMaxSplits + s2] *= inv;
+        for (int s2 = 0; s2 < ntot; ++s2) w[j * kFuseMaxSplits + s2] *= inv;
         if (p.lse) p.lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
     named_bar_sync(1, kNW * 32);
@@ -234,9 +253,9 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
         const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
         const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * p.max_splits * D) + d4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s2 = 0; s2 < nsplit; ++s2) {
+        for (int s2 = 0; s2 < ntot; ++s2) {
             const float ws = w[j * kFuseMaxSplits + s2];
-            const float4 v = __ldcg(src + (size_t)s2 * (D / 4));
+            const float4 v = __ldcg(src + (size_t)(s2 < pre ? s2 : p.part_base + s2 - pre) * (D / 4));
             acc.x += ws * v.x;
             acc.y += ws * v.y;
             acc.z += ws * v.z;
@@ -298,10 +317,12 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     }
     if (L < 0) L = 0;
     const int nblk = (int)((L + kBS - 1) / kBS);
-    const int blk0 = split * p.part_blocks;
+    const int sblk = start_block(p, b, L);
+    const int pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
+    const int blk0 = sblk + split * p.part_blocks;
     if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
     const int nloc = max(0, min(p.part_blocks, nblk - blk0));
-    const int nsplit = max(1, (nblk + p.part_blocks - 1) / p.part_blocks);
+    const int nsplit = max(1, (nblk - sblk + p.part_blocks - 1) / p.part_blocks);
 
     // ---- shared memory
     extern __shared__ __align__(128) char smem[];
@@ -533,7 +554,7 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     }
     named_bar_sync(1, kNW * 32);
 
-    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, tid);
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid);
 }
 
 // ---------------------------------------------------------------------------
@@ -631,10 +652,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     if (L < 0) L = 0;
     const int nblk = (int)((L + kBS - 1) / kBS);
-    const int blk0 = split * p.part_blocks;
-    if (blk0 >= nblk && split > 0) return;
+    const int sblk = start_block(p, b, L);
+    const int pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
+    const int blk0 = sblk + split * p.part_blocks;
+    if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
     const int nloc = max(0, min(p.part_blocks, nblk - blk0));
-    const int nsplit = max(1, (nblk + p.part_blocks - 1) / p.part_blocks);
+    const int nsplit = max(1, (nblk - sblk + p.part_blocks - 1) / p.part_blocks);
 
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -830,7 +853,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     }
     named_bar_sync(1, kNW * 32);
 
-    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, tid);
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid);
 }
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks) {
@@ -849,7 +872,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
                                                     int max_len_tokens, int batch,
                                                     int num_q_heads, int head_dim,
                                                     int part_blocks, int max_splits, void *out,
-                                                    int out_bf16, float *lse, int min_splits) {
+                                                    int out_bf16, float *lse, int min_splits,
+                                                    const int32_t *start_tokens, int part_base) {
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= batch * num_q_heads) return;
@@ -862,19 +886,28 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
     if (L > max_len_tokens) L = max_len_tokens;
     if (L < 0) L = 0;
     const int nblk = (int)((L + kBS - 1) / kBS);
-    const int nsplit = max(1, (nblk + part_blocks - 1) / part_blocks);
-    if (nsplit < min_splits) return;  // the decode kernel wrote the final result
+    int sblk = 0;  // as start_block() in the decode kernels
+    if (start_tokens) {
+        long long st = start_tokens[b];
+        st = st < 0 ? 0 : (st > L ? L : st);
+        sblk = (int)(st / kBS);
+    }
+    const int pre = sblk > 0 ? part_base : 0;
+    const int nsplit = max(1, (nblk - sblk + part_blocks - 1) / part_blocks);
+    const int ntot = pre + nsplit;
+    if (ntot < min_splits) return;  // the decode kernel wrote the final result
+    auto slot = [&](int s) { return s < pre ? s : part_base + s - pre; };
     const float *ls = ws_lse + (size_t)row * max_splits;
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ls[s]);
+    for (int s = 0; s < ntot; ++s) M = fmaxf(M, ls[slot(s)]);
     float den = 0.f;
-    for (int s = 0; s < nsplit; ++s) den += M == -INFINITY ? 0.f : exp2f(ls[s] - M);
+    for (int s = 0; s < ntot; ++s) den += M == -INFINITY ? 0.f : exp2f(ls[slot(s)] - M);
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int d = lane; d < head_dim; d += 32) {
         float num = 0.f;
         if (M != -INFINITY)
-            for (int s = 0; s < nsplit; ++s)
-                num += exp2f(ls[s] - M) * ws_o[((size_t)row * max_splits + s) * head_dim + d];
+            for (int s = 0; s < ntot; ++s)
+                num += exp2f(ls[slot(s)] - M) * ws_o[((size_t)row * max_splits + slot(s)) * head_dim + d];
         const float o = num * inv;
         if (out_bf16)
             reinterpret_cast<uint16_t *>(out)[(size_t)row * head_dim + d] = float_to_bf16_rn(o);
@@ -956,7 +989,9 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     const int G = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
     int pb = 0, ms = 0;
     split_plan(a.batch, a.num_kv_heads, a.max_blocks, a.num_splits, &pb, &ms);
-    const size_t need = decode_workspace_bytes(a.batch, a.num_q_heads, a.head_dim, ms);
+    if (a.part_base < 0 || (a.part_base > 0 && !a.start_tokens)) return KV_ERR_ARG;
+    const int slots = a.part_base + ms;  // workspace partial results per (sequence, query head)
+    const size_t need = decode_workspace_bytes(a.batch, a.num_q_heads, a.head_dim, slots);
     if (need > 0 && (!a.workspace || a.workspace_bytes < need)) return KV_ERR_ARG;
     if (ms > 65535 || a.batch > 65535 || a.num_kv_heads > 65535) return KV_ERR_UNSUPPORTED;
 
@@ -979,12 +1014,14 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.g = g;
     kp.scale_log2 = a.scale * 1.4426950408889634f;
     kp.part_blocks = pb;
-    kp.max_splits = ms;
+    kp.max_splits = slots;
+    kp.start_tokens = a.start_tokens;
+    kp.part_base = a.part_base;
     kp.out = a.out;
     kp.out_bf16 = a.out_dtype == KV_BF16;
     kp.lse = a.lse;
     kp.ws_o = static_cast<float *>(a.workspace);
-    kp.ws_lse = need > 0 ? kp.ws_o + (size_t)a.batch * a.num_q_heads * ms * a.head_dim : nullptr;
+    kp.ws_lse = need > 0 ? kp.ws_o + (size_t)a.batch * a.num_q_heads * slots * a.head_dim : nullptr;
     kp.err = a.err;
 
     kp.req_maps = a.req_maps;
@@ -1019,14 +1056,14 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
                 : (linear ? launch_g<64, false, true>(G, kp, grid, a.stream)
                           : launch_g<64, false, false>(G, kp, grid, a.stream));
     }
-    if (st != KV_OK || ms <= 1) return st;
+    if (st != KV_OK || slots <= 1) return st;
     const int min_splits = kp.counters ? kFuseMaxSplits + 1 : 2;
-    if (ms < min_splits) return st;  // every merge happens inside the decode kernel
+    if (slots < min_splits) return st;  // every merge happens inside the decode kernel
     const int rows = a.batch * a.num_q_heads;
     merge_kernel<<<(rows + 3) / 4, 128, 0, a.stream>>>(
         kp.ws_o, kp.ws_lse, a.seq_lens, linear ? a.mapped_tokens : nullptr, a.req_ids,
-        a.max_requests, a.max_blocks * kBS, a.batch, a.num_q_heads, a.head_dim, pb, ms, a.out,
-        kp.out_bf16, a.lse, min_splits);
+        a.max_requests, a.max_blocks * kBS, a.batch, a.num_q_heads, a.head_dim, pb, slots, a.out,
+        kp.out_bf16, a.lse, min_splits, a.start_tokens, a.part_base);
     return cuda_status(cudaGetLastError());
 }
 

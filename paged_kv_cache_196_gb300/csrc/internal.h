@@ -89,6 +89,11 @@ struct DecodeArgs {
     kv_dtype out_dtype;
     float *lse;
     int num_splits;
+    // cascade: the first start_tokens[b] tokens of sequence b (whole blocks)
+    // were attended elsewhere and left part_base partial results in slots
+    // [0, part_base) of the workspace; null / 0 otherwise
+    const int32_t *start_tokens;
+    int part_base;
     int *counters;
     long long counter_slots;
     void *workspace;

@@ -27,9 +27,12 @@ def _append_tokens(pool, k, v, slots):
         pk.kv_append(pool, dev(k), dev(v), dev(np.asarray(slots, np.int64)), len(slots))
 
 
-def build_and_step(inp, share: bool, max_blocks: int, seed: int):
+def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: int = 0):
     """Builds the cache (shared or private prefixes), runs the step; returns
-    (out, lse, tables, refcount checks, cow pair count)."""
+    (out, lse, tables, refcount checks, cow pair count, cascade out, cascade lse).
+    The cascade decode (shared layout only) reads each group's shared blocks
+    once; a sequence's shared tokens are its leading table entries that are
+    still the group's prefix blocks after the step's copy-on-write."""
     lens = inp["lens"]
     B, G, P = len(lens), inp["group_size"], inp["prefix_len"]
     hkv, d = inp["new_k"].shape[1], inp["new_k"].shape[2]
@@ -94,7 +97,32 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int):
     torch.cuda.synchronize()
     assert pk.kv_get_device_error(pool) == 0
     refs = {int(t): pk.kv_allocator_refcount(alloc, int(t)) for t in np.unique(tables[tables >= 0])}
-    res = host(out).astype(np.float64), host(lse).astype(np.float64), tables.copy(), refs, len(src)
+    out_c = lse_c = None
+    if share:
+        groups = -(-B // G)
+        group_seqs = np.full((groups, G), -1, np.int32)
+        shared = np.zeros(B, np.int32)
+        for b in range(B):
+            group_seqs[b // G, b % G] = b
+            tpl = templates[b // G]
+            k = 0
+            while k < len(tpl) and tables[b, k] == tpl[k]:
+                k += 1
+            shared[b] = k * BS
+        ps = pk.kv_cascade_plan(groups, hkv, P // BS, prefix_splits)
+        wsc = pk.kv_cascade_workspace_size(B, hq, hkv, d, max_blocks, 0, ps)
+        wc = torch.empty(max(wsc // 4, 1), dtype=torch.float32, device="cuda")
+        oc = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
+        lc = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+        pk.paged_decode_attention_cascade(pool, dev(inp["q"]), dev(tables), max_blocks,
+                                          dev(new_lens), B, hq, 1 / math.sqrt(d), dev(group_seqs),
+                                          groups, G, dev(shared), P // BS, ps, oc, pk.KV_F32, lc, 0,
+                                          wc, wsc)
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error(pool) == 0
+        out_c, lse_c = host(oc).astype(np.float64), host(lc).astype(np.float64)
+    res = (host(out).astype(np.float64), host(lse).astype(np.float64), tables.copy(), refs, len(src),
+           out_c, lse_c)
     pk.kv_pool_destroy(pool)
     return res
 
@@ -122,9 +150,10 @@ def oracle_step(inp):
     return oracle.paged_decode(pk_, pv_, tables, new_lens, inp["q"], 1 / math.sqrt(d))
 
 
-def _check(inp, max_blocks, sample=None):
-    out_s, lse_s, tab_s, refs, ncow = build_and_step(inp, True, max_blocks, seed=91)
-    out_p, lse_p, _, _, ncow_p = build_and_step(inp, False, max_blocks, seed=92)
+def _check(inp, max_blocks, prefix_splits=0):
+    out_s, lse_s, tab_s, refs, ncow, out_c, lse_c = build_and_step(inp, True, max_blocks, seed=91,
+                                                                   prefix_splits=prefix_splits)
+    out_p, lse_p, _, _, ncow_p, _, _ = build_and_step(inp, False, max_blocks, seed=92)
     # shared blocks == private copies, bit for bit
     np.testing.assert_array_equal(out_s, out_p)
     np.testing.assert_array_equal(lse_s, lse_p)
@@ -148,12 +177,24 @@ def _check(inp, max_blocks, sample=None):
     ref, ref_lse = oracle_step(inp)
     assert_close_scaled(out_s, ref, 2e-3, "shared-prefix step")
     np.testing.assert_allclose(lse_s, ref_lse, atol=1e-3)
+    # cascade decode: the same maths with the shared blocks read once per group
+    assert_close_scaled(out_c, ref, 2e-3, "cascade decode")
+    np.testing.assert_allclose(lse_c, ref_lse, atol=1e-3)
 
 
 def test_shared_prefix_step_two_groups():
     require_cuda()
     inp = W.shared_prefix_inputs(batch=32)
     _check(inp, max_blocks=(2048 + 1 + 15) // 16)
+
+
+@pytest.mark.parametrize("prefix_splits", [1, 3, 8])
+def test_cascade_prefix_splits_and_ragged_group(prefix_splits):
+    """Cascade with several key-range partitions of the prefix (8 = one per
+    128-key tile) and a last group with empty member slots (37 = 2 x 16 + 5)."""
+    require_cuda()
+    inp = W.shared_prefix_inputs(batch=37, seed_offset=1)
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits)
 
 
 @pytest.mark.slow
