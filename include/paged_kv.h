@@ -259,10 +259,13 @@ kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int 
 /* Chooses num_splits for paged_decode_attention / contig_decode_attention
  * from the sequence lengths as the host knows them (a serving host keeps its
  * own block tables, so it has them).  host_seq_lens: host int32[batch].
- * Prefers the smallest partitions whose CTAs all fit in one wave of at most
- * 2.4 CTAs per SM on this GPU (measured to stream fastest); when no split
- * fits, the largest partitions that still give at least three full waves.  The result depends only on the lengths, the batch
- * shape and the SM count.  Host only; *num_splits >= 1. */
+ * The bf16 / head_dim 128 decode runs partitions of 256 blocks or more with a
+ * deep copy ring at three CTAs per SM, shorter ones at five CTAs per SM.  The
+ * plan prefers one wave: the smallest long partitions whose CTAs fit in at
+ * most 2.4 per SM (measured to stream fastest), else the smallest short
+ * partitions that fit in five per SM; when no split fits, the largest
+ * partitions that still give several full waves.  The result depends only on
+ * the lengths, the batch shape and the SM count.  Host only; *num_splits >= 1. */
 kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_heads,
                          int max_blocks, int *num_splits);
 
@@ -281,7 +284,9 @@ kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_hea
  *   workspace     device scratch of at least kv_decode_workspace_size bytes
  *                 (may be NULL when that size is 0).
  * An empty sequence gives out = 0 and lse = -inf.  The result does not depend
- * on where the blocks sit in the pool (bit-identical for any placement). */
+ * on where the blocks sit in the pool (bit-identical for any placement).
+ * Decode calls on one pool must not run concurrently on the GPU (the fused
+ * split merge uses the pool's arrival counters): order them on one stream. */
 kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *block_tables,
                                  int max_blocks, const int32_t *seq_lens, int batch,
                                  int num_q_heads, float scale, void *out, kv_dtype out_dtype,

@@ -29,6 +29,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -54,11 +56,18 @@ namespace pkv {
 #ifndef PKV_TC_MIN_G
 #define PKV_TC_MIN_G 3   // smallest head group routed to the tensor-core decode
 #endif
+#ifndef PKV_TC_DEEP_BLOCKS
+#define PKV_TC_DEEP_BLOCKS 256  // partitions this long use the deep-ring tensor-core decode
+#endif
+#ifndef PKV_TC_MULTILANE
+#define PKV_TC_MULTILANE 1  // the four boxes of a K/V block are issued by four producer lanes
+#endif
 constexpr int kNW = PKV_DECODE_WARPS;    // consumer warps per CTA
 constexpr int kDecodeThreads = (kNW + 1) * 32;
 constexpr int kBS = 16;                  // tokens per block
 constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
 constexpr int kNStage = PKV_DECODE_STAGES;  // pipeline depth (a multiple of kNW)
+constexpr int kTcDeepBlocks = PKV_TC_DEEP_BLOCKS;
 // Splits per (sequence, kv head) merged inside the decode kernel by the last
 // CTA of that pair; longer plans leave the merge to merge_kernel.
 constexpr int kFuseMaxSplits = 32;
@@ -155,8 +164,8 @@ KV_DEVICE void reduce_scatter16(float *v, int lane) {
 
 // Bytes of the stage ring; the final cross-warp merge reuses it.
 template <int D, int G, bool BF16>
-constexpr size_t decode_ring_bytes() {
-    constexpr size_t ring = (size_t)kNStage * 2 * TileShape<D, BF16>::kBytes;
+constexpr size_t decode_ring_bytes(int nstage = kNStage) {
+    const size_t ring = (size_t)nstage * 2 * TileShape<D, BF16>::kBytes;
     constexpr size_t merge =
         (size_t)kNW * (G * D + 2 * G) * sizeof(float) + (G * kFuseMaxSplits + 4) * sizeof(float);
     return ((ring > merge ? ring : merge) + 127) / 128 * 128;
@@ -620,8 +629,94 @@ KV_DEVICE void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *
 
 constexpr int kTcTile = 16 * 128 * 2;  // one (block, head) tile: 4 KiB, two 2 KiB swizzled halves
 
-template <bool LINEAR>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
+// One 16-token block for the 8 (padded) query heads of a warp: S^T = K Q^T
+// on mma.sync, online softmax in the log2 domain, O^T += V^T P^T with P split
+// into bf16 hi + lo parts.  kt / vt: shared addresses of the block's swizzled
+// K and V tiles; ntok: valid tokens in the block (the rest are masked, their V
+// lanes zeroed).  State (m_run, l_run, o) is this lane's share.
+KV_DEVICE void tc_attend_block(const uint32_t (&qf)[8][2], uint32_t kt, uint32_t vt, int ntok,
+                               float scale_log2, int lane, float (&m_run)[2], float (&l_run)[2],
+                               float (&o)[8][4]) {
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3;
+    const int rowA = (lane & 7) + (mi & 1) * 8;   // K: token row (non-transposed A)
+    const int tokV = (lane & 7) + (mi >> 1) * 8;  // V: token row (transposed A)
+    // ---- S^T = K Q^T
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int chunk = 2 * (kk & 3) + (mi >> 1);
+        const uint32_t addr = kt + (kk >> 2) * (kTcTile / 2) + rowA * 128 + ((chunk ^ (rowA & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        mma::ldsm_x4(addr, a0, a1, a2, a3);
+        mma::mma_bf16(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+    }
+    // c0,c1: token g, heads 2t,2t+1; c2,c3: token g+8
+    const bool v0 = g < ntok, v1 = g + 8 < ntok;
+    float s0 = v0 ? c[0] * scale_log2 : -INFINITY;
+    float s1 = v0 ? c[1] * scale_log2 : -INFINITY;
+    float s2 = v1 ? c[2] * scale_log2 : -INFINITY;
+    float s3 = v1 ? c[3] * scale_log2 : -INFINITY;
+    float mh0 = fmaxf(s0, s2), mh1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+        mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, x));
+        mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, x));
+    }
+    const float mn0 = fmaxf(m_run[0], mh0), mn1 = fmaxf(m_run[1], mh1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+    const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
+    const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
+    l_run[0] = l_run[0] * al0 + (p0 + p2);
+    l_run[1] = l_run[1] * al1 + (p1 + p3);
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+    }
+    // ---- P^T fragments (bf16 hi + lo), via transpose of the S layout
+    const uint32_t h01 = mma::pack_bf16(p0, p1), h23 = mma::pack_bf16(p2, p3);
+    const uint32_t l01 = mma::pack_bf16(p0 - mma::bf16_lo_f(h01), p1 - mma::bf16_hi_f(h01));
+    const uint32_t l23 = mma::pack_bf16(p2 - mma::bf16_lo_f(h23), p3 - mma::bf16_hi_f(h23));
+    const uint32_t bh0 = mma::movm_t(h01), bh1 = mma::movm_t(h23);
+    const uint32_t bl0 = mma::movm_t(l01), bl1 = mma::movm_t(l23);
+    // token masks for the V fragments (pairs 2t,2t+1 and 2t+8,2t+9)
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (ntok < kBS) {
+        mlo = (2 * t < ntok ? 0xffffu : 0u) | (2 * t + 1 < ntok ? 0xffff0000u : 0u);
+        mhi = (2 * t + 8 < ntok ? 0xffffu : 0u) | (2 * t + 9 < ntok ? 0xffff0000u : 0u);
+    }
+    // ---- O^T += V^T P^T
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int cidx = 2 * mt + (mi & 1);
+        const uint32_t addr = vt + (cidx >> 3) * (kTcTile / 2) + tokV * 128 +
+                              (((cidx & 7) ^ (tokV & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        mma::ldsm_x4_t(addr, a0, a1, a2, a3);
+        // a0/a1: tokens 2t,2t+1; a2/a3: tokens 2t+8,2t+9.  Unused slots may
+        // hold anything: their lanes are zeroed, never multiplied by 0.
+        a0 &= mlo;
+        a1 &= mlo;
+        a2 &= mhi;
+        a3 &= mhi;
+        mma::mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+        mma::mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
+
+// NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
+// compiled for MINB resident CTAs per SM.
+template <bool LINEAR, int NST, int MINB>
+__global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
     constexpr int G = 8, D = 128;
@@ -661,12 +756,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
 
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    char *stages = smem;  // kNStage x (K tile, V tile), swizzled
-    constexpr size_t kRing = decode_ring_bytes<D, G, true>();
+    char *stages = smem;  // NST x (K tile, V tile), swizzled
+    constexpr size_t kRing = decode_ring_bytes<D, G, true>(NST);
+    static_assert(NST % kNW == 0, "each stage must belong to one consumer warp");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
-    uint64_t *empty = full + kNStage;
-    int *stage_valid = reinterpret_cast<int *>(empty + kNStage);
-    int32_t *tbl = stage_valid + kNStage;  // [part_blocks]
+    uint64_t *empty = full + NST;
+    int *stage_valid = reinterpret_cast<int *>(empty + NST);
+    int32_t *tbl = stage_valid + NST;  // [part_blocks]
 
     if (warp == kNW) {
         if constexpr (!LINEAR) {
@@ -674,7 +770,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
             for (int i = lane; i < nloc; i += 32) tbl[i] = __ldg(row + i);
         }
         if (lane == 0) {
-            for (int st = 0; st < kNStage; ++st) {
+            for (int st = 0; st < NST; ++st) {
                 mbar_init(&full[st], 1);
                 mbar_init(&empty[st], 32);
             }
@@ -687,37 +783,50 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_k) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
-            const uint64_t policy = l2_evict_first_policy();
-            int issued = 0;
-            for (int i = 0; i < nloc; ++i) {
-                const int st = i % kNStage, r = i / kNStage;
-                if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err)) break;
-                int y;
-                bool valid = true;
-                if constexpr (LINEAR) {
-                    y = (int)((long long)h * p.head_stride + (long long)(blk0 + i) * kBS);
-                } else {
-                    const int id = tbl[i];
-                    valid = id >= 0 && id < p.num_blocks;
-                    if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                    y = ((valid ? id : 0) * p.num_kv_heads + h) * kBS;
-                }
+        }
+        const uint64_t policy = l2_evict_first_policy();
+        int issued = 0;
+        for (int i = 0; i < nloc; ++i) {
+            const int st = i % NST, r = i / NST;
+            bool bad = false;
+            if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            int y;
+            bool valid = true;
+            if constexpr (LINEAR) {
+                y = (int)((long long)h * p.head_stride + (long long)(blk0 + i) * kBS);
+            } else {
+                const int id = tbl[i];
+                valid = id >= 0 && id < p.num_blocks;
+                y = ((valid ? id : 0) * p.num_kv_heads + h) * kBS;
+            }
+            char *dst = stages + st * 2 * kTcTile;
+            if (lane == 0) {
+                if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
                 stage_valid[st] = valid ? 1 : 0;
-                char *dst = stages + st * 2 * kTcTile;
-                if (valid) {
+                if (valid)
                     mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
+                else
+                    mbar_arrive(&full[st]);
+            }
+            if (valid) {
+                if (PKV_TC_MULTILANE) {
+                    // lane x issues box x: K half 0, K half 1, V half 0, V half 1
+                    if (lane < 4)
+                        mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
+                                   lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
+                } else if (lane == 0) {
                     mma::tma2d(dst, map_k, 0, y, &full[st], policy);
                     mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
                     mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
                     mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
-                } else {
-                    mbar_arrive(&full[st]);
                 }
-                issued = i + 1;
             }
-            for (int st = 0; st < kNStage && st < issued; ++st)
-                mbar_wait(&full[st], ((issued - 1 - st) / kNStage) & 1, p.err);
+            issued = i + 1;
         }
+        if (lane == 0)
+            for (int st = 0; st < NST && st < issued; ++st)
+                mbar_wait(&full[st], ((issued - 1 - st) / NST) & 1, p.err);
         return;
     }
 
@@ -742,88 +851,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     const uint32_t stage_base = smem_addr(stages);
-    // ldmatrix row / chunk selectors for this lane
-    const int mi = lane >> 3;
-    const int rowA = (lane & 7) + (mi & 1) * 8;      // K: token row (non-transposed A)
-    const int tokV = (lane & 7) + (mi >> 1) * 8;     // V: token row (transposed A)
 
     for (int i = warp; i < nloc; i += kNW) {
-        const int st = i % kNStage, r = i / kNStage;
+        const int st = i % NST, r = i / NST;
         if (!mbar_wait(&full[st], r & 1, p.err)) break;
         int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
         if (!stage_valid[st]) ntok = 0;
         const uint32_t kt = stage_base + st * 2 * kTcTile;
         const uint32_t vt = kt + kTcTile;
 
-        // ---- S^T = K Q^T
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const int chunk = 2 * (kk & 3) + (mi >> 1);
-            const uint32_t addr = kt + (kk >> 2) * (kTcTile / 2) + rowA * 128 + ((chunk ^ (rowA & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            mma::ldsm_x4(addr, a0, a1, a2, a3);
-            mma::mma_bf16(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-        }
-        // c0,c1: token g, heads 2t,2t+1; c2,c3: token g+8
-        const bool v0 = g < ntok, v1 = g + 8 < ntok;
-        float s0 = v0 ? c[0] * p.scale_log2 : -INFINITY;
-        float s1 = v0 ? c[1] * p.scale_log2 : -INFINITY;
-        float s2 = v1 ? c[2] * p.scale_log2 : -INFINITY;
-        float s3 = v1 ? c[3] * p.scale_log2 : -INFINITY;
-        float mh0 = fmaxf(s0, s2), mh1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int x = 4; x <= 16; x <<= 1) {
-            mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, x));
-            mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, x));
-        }
-        const float mn0 = fmaxf(m_run[0], mh0), mn1 = fmaxf(m_run[1], mh1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m_run[0] - mu0), al1 = exp2f(m_run[1] - mu1);
-        m_run[0] = mn0;
-        m_run[1] = mn1;
-        const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
-        const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
-        l_run[0] = l_run[0] * al0 + (p0 + p2);
-        l_run[1] = l_run[1] * al1 + (p1 + p3);
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-            }
-        }
-        // ---- P^T fragments (bf16 hi + lo), via transpose of the S layout
-        const uint32_t h01 = mma::pack_bf16(p0, p1), h23 = mma::pack_bf16(p2, p3);
-        const uint32_t l01 = mma::pack_bf16(p0 - mma::bf16_lo_f(h01), p1 - mma::bf16_hi_f(h01));
-        const uint32_t l23 = mma::pack_bf16(p2 - mma::bf16_lo_f(h23), p3 - mma::bf16_hi_f(h23));
-        const uint32_t bh0 = mma::movm_t(h01), bh1 = mma::movm_t(h23);
-        const uint32_t bl0 = mma::movm_t(l01), bl1 = mma::movm_t(l23);
-        // token masks for the V fragments (pairs 2t,2t+1 and 2t+8,2t+9)
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (ntok < kBS) {
-            mlo = (2 * t < ntok ? 0xffffu : 0u) | (2 * t + 1 < ntok ? 0xffff0000u : 0u);
-            mhi = (2 * t + 8 < ntok ? 0xffffu : 0u) | (2 * t + 9 < ntok ? 0xffff0000u : 0u);
-        }
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int cidx = 2 * mt + (mi & 1);
-            const uint32_t addr = vt + (cidx >> 3) * (kTcTile / 2) + tokV * 128 +
-                                  (((cidx & 7) ^ (tokV & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            mma::ldsm_x4_t(addr, a0, a1, a2, a3);
-            // a0/a1: tokens 2t,2t+1; a2/a3: tokens 2t+8,2t+9.  Unused slots may
-            // hold anything: their lanes are zeroed, never multiplied by 0.
-            a0 &= mlo;
-            a1 &= mlo;
-            a2 &= mhi;
-            a3 &= mhi;
-            mma::mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma::mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
-        }
+        tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
         __syncwarp();
         mbar_arrive(&empty[st]);
     }
@@ -856,9 +893,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid);
 }
 
-static size_t decode_tc_smem_bytes(bool linear, int part_blocks) {
-    return 1024 + decode_ring_bytes<128, 8, true>() + 2 * kNStage * sizeof(uint64_t) +
-           kNStage * sizeof(int) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
+static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst) {
+    return 1024 + decode_ring_bytes<128, 8, true>(nst) + 2 * nst * sizeof(uint64_t) +
+           nst * sizeof(int) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
 }
 
 // Merges the per-split results of sequences cut into more than one split:
@@ -1035,11 +1072,18 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     const bool use_tc = bf && a.head_dim == 128 && g >= PKV_TC_MIN_G &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
     if (use_tc) {
-        const size_t smem = decode_tc_smem_bytes(linear, pb);
+        // Long partitions: a deep ring (8 stages) and 3 CTAs per SM; short
+        // ones: more CTAs at once (5 per SM) with 4 stages each.  Sweeps on
+        // GB300 (Llama-3-8B shape, 129-block partitions: 5959 vs 5502 GB/s;
+        // Yi-6B shape, 384-512-block partitions: 6288 vs 5965 GB/s).
+        const bool deep = pb >= kTcDeepBlocks;
+        const int nst = deep ? 8 : 4;
+        const size_t smem = decode_tc_smem_bytes(linear, pb, nst);
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = linear ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+        auto fn = deep ? (linear ? decode_tc_kernel<true, 8, 3> : decode_tc_kernel<false, 8, 3>)
+                       : (linear ? decode_tc_kernel<true, 4, 5> : decode_tc_kernel<false, 4, 5>);
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
@@ -1090,12 +1134,17 @@ kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_hea
         *num_splits = 1;
         return KV_OK;
     }
-    // Both decode kernels keep up to three CTAs resident per SM, but a single
-    // wave streams fastest at about two to two and a half CTAs per SM (sweeps
-    // of the Yi-6B-shaped workload on GB300: 2.0-2.3 per SM reach ~0.95 of the
-    // copy bandwidth, 2.7-3.0 per SM drop to ~0.65).
-    const long long slots = (long long)(2.4 * sm_count());
-    const long long resident = 3LL * sm_count();
+    // The tensor-core decode runs long partitions (>= kTcDeepBlocks blocks)
+    // with a deep ring at three CTAs per SM and shorter ones at five CTAs per
+    // SM.  A deep-ring wave streams fastest at about two to two and a half
+    // CTAs per SM (sweeps of the Yi-6B-shaped workload on GB300: 2.0-2.3 per
+    // SM reach ~0.95 of the copy bandwidth, 2.7-3.0 per SM drop to ~0.65); the
+    // five-per-SM kernel is best with a full single wave (Llama-3-8B shape:
+    // 760 CTAs on 152 SMs, 0.89).  The CUDA-core decode keeps three per SM.
+    const int sm = sm_count();
+    auto deep = [&](int pb) { return pb >= kTcDeepBlocks; };
+    auto one_wave = [&](int pb) { return deep(pb) ? (long long)(2.4 * sm) : 5LL * sm; };
+    auto resident = [&](int pb) { return deep(pb) ? 3LL * sm : 5LL * sm; };
     std::vector<int> nblk(batch);
     int longest = 1;
     for (int b = 0; b < batch; ++b) {
@@ -1116,23 +1165,25 @@ kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_hea
         split_plan(batch, num_kv_heads, max_blocks, splits, &pb, &ms);
         return pb;
     };
-    // 1) One wave if it fits: the smallest partitions whose CTAs all run at
-    //    once (every CTA streams at the same time, none waits for a slot),
-    //    at most `slots` of them.
-    // 2) Otherwise at least three waves of smaller partitions, so the last,
-    //    partly filled wave is a small share of the time.
-    int best = 0;
+    // 1) One wave if it fits (every CTA streams at the same time, none waits
+    //    for a slot): the smallest deep-ring partitions that fit, else the
+    //    smallest short partitions that fit.
+    // 2) Otherwise the largest partitions that still give several full waves
+    //    (three deep, two short), so the last, partly filled wave is a small
+    //    share of the time.
+    int best_deep = 0, best_wide = 0;
     for (int s = 1; s <= 4096; ++s) {
         const int pb = plan_pb(s);
-        if (ctas(pb) <= slots) best = s;  // more splits -> smaller partitions
+        if (ctas(pb) <= one_wave(pb)) (deep(pb) ? best_deep : best_wide) = s;
         if (pb <= kNW) break;
     }
+    int best = best_deep ? best_deep : best_wide;
     if (best == 0) {
         best = 1;
         for (int s = 1; s <= 4096; ++s) {
             const int pb = plan_pb(s);
             best = s;
-            if (ctas(pb) >= 3 * resident || pb <= 32) break;
+            if (ctas(pb) >= (deep(pb) ? 3 : 2) * resident(pb) || pb <= 32) break;
         }
     }
     *num_splits = best;
