@@ -317,21 +317,32 @@ def run_ours(args, rank, world, local_rank):
     value = job_throughput(kv_bytes, K, world, total_ms) / 1e9
     tokens_per_s = job_throughput(B, K, world, total_ms)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: each step copies
+    # its inputs (q, the new k/v, the slots or positions, the lengths) from one
+    # pinned host buffer in a single transfer, runs the step on views of the
+    # device copy, and reads the output back.
     Ke = min(K, 2000)
-    h_q = torch.from_numpy(inp["q"].view(np.int16)).pin_memory()
-    h_k = k_new.cpu().pin_memory()
-    h_v = v_new.cpu().pin_memory()
-    h_out = torch.empty((B, hq, d), dtype=torch.int16).pin_memory()
+    h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu(),
+               torch.from_numpy(last.astype(np.int32) if contig else slots), torch.from_numpy(lens)]
+    offs, total = [], 0
+    for t in h_parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    views = []
+    for t, o in zip(h_parts, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].view(t.dtype).copy_(t.reshape(-1))
+        views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
+    q, k_new, v_new = views[0], views[1], views[2]
     if contig:
-        h_idx = torch.from_numpy(last.astype(np.int32)).pin_memory()
-        d_idx = d_pos
+        d_pos = views[3]
     else:
-        h_idx = torch.from_numpy(slots).pin_memory()
-        d_idx = d_slots
-    h_lens = torch.from_numpy(lens).pin_memory()
-    h2d = h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_idx.numel() * h_idx.element_size() \
-        + h_lens.numel() * 4
+        d_slots = views[3]
+    d_lens = views[4]
+    h_out = torch.empty((B, hq, d), dtype=torch.int16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_parts)
     d2h = h_out.numel() * 2
     if dist:
         tdist.barrier()
@@ -340,11 +351,7 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(Ke):
-        q.copy_(h_q, non_blocking=True)
-        k_new.copy_(h_k, non_blocking=True)
-        v_new.copy_(h_v, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         append()
         attend()
         h_out.copy_(out, non_blocking=True)
