@@ -209,6 +209,27 @@ kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool);
 /* The pool's allocator (borrowed; destroyed with the pool). */
 kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out);
 
+/* Block manager calls on the pool's own allocator ("Makale Bulteni --
+ * PagedAttention ve vLLM", "Iddia ve Gerceklik": blocks come from a free
+ * pool on demand, are shared between sequences by reference and are copied
+ * on write).  Host only, like the kv_allocator_* calls they wrap:
+ *   kv_alloc_blocks   n free blocks (refcount 1) into ids_out; KV_ERR_OOM
+ *                     (nothing taken) if fewer are free;
+ *   kv_share_blocks   one more reference on each listed block;
+ *   kv_free_blocks    one reference fewer; a block reaching 0 is free again. */
+kv_status kv_alloc_blocks(kv_pool_t p, int n, int32_t *ids_out);
+kv_status kv_share_blocks(kv_pool_t p, int n, const int32_t *ids);
+kv_status kv_free_blocks(kv_pool_t p, int n, const int32_t *ids);
+
+/* Copy-on-write of one block before a write into it: if *block_id_inout is
+ * held by more than one reference, a free block is taken, the whole block
+ * (all heads and slots of K and V) is copied into it on `stream`, the old
+ * block loses this caller's reference, *block_id_inout becomes the new id
+ * and *copied = 1.  A block held once is left as is (*copied = 0).
+ * KV_ERR_ARG for a free or out-of-range id; KV_ERR_OOM (nothing changed)
+ * when no block is free.  Batches: kv_prepare_append_batch + kv_copy_blocks. */
+kv_status kv_cow_if_shared(kv_pool_t p, int32_t *block_id_inout, int *copied, void *stream);
+
 /* KV append: writes the new tokens' keys and values into their pool slots
  * ("Makale Bulteni -- PagedAttention ve vLLM", "Iddia ve Gerceklik";
  * "PagedAttention Nedir?", "Nasil Calisir?" steps 1-3).

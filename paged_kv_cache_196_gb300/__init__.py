@@ -21,7 +21,8 @@ __all__ = [
     "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch",
     "kv_prefix_cache_create", "kv_prefix_cache_destroy", "kv_prefix_cache_match",
     "kv_prefix_cache_insert", "kv_prefix_cache_evict", "kv_prefix_cache_stats", "kv_pool_create", "kv_pool_destroy",
-    "kv_pool_ptrs", "kv_pool_allocator", "kv_append", "kv_copy_blocks", "kv_swap_out",
+    "kv_pool_ptrs", "kv_pool_allocator", "kv_alloc_blocks", "kv_share_blocks", "kv_free_blocks",
+    "kv_cow_if_shared", "kv_append", "kv_copy_blocks", "kv_swap_out",
     "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_decode_attention_noalloc", "kv_cascade_plan", "kv_cascade_workspace_size",
@@ -76,6 +77,10 @@ _SIGS = {
     "kv_pool_destroy": [_vp],
     "kv_pool_ptrs": [_vp, _P(_vp), _P(_vp)],
     "kv_pool_allocator": [_vp, _P(_vp)],
+    "kv_alloc_blocks": [_vp, _i32, _vp],
+    "kv_share_blocks": [_vp, _i32, _vp],
+    "kv_free_blocks": [_vp, _i32, _vp],
+    "kv_cow_if_shared": [_vp, _P(_i32), _P(_i32), _vp],
     "kv_append": [_vp, _vp, _vp, _vp, _i32, _vp],
     "kv_copy_blocks": [_vp, _vp, _vp, _i32, _vp],
     "kv_swap_out": [_vp, _vp, _i32, _vp, _vp],
@@ -309,6 +314,30 @@ def kv_pool_allocator(p: int) -> int:
     a = _vp()
     _check(lib().kv_pool_allocator(p, ctypes.byref(a)), "kv_pool_allocator")
     return a.value
+
+
+def kv_alloc_blocks(p: int, ids_out):
+    """Fills ids_out (int32 numpy array) with len(ids_out) fresh blocks of the pool."""
+    _check(lib().kv_alloc_blocks(p, len(ids_out), _ptr(ids_out)), "kv_alloc_blocks")
+
+
+def kv_share_blocks(p: int, ids):
+    """ids: int32 numpy array."""
+    _check(lib().kv_share_blocks(p, len(ids), _ptr(ids)), "kv_share_blocks")
+
+
+def kv_free_blocks(p: int, ids):
+    """ids: int32 numpy array."""
+    _check(lib().kv_free_blocks(p, len(ids), _ptr(ids)), "kv_free_blocks")
+
+
+def kv_cow_if_shared(p: int, block_id: int, stream=None):
+    """Returns (block id to write into, copied?)."""
+    bid = _i32(block_id)
+    copied = _i32()
+    _check(lib().kv_cow_if_shared(p, ctypes.byref(bid), ctypes.byref(copied), _stream(stream)),
+           "kv_cow_if_shared")
+    return bid.value, bool(copied.value)
 
 
 def kv_append(p: int, k_new, v_new, slot_mapping, num_tokens: int, stream=None):

@@ -87,6 +87,17 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
     }
 }
 
+// Copies one whole block (all heads and slots of K and V), src -> dst; the
+// host checked both ids.
+__global__ void __launch_bounds__(256) copy_block_kernel(uint4 *__restrict__ k_pool,
+                                                         uint4 *__restrict__ v_pool, int src,
+                                                         int dst, int block_chunks) {
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < block_chunks; c += gridDim.x * blockDim.x) {
+        k_pool[(long long)dst * block_chunks + c] = k_pool[(long long)src * block_chunks + c];
+        v_pool[(long long)dst * block_chunks + c] = v_pool[(long long)src * block_chunks + c];
+    }
+}
+
 // Swap: whole blocks (K and V, all heads) between the pool and a buffer the
 // GPU can address directly (pinned host memory on this system: the stores /
 // loads cross NVLink-C2C or PCIe).  Host layout: [n][K|V][block chunks].
@@ -191,6 +202,43 @@ kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool) {
 kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out) {
     if (!p || !out) return KV_ERR_ARG;
     *out = p->alloc;
+    return KV_OK;
+}
+
+kv_status kv_alloc_blocks(kv_pool_t p, int n, int32_t *ids_out) {
+    if (!p) return KV_ERR_ARG;
+    return kv_allocator_alloc(p->alloc, n, ids_out);
+}
+
+kv_status kv_share_blocks(kv_pool_t p, int n, const int32_t *ids) {
+    if (!p) return KV_ERR_ARG;
+    return kv_allocator_share(p->alloc, n, ids);
+}
+
+kv_status kv_free_blocks(kv_pool_t p, int n, const int32_t *ids) {
+    if (!p) return KV_ERR_ARG;
+    return kv_allocator_free(p->alloc, n, ids);
+}
+
+kv_status kv_cow_if_shared(kv_pool_t p, int32_t *block_id_inout, int *copied, void *stream) {
+    if (!p || !block_id_inout || !copied) return KV_ERR_ARG;
+    *copied = 0;
+    const int32_t old = *block_id_inout;
+    int rc = 0;
+    if (kv_allocator_refcount(p->alloc, old, &rc) != KV_OK || rc <= 0) return KV_ERR_ARG;
+    if (rc == 1) return KV_OK;  // private already: write in place
+    int32_t fresh = -1;
+    if (kv_status st = kv_allocator_alloc(p->alloc, 1, &fresh)) return st;
+    const int block_chunks = p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype) / 16;
+    copy_block_kernel<<<grid_for(block_chunks, 256), 256, 0, as_stream(stream)>>>(
+        (uint4 *)p->k, (uint4 *)p->v, old, fresh, block_chunks);
+    if (kv_status st = cuda_status(cudaGetLastError())) {
+        kv_allocator_free(p->alloc, 1, &fresh);
+        return st;
+    }
+    kv_allocator_free(p->alloc, 1, &old);  // the other holders keep it (rc > 1)
+    *block_id_inout = fresh;
+    *copied = 1;
     return KV_OK;
 }
 
