@@ -262,21 +262,23 @@ def run_ours(args, rank, world, local_rank):
     else:
         d_pos = torch.from_numpy(last.astype(np.int32)).cuda()
 
+    # One step: the new tokens' K/V go into their slots, then decode over
+    # all tokens.  Paged: one call (the append fused into the decode kernel);
+    # contiguous: the append, then the decode.
     def append():
         if contig:
             pk.kv_contig_append(ctx, k_new, v_new, req_ids, d_pos, B)
-        else:
-            pk.kv_append(pool, k_new, v_new, d_slots, B)
 
     def attend():
         if contig:
             pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, pk.KV_BF16,
                                        None, splits, ws, ws_bytes)
         else:
-            pk.paged_decode_attention(pool, q, d_tables, max_blocks, d_lens, B, hq, scale, out,
-                                      pk.KV_BF16, None, splits, ws, ws_bytes)
+            pk.paged_append_and_decode(pool, q, k_new, v_new, d_slots, d_tables, max_blocks, d_lens,
+                                       B, hq, scale, out, pk.KV_BF16, None, splits, ws, ws_bytes)
 
-    launches_per_step = 2 + (1 if max_splits > 1 else 0)
+    # merge_kernel runs only for plans of more than 32 splits
+    launches_per_step = (2 if contig else 1) + (1 if max_splits > 32 else 0)
 
     # ---- warm-up
     for _ in range(args.warmup):
@@ -401,8 +403,10 @@ def run_ours(args, rank, world, local_rank):
         "decode_tokens_per_s": round(tokens_per_s, 1),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("contig_decode_attention" if contig else "paged_decode_attention")
-                      + f" ({kname}" + (" + split merge kernel)" if max_splits > 32 else ")"),
+            "kernel": ("contig_decode_attention" if contig else "paged_append_and_decode")
+                      + f" ({kname}" + ("" if contig or kname != "decode_tc_kernel" else
+                                         ", the append fused")
+                      + (" + split merge kernel)" if max_splits > 32 else ")"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",

@@ -314,6 +314,27 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
                                  float *lse_out, int num_splits, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* One decode step: kv_append of one new token per sequence followed by
+ * paged_decode_attention ("PagedAttention Nedir?", "Nasil Calisir?": the
+ * new token's KV is written into its block, then the step attends all
+ * tokens).  Same results as those two calls (the pool receives the same
+ * bytes, the output is bit-identical).
+ *   k_new, v_new   device [batch][num_kv_heads][head_dim], pool dtype, 16-byte
+ *                  aligned: the token appended to each sequence;
+ *   slot_mapping   device int64[batch]: its slot; negative = none.  The slot
+ *                  must be position seq_lens[b] - 1 of sequence b (seq_lens
+ *                  count the new token) in a block only sequence b holds
+ *                  (copy shared blocks first: kv_cow_if_shared / kv_copy_blocks).
+ * Other arguments as paged_decode_attention.  For bf16 pools with head_dim
+ * 128 and >= 3 query heads per kv head the append is fused into the decode
+ * kernel (one launch); other shapes run the two calls. */
+kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
+                                  const void *v_new, const int64_t *slot_mapping,
+                                  const int32_t *block_tables, int max_blocks,
+                                  const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                                  void *out, kv_dtype out_dtype, float *lse_out, int num_splits,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* paged_decode_attention without a workspace argument, for callers that
  * cannot allocate device memory where they run decode (a plugin whose host
  * framework owns all device memory; a serving loop that must not call

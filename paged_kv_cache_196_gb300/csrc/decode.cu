@@ -96,6 +96,11 @@ struct DecodeKParams {
     int max_splits;
     const int32_t *start_tokens;  // cascade: tokens of each sequence attended elsewhere, or null
     int part_base;                // cascade: workspace slots [0, part_base) hold those results
+    // fused append (tensor-core decode only): each sequence's new token
+    // ([batch][num_kv_heads][128] bf16) and its pool slot, or null
+    const uint4 *new_k;
+    const uint4 *new_v;
+    const int64_t *new_slots;
     void *out;
     int out_bf16;
     float *lse;
@@ -762,7 +767,8 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
     uint64_t *empty = full + NST;
     int *stage_valid = reinterpret_cast<int *>(empty + NST);
-    int32_t *tbl = stage_valid + NST;  // [part_blocks]
+    uint4 *newrow = reinterpret_cast<uint4 *>(stage_valid + NST);  // [32]: fused append's K, V rows
+    int32_t *tbl = reinterpret_cast<int32_t *>(newrow + 32);       // [part_blocks]
 
     if (warp == kNW) {
         if constexpr (!LINEAR) {
@@ -832,6 +838,27 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
 
     // ---- consumer warps: lane = (g = lane / 4, t = lane % 4)
     const int g = lane >> 2, t = lane & 3;
+    // Fused append: the last split of (b, h) writes the new token's K/V row
+    // (head h) to its pool slot and, since the block holding it may have been
+    // copied before that write lands, patches the row into its own copy of
+    // the sequence's last block.  Lane x < 16 carries 16-byte chunk x of the
+    // K row, lane 16 + x chunk x of the V row.
+    const bool fuse = p.new_k != nullptr && split == nsplit - 1;
+    const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk;
+    if (fuse && warp == (patch ? (nloc - 1) % kNW : 0)) {
+        const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
+        const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
+        newrow[lane] = v;  // kept in shared memory until the last block arrives
+        const long long slot = p.new_slots[b];
+        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
+            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
+            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
+                         row * (D * 2 / 16) + (lane & 15);
+            *dst = v;
+        } else if (slot >= 0 && lane == 0) {
+            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+        }
+    }
     // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
     uint32_t qf[8][2];
     {
@@ -859,6 +886,14 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         if (!stage_valid[st]) ntok = 0;
         const uint32_t kt = stage_base + st * 2 * kTcTile;
         const uint32_t vt = kt + kTcTile;
+        if (patch && i == nloc - 1 && ntok > 0) {
+            // the new token is row (L - 1) % 16 of the sequence's last block
+            const int orow = (int)((L - 1) % kBS), c = lane & 15;
+            char *tile = stages + st * 2 * kTcTile + (lane < 16 ? 0 : kTcTile);
+            *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTcTile / 2) + orow * 128 +
+                                       (((c & 7) ^ (orow & 7)) << 4)) = newrow[lane];
+            __syncwarp();
+        }
 
         tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
         __syncwarp();
@@ -895,7 +930,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst) {
     return 1024 + decode_ring_bytes<128, 8, true>(nst) + 2 * nst * sizeof(uint64_t) +
-           nst * sizeof(int) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
+           nst * sizeof(int) + 32 * sizeof(uint4) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
 }
 
 // Merges the per-split results of sequences cut into more than one split:
@@ -1054,6 +1089,9 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.max_splits = slots;
     kp.start_tokens = a.start_tokens;
     kp.part_base = a.part_base;
+    kp.new_k = static_cast<const uint4 *>(a.new_k);
+    kp.new_v = static_cast<const uint4 *>(a.new_v);
+    kp.new_slots = a.new_slots;
     kp.out = a.out;
     kp.out_bf16 = a.out_dtype == KV_BF16;
     kp.lse = a.lse;
@@ -1071,6 +1109,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     // tiled-TMA maps of the K/V storage are available.
     const bool use_tc = bf && a.head_dim == 128 && g >= PKV_TC_MIN_G &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
+    if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
     if (use_tc) {
         // Long partitions: a deep ring (8 stages) and 3 CTAs per SM; short
         // ones: more CTAs at once (5 per SM) with 4 stages each.  Sweeps on
@@ -1234,6 +1273,57 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
         a.pool_map_k = &p->tmap_k;
         a.pool_map_v = &p->tmap_v;
     }
+    return launch_decode(a, false);
+}
+
+kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
+                                  const void *v_new, const int64_t *slot_mapping,
+                                  const int32_t *block_tables, int max_blocks,
+                                  const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                                  void *out, kv_dtype out_dtype, float *lse_out, int num_splits,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (!p || batch < 0 || max_blocks < 0 || (batch > 0 && max_blocks > 0 && !block_tables))
+        return KV_ERR_ARG;
+    if (batch == 0) return KV_OK;
+    if (!k_new || !v_new || !slot_mapping) return KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return KV_ERR_ARG;
+    DecodeArgs a{};
+    a.q = q;
+    a.k_pool = p->k;
+    a.v_pool = p->v;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.num_blocks = p->num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.head_dim = p->head_dim;
+    a.dtype = p->dtype;
+    a.scale = scale;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse_out;
+    a.num_splits = num_splits;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.err = p->err;
+    a.counters = p->counters;
+    a.counter_slots = kv_pool::kCounterSlots;
+    a.stream = as_stream(stream);
+    if (p->dtype == KV_BF16 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
+        a.pool_map_k = &p->tmap_k;
+        a.pool_map_v = &p->tmap_v;
+    }
+    a.new_k = k_new;
+    a.new_v = v_new;
+    a.new_slots = slot_mapping;
+    const kv_status st = launch_decode(a, false);
+    if (st != KV_ERR_UNSUPPORTED) return st;
+    // shapes the fused kernel does not cover: the append, then the decode
+    if (kv_status st1 = kv_append(p, k_new, v_new, slot_mapping, batch, stream)) return st1;
+    a.new_k = a.new_v = nullptr;
+    a.new_slots = nullptr;
     return launch_decode(a, false);
 }
 

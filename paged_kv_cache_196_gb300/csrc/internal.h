@@ -94,6 +94,11 @@ struct DecodeArgs {
     // [0, part_base) of the workspace; null / 0 otherwise
     const int32_t *start_tokens;
     int part_base;
+    // fused append of one new token per sequence (tensor-core decode only):
+    // device [batch][num_kv_heads][head_dim] K and V rows and int64 slots, or null
+    const void *new_k;
+    const void *new_v;
+    const int64_t *new_slots;
     int *counters;
     long long counter_slots;
     void *workspace;
