@@ -259,6 +259,10 @@ def run_ours(args, rank, world, local_rank):
     part_blocks, max_splits = pk.kv_decode_split_plan(B, hkv, max_blocks, splits)
     if not contig:
         d_slots = torch.from_numpy(slots).cuda()
+        # the grid takes the sequences longest first (one wave loads the SMs evenly)
+        h_order = np.zeros(B, np.int32)
+        pk.kv_decode_order(lens.astype(np.int32), h_order)
+        d_order = torch.from_numpy(h_order).cuda()
     else:
         d_pos = torch.from_numpy(last.astype(np.int32)).cuda()
 
@@ -275,7 +279,8 @@ def run_ours(args, rank, world, local_rank):
                                        None, splits, ws, ws_bytes)
         else:
             pk.paged_append_and_decode(pool, q, k_new, v_new, d_slots, d_tables, max_blocks, d_lens,
-                                       B, hq, scale, out, pk.KV_BF16, None, splits, ws, ws_bytes)
+                                       B, hq, scale, out, pk.KV_BF16, None, splits, ws, ws_bytes,
+                                       seq_order=d_order)
 
     # merge_kernel runs only for plans of more than 32 splits
     launches_per_step = (2 if contig else 1) + (1 if max_splits > 32 else 0)
@@ -326,6 +331,8 @@ def run_ours(args, rank, world, local_rank):
     Ke = min(K, 2000)
     h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu(),
                torch.from_numpy(last.astype(np.int32) if contig else slots), torch.from_numpy(lens)]
+    if not contig:
+        h_parts.append(torch.from_numpy(h_order))  # recomputed on the host for every batch
     offs, total = [], 0
     for t in h_parts:
         offs.append(total)
@@ -343,6 +350,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         d_slots = views[3]
     d_lens = views[4]
+    if not contig:
+        d_order = views[5]
     h_out = torch.empty((B, hq, d), dtype=torch.int16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h_parts)
     d2h = h_out.numel() * 2

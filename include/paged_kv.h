@@ -290,6 +290,11 @@ kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int 
 kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_heads,
                          int max_blocks, int *num_splits);
 
+/* The batch's sequences ordered by length, longest first (ties in batch
+ * order), for the seq_order argument of paged_append_and_decode.  Host only:
+ * host_seq_lens and order_out are host int32[batch]. */
+kv_status kv_decode_order(const int32_t *host_seq_lens, int batch, int32_t *order_out);
+
 /* Paged decode attention: one query token per sequence attends all
  * seq_lens[b] tokens of its cache, reading K/V blocks through the block
  * table ("PagedAttention Nedir?", "Nasil Calisir?" step 4), with
@@ -325,13 +330,18 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
  *                  must be position seq_lens[b] - 1 of sequence b (seq_lens
  *                  count the new token) in a block only sequence b holds
  *                  (copy shared blocks first: kv_cow_if_shared / kv_copy_blocks).
+ *   seq_order      device int32[batch] or NULL: a permutation of the batch,
+ *                  the order in which the kernel's grid takes the sequences
+ *                  (kv_decode_order: longest first, so one wave of CTAs loads
+ *                  the SMs evenly).  It changes no result.
  * Other arguments as paged_decode_attention.  For bf16 pools with head_dim
  * 128 and >= 3 query heads per kv head the append is fused into the decode
  * kernel (one launch); other shapes run the two calls. */
 kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
                                   const void *v_new, const int64_t *slot_mapping,
                                   const int32_t *block_tables, int max_blocks,
-                                  const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                                  const int32_t *seq_lens, const int32_t *seq_order, int batch,
+                                  int num_q_heads, float scale,
                                   void *out, kv_dtype out_dtype, float *lse_out, int num_splits,
                                   void *workspace, size_t workspace_bytes, void *stream);
 

@@ -25,7 +25,7 @@ __all__ = [
     "kv_cow_if_shared", "kv_append", "kv_copy_blocks", "kv_swap_out",
     "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
-    "paged_append_and_decode",
+    "paged_append_and_decode", "kv_decode_order",
     "paged_decode_attention_noalloc", "kv_cascade_plan", "kv_cascade_workspace_size",
     "paged_decode_attention_cascade", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
@@ -92,8 +92,9 @@ _SIGS = {
     "kv_decode_plan": [_vp, _i32, _i32, _i32, _P(_i32)],
     "paged_decode_attention": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32,
                                _vp, _sz, _vp],
-    "paged_append_and_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
-                                _i32, _vp, _i32, _vp, _sz, _vp],
+    "paged_append_and_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _f32,
+                                _vp, _i32, _vp, _i32, _vp, _sz, _vp],
+    "kv_decode_order": [_vp, _i32, _vp],
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _vp, _i32, _vp],
     "kv_cascade_plan": [_i32, _i32, _i32, _i32, _P(_i32)],
@@ -402,14 +403,22 @@ def paged_decode_attention(p: int, q, block_tables, max_blocks: int, seq_lens, b
            "paged_decode_attention")
 
 
+def kv_decode_order(host_seq_lens, order_out):
+    """host_seq_lens, order_out: int32 numpy arrays of the batch size (host)."""
+    _check(lib().kv_decode_order(_ptr(host_seq_lens), len(host_seq_lens), _ptr(order_out)),
+           "kv_decode_order")
+
+
 def paged_append_and_decode(p: int, q, k_new, v_new, slot_mapping, block_tables, max_blocks: int,
                             seq_lens, batch: int, num_q_heads: int, scale: float, out,
                             out_dtype: int, lse_out=None, num_splits: int = 0, workspace=None,
-                            workspace_bytes: int = 0, stream=None):
+                            workspace_bytes: int = 0, stream=None, seq_order=None):
     """kv_append of one token per sequence, then paged_decode_attention (one
-    fused launch where supported); see the C header."""
+    fused launch where supported); seq_order: device int32 permutation of the
+    batch or None.  See the C header."""
     _check(lib().paged_append_and_decode(p, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
-                                         _ptr(block_tables), max_blocks, _ptr(seq_lens), batch,
+                                         _ptr(block_tables), max_blocks, _ptr(seq_lens),
+                                         _ptr(seq_order), batch,
                                          num_q_heads, scale, _ptr(out), out_dtype, _ptr(lse_out),
                                          num_splits, _ptr(workspace), workspace_bytes,
                                          _stream(stream)), "paged_append_and_decode")

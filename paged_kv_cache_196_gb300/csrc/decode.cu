@@ -101,6 +101,9 @@ struct DecodeKParams {
     const uint4 *new_k;
     const uint4 *new_v;
     const int64_t *new_slots;
+    // order in which the grid takes the sequences (a permutation of the
+    // batch, e.g. longest first so a single wave loads the SMs evenly), or null
+    const int32_t *seq_order;
     void *out;
     int out_bf16;
     float *lse;
@@ -301,7 +304,12 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     constexpr int kPasses = 8 * HS;            // passes over a 16-token block
     static_assert(GH >= 1 && (HS == 1 || HS == 2), "bad head split");
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
+    if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
+        if (threadIdx.x == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- the slice of keys this CTA owns
@@ -725,7 +733,12 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
     constexpr int G = 8, D = 128;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
+    if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
+        if (threadIdx.x == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     long long L = p.seq_lens[b];
@@ -1092,6 +1105,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.new_k = static_cast<const uint4 *>(a.new_k);
     kp.new_v = static_cast<const uint4 *>(a.new_v);
     kp.new_slots = a.new_slots;
+    kp.seq_order = a.seq_order;
     kp.out = a.out;
     kp.out_bf16 = a.out_dtype == KV_BF16;
     kp.lse = a.lse;
@@ -1161,6 +1175,16 @@ kv_status kv_decode_split_plan(int batch, int num_kv_heads, int max_blocks, int 
     if (!part_blocks || !max_splits || batch < 0 || num_kv_heads <= 0 || max_blocks < 0)
         return KV_ERR_ARG;
     split_plan(batch, num_kv_heads, max_blocks, num_splits, part_blocks, max_splits);
+    return KV_OK;
+}
+
+kv_status kv_decode_order(const int32_t *host_seq_lens, int batch, int32_t *order_out) {
+    if (batch < 0 || (batch > 0 && (!host_seq_lens || !order_out))) return KV_ERR_ARG;
+    std::vector<int32_t> idx(batch);
+    for (int b = 0; b < batch; ++b) idx[b] = b;
+    std::stable_sort(idx.begin(), idx.end(),
+                     [&](int32_t x, int32_t y) { return host_seq_lens[x] > host_seq_lens[y]; });
+    for (int b = 0; b < batch; ++b) order_out[b] = idx[b];
     return KV_OK;
 }
 
@@ -1279,7 +1303,8 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
 kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
                                   const void *v_new, const int64_t *slot_mapping,
                                   const int32_t *block_tables, int max_blocks,
-                                  const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                                  const int32_t *seq_lens, const int32_t *seq_order, int batch,
+                                  int num_q_heads, float scale,
                                   void *out, kv_dtype out_dtype, float *lse_out, int num_splits,
                                   void *workspace, size_t workspace_bytes, void *stream) {
     if (!p || batch < 0 || max_blocks < 0 || (batch > 0 && max_blocks > 0 && !block_tables))
@@ -1318,6 +1343,7 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
     a.new_k = k_new;
     a.new_v = v_new;
     a.new_slots = slot_mapping;
+    a.seq_order = seq_order;
     const kv_status st = launch_decode(a, false);
     if (st != KV_ERR_UNSUPPORTED) return st;
     // shapes the fused kernel does not cover: the append, then the decode

@@ -99,6 +99,7 @@ struct DecodeArgs {
     const void *new_k;
     const void *new_v;
     const int64_t *new_slots;
+    const int32_t *seq_order;  // device permutation of the batch: grid order, or null
     int *counters;
     long long counter_slots;
     void *workspace;

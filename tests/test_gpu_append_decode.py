@@ -40,7 +40,7 @@ def _setup(lens_after, hq, hkv, d, dtype, seed):
     return lens, tables, pool_k, pool_v, slots, k_new, v_new, q
 
 
-def _run(fused, lens, tables, pool_k, pool_v, slots, k_new, v_new, q, splits):
+def _run(fused, lens, tables, pool_k, pool_v, slots, k_new, v_new, q, splits, order=None):
     bf = pool_k.dtype == np.uint16
     nb, hkv, _, d = pool_k.shape
     B, hq, _ = q.shape
@@ -56,7 +56,8 @@ def _run(fused, lens, tables, pool_k, pool_v, slots, k_new, v_new, q, splits):
     args = (dev(tables), maxb, dev(lens), B, hq, 1.0 / math.sqrt(d), out, pk.KV_F32, lse, splits,
             ws, wsb)
     if fused:
-        pk.paged_append_and_decode(pool, dev(q), dev(k_new), dev(v_new), dev(slots), *args)
+        pk.paged_append_and_decode(pool, dev(q), dev(k_new), dev(v_new), dev(slots), *args,
+                                   seq_order=None if order is None else dev(order))
     else:
         pk.kv_append(pool, dev(k_new), dev(v_new), dev(slots), B)
         pk.paged_decode_attention(pool, dev(q), *args)
@@ -89,3 +90,19 @@ def test_fused_step_equals_append_then_decode(shape):
     oracle.append(pk_, pv_, k_new, v_new, slots)
     ref, ref_lse = oracle.paged_decode(pk_, pv_, tables, lens_, q, 1.0 / math.sqrt(d))
     assert_close_scaled(b[0], ref, 2e-3 if dtype == "bf16" else 1e-5, "fused step")
+
+
+def test_sequence_order_changes_no_result():
+    """The grid may take the sequences in any order (kv_decode_order: longest
+    first); output, lse and pool bytes stay bit-identical."""
+    require_cuda()
+    lens = [700, 33, 2000, 1, 1500, 16, 900, 260]
+    case = _setup(lens, 32, 8, 128, "bf16", seed=5)
+    order = np.zeros(len(lens), np.int32)
+    pk.kv_decode_order(np.asarray(lens, np.int32), order)
+    assert order.tolist() == [2, 4, 6, 0, 7, 1, 5, 3]
+    for splits in (0, 3):
+        a = _run(True, *case, splits=splits)
+        b = _run(True, *case, splits=splits, order=order)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x.view(np.uint32) if x.dtype == np.float32 else x, y.view(np.uint32) if y.dtype == np.float32 else y)
