@@ -751,6 +751,10 @@ def run_shared_prefix(args, rank, world, local_rank):
     wsc = torch.empty(max(wsc_bytes // 4, 1), dtype=torch.float32, device="cuda")
     d_groups = torch.from_numpy(group_seqs).cuda()
     d_shared = torch.from_numpy(shared).cuda()
+    # the suffix grid takes the sequences with the longest own part first
+    s_order = np.zeros(B, np.int32)
+    pk.kv_decode_order(suffix_lens, s_order)
+    d_sorder = torch.from_numpy(s_order).cuda()
 
     def decode_plain():
         pk.paged_decode_attention(pool, q, d_tables, max_blocks, d_lens, B, hq, scale, out,
@@ -759,7 +763,8 @@ def run_shared_prefix(args, rank, world, local_rank):
     def decode_cascade():
         pk.paged_decode_attention_cascade(pool, q, d_tables, max_blocks, d_lens, B, hq, scale,
                                           d_groups, groups, G, d_shared, prefix_blocks, psplits,
-                                          out, pk.KV_BF16, None, csplits, wsc, wsc_bytes)
+                                          out, pk.KV_BF16, None, csplits, wsc, wsc_bytes,
+                                          seq_order=d_sorder)
 
     def step(ev=None, decode=decode_cascade):
         if n_cow:

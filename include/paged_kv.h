@@ -390,7 +390,10 @@ kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32
  *                  key-range partitions of each group's prefix;
  *   num_splits, workspace: as paged_decode_attention, for the suffix (the
  *                  blocks after each sequence's shared part); the workspace
- *                  must hold kv_cascade_workspace_size bytes.
+ *                  must hold kv_cascade_workspace_size bytes;
+ *   seq_order      device int32[batch] or NULL: the order in which the suffix
+ *                  grid takes the sequences (as paged_append_and_decode; e.g.
+ *                  kv_decode_order of the suffix lengths).
  * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16,
  * head_dim 128 and group_size * (num_q_heads / num_kv_heads) <= 128, else
  * KV_ERR_UNSUPPORTED.  Two kernels run in stream order: the prefix kernel
@@ -406,8 +409,8 @@ kv_status paged_decode_attention_cascade(
     kv_pool_t p, const void *q, const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
     int batch, int num_q_heads, float scale, const int32_t *group_seqs, int num_groups,
     int group_size, const int32_t *shared_tokens, int max_prefix_blocks, int prefix_splits,
-    void *out, kv_dtype out_dtype, float *lse_out, int num_splits, void *workspace,
-    size_t workspace_bytes, void *stream);
+    void *out, kv_dtype out_dtype, float *lse_out, int num_splits, const int32_t *seq_order,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /* Chunked causal paged prefill ("Makale Bulteni -- vAttention", "Iddia ve
  * Gerceklik": the prefill kernels are where paging costs most).  Sequence b

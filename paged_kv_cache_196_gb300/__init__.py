@@ -100,8 +100,8 @@ _SIGS = {
     "kv_cascade_plan": [_i32, _i32, _i32, _i32, _P(_i32)],
     "kv_cascade_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
     "paged_decode_attention_cascade": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
-                                       _i32, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _sz,
-                                       _vp],
+                                       _i32, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _vp,
+                                       _sz, _vp],
     "paged_prefill_attention": [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
                                 _i32, _vp, _vp],
     "kv_get_device_error": [_vp, _P(_i32), _vp],
@@ -459,13 +459,13 @@ def paged_decode_attention_cascade(p: int, q, block_tables, max_blocks: int, seq
                                    group_size: int, shared_tokens, max_prefix_blocks: int,
                                    prefix_splits: int, out, out_dtype: int, lse_out=None,
                                    num_splits: int = 0, workspace=None, workspace_bytes: int = 0,
-                                   stream=None):
+                                   stream=None, seq_order=None):
     """Decode with each group's shared prefix blocks read once; see the C header."""
     _check(lib().paged_decode_attention_cascade(
         p, _ptr(q), _ptr(block_tables), max_blocks, _ptr(seq_lens), batch, num_q_heads, scale,
         _ptr(group_seqs), num_groups, group_size, _ptr(shared_tokens), max_prefix_blocks,
-        prefix_splits, _ptr(out), out_dtype, _ptr(lse_out), num_splits, _ptr(workspace),
-        workspace_bytes, _stream(stream)), "paged_decode_attention_cascade")
+        prefix_splits, _ptr(out), out_dtype, _ptr(lse_out), num_splits, _ptr(seq_order),
+        _ptr(workspace), workspace_bytes, _stream(stream)), "paged_decode_attention_cascade")
 
 
 def paged_prefill_attention(p: int, q, cu_q, total_q: int, max_q_len: int, block_tables,

@@ -518,8 +518,8 @@ kv_status paged_decode_attention_cascade(
     kv_pool_t p, const void *q, const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
     int batch, int num_q_heads, float scale, const int32_t *group_seqs, int num_groups,
     int group_size, const int32_t *shared_tokens, int max_prefix_blocks, int prefix_splits,
-    void *out, kv_dtype out_dtype, float *lse_out, int num_splits, void *workspace,
-    size_t workspace_bytes, void *stream) {
+    void *out, kv_dtype out_dtype, float *lse_out, int num_splits, const int32_t *seq_order,
+    void *workspace, size_t workspace_bytes, void *stream) {
     if (!p || batch < 0 || max_blocks < 0 || num_q_heads <= 0 || num_groups < 0 || group_size < 0 ||
         max_prefix_blocks < 0 || prefix_splits < 0 || num_splits < 0)
         return KV_ERR_ARG;
@@ -560,6 +560,7 @@ kv_status paged_decode_attention_cascade(
     a.num_splits = num_splits;
     a.start_tokens = shared_tokens;
     a.part_base = ps;
+    a.seq_order = seq_order;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;

@@ -114,10 +114,15 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: 
         wc = torch.empty(max(wsc // 4, 1), dtype=torch.float32, device="cuda")
         oc = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
         lc = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+        order = None
+        if prefix_splits == 3:  # also the suffix grid in longest-first order
+            order = np.zeros(B, np.int32)
+            pk.kv_decode_order((new_lens - shared).astype(np.int32), order)
+            order = dev(order)
         pk.paged_decode_attention_cascade(pool, dev(inp["q"]), dev(tables), max_blocks,
                                           dev(new_lens), B, hq, 1 / math.sqrt(d), dev(group_seqs),
                                           groups, G, dev(shared), P // BS, ps, oc, pk.KV_F32, lc, 0,
-                                          wc, wsc)
+                                          wc, wsc, seq_order=order)
         torch.cuda.synchronize()
         assert pk.kv_get_device_error(pool) == 0
         out_c, lse_c = host(oc).astype(np.float64), host(lc).astype(np.float64)
