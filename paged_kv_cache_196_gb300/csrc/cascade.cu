@@ -44,6 +44,10 @@
 #include "internal.h"
 #include "tc.cuh"
 
+#ifndef PKV_TMA_MULTILANE
+#define PKV_TMA_MULTILANE 1  // the boxes of a K/V tile are issued by eight lanes
+#endif
+
 namespace pkv {
 namespace {
 
@@ -58,7 +62,7 @@ constexpr int kCsQOff = 0;
 constexpr int kCsKOff = kCsTileBytes;                   // 2 stages
 constexpr int kCsVOff = kCsKOff + 2 * kCsTileBytes;     // 2 stages
 constexpr int kCsBarOff = kCsVOff + 2 * kCsTileBytes;   // 160 KiB
-constexpr int kCsSmemBytes = kCsBarOff + 256 + 1024;    // barriers, alignment slack
+constexpr int kCsSmemBytes = kCsBarOff + 2048 + 1024;   // barriers and exchange, alignment slack
 constexpr float kCsRescaleThreshold = 8.0f;             // log2 units
 constexpr uint32_t kColO = 256;
 
@@ -66,6 +70,21 @@ KV_DEVICE float cs_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Named barrier that also returns the OR of a flag over the participating
+// threads, so that they all take the same decision.
+KV_DEVICE bool cs_bar_or(int id, int threads, bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
 }
 
 KV_DEVICE float cs_max3(float a, float b, float c) {
@@ -105,7 +124,12 @@ struct CsBars {
     int abort;
     int n_pre;   // prefix tokens of the group (longest member)
     int leader;  // sequence whose table lists the prefix blocks
+    // duplicated rows (groups of at most 64 rows): the two threads of a row
+    // exchange half-row maxima (by tile parity) and, at the end, row sums
+    float xmax[2][64][2];
+    float xsum[64][2];
 };
+static_assert(sizeof(CsBars) <= 2048, "barrier block too large");
 
 // Tokens of sequence b attended by the prefix kernel: shared_tokens[b]
 // clamped to [0, min(L, max_blocks * 16)], rounded down to whole blocks.
@@ -121,6 +145,14 @@ KV_DEVICE int prefix_limit(const CascadeParams &p, int b) {
     return (int)(st / 16) * 16;
 }
 
+// DUP: the group has at most 64 query rows.  Q rows 64..127 repeat rows
+// 0..63, so the tensor core produces every score row twice, in TMEM lanes r
+// and r + 64, at no extra cost; thread r then takes keys 0..63 of the row and
+// thread r + 64 keys 64..127 (the two warps sit on different SM sub-partitions,
+// which a TMEM lane quadrant would not allow otherwise).  Each writes its P
+// into its own key half of the row and zeros into the other half, so the one
+// PV product yields two partial O rows, added in the epilogue.
+template <bool DUP>
 __global__ void __launch_bounds__(kCsThreads, 1)
     cascade_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const CascadeParams p) {
@@ -168,17 +200,19 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);  // prefix longer than the planned splits
 
     // ---- this thread's query row (softmax warps): member slot s, head i
-    const int r = tid;  // valid for tid < 128
+    const int r = tid;               // TMEM lane, valid for tid < 128
+    const int qr = DUP ? r & 63 : r;  // query row of the group
+    const int half = DUP ? r >> 6 : 0;  // DUP: which 64 keys of each tile
     int member = -1, lim = 0;
-    if (tid < kCsRows && r < p.group_size * p.g) {
-        member = p.group_seqs[(size_t)grp * p.group_size + r / p.g];
+    if (tid < kCsRows && qr < p.group_size * p.g) {
+        member = p.group_seqs[(size_t)grp * p.group_size + qr / p.g];
         if (member >= p.batch) member = -1;
         lim = prefix_limit(p, member);
     }
-    const size_t orow = member >= 0 ? (size_t)member * p.num_q_heads + h * p.g + r % p.g : 0;
+    const size_t orow = member >= 0 ? (size_t)member * p.num_q_heads + h * p.g + qr % p.g : 0;
 
     if (n == 0) {  // no keys of the prefix here: empty partial results
-        if (tid < kCsRows && member >= 0 && lim > 0) {
+        if (tid < kCsRows && half == 0 && member >= 0 && lim > 0) {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_splits + ps) * kCsD);
             for (int k = 0; k < kCsD / 4; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             p.ws_lse[orow * p.max_splits + ps] = -INFINITY;
@@ -244,16 +278,26 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             if (lane == 0)
                 stop = *abort_flag || (t >= 2 && !mbar_wait(&empty[s], ((t - 2) >> 1) & 1, p.err));
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
-            int ys[8];
+            char *dst = ring + s * kCsTileBytes;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], kCsTileBytes);
+            __syncwarp();
+            if (PKV_TMA_MULTILANE) {
+                // lane b < 8 issues the two boxes of block b (its own table entry):
+                // one thread issuing all 16 boxes of a tile is the slower path
+                if (lane < 8) {
+                    tc::tma_load_2d(dst + lane * 2048, map, 0, y_cur, &full[s]);
+                    tc::tma_load_2d(dst + kCsHalfBytes + lane * 2048, map, 64, y_cur, &full[s]);
+                }
+            } else {
+                int ys[8];
 #pragma unroll
-            for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
-            if (lane == 0) {
-                char *dst = ring + s * kCsTileBytes;
-                mbar_arrive_expect_tx(&full[s], kCsTileBytes);
+                for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
+                if (lane == 0) {
 #pragma unroll
-                for (int bi = 0; bi < 8; ++bi) {
-                    tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
-                    tc::tma_load_2d(dst + kCsHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
+                    for (int bi = 0; bi < 8; ++bi) {
+                        tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
+                        tc::tma_load_2d(dst + kCsHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
+                    }
                 }
             }
             issued = t + 1;
@@ -347,6 +391,157 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             tc::fence_proxy_async_smem();
             mbar_arrive(&bars->qfull);
         }
+        if constexpr (DUP) {
+            // pair barrier of the two warps holding the same rows (warps w, w + 2)
+            const int pair_bar = 1 + (warp & 1);
+            float m_used = -INFINITY, l_sum = 0.f;
+            bool ok = true, bad_next = false;
+            const uint32_t zero16[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+            for (int j = 0; j < n; ++j) {
+                const int sb = j & 1;
+                bool bad = bad_next || *abort_flag != 0;
+                if (!bad) bad = !mbar_wait(&bars->sfull[sb], (j >> 1) & 1, p.err);
+                tc::fence_after_sync();
+                const uint32_t scol = tmem + lane_base + sb * 128;
+                uint32_t sv[2][32];
+                float mhalf = -INFINITY;
+                const int klim = max(0, min(64, lim - (t0 + j) * kCsBN - 64 * half));  // keys kept in my half
+                if (!bad) {
+                    tc::tmem_ld32(scol + 64 * half, sv[0]);
+                    tc::tmem_ld32(scol + 64 * half + 32, sv[1]);
+                    tc::tmem_wait_ld();
+                    if (__any_sync(0xffffffffu, klim < 64)) {
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (32 * i + k >= klim) sv[i][k] = __float_as_uint(-INFINITY);
+                    }
+                    float mx[4];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t *v = &sv[c4 >> 1][16 * (c4 & 1)];
+                        float m = cs_max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+                        for (int k = 3; k < 15; k += 2)
+                            m = cs_max3(m, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+                        mx[c4] = fmaxf(m, __uint_as_float(v[15]));
+                    }
+                    mhalf = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                }
+                bars->xmax[j & 1][qr][half] = mhalf;
+                // both halves decide together whether to go on (the barrier has no timeout)
+                if (cs_bar_or(pair_bar, 64, bad)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                const float mrow = fmaxf(bars->xmax[j & 1][qr][0], bars->xmax[j & 1][qr][1]) *
+                                   p.scale_log2;  // scale > 0
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_used == -INFINITY) {
+                    m_used = mrow;
+                } else if (mrow > m_used + kCsRescaleThreshold) {
+                    alpha = cs_ex2(m_used - mrow);
+                    m_used = mrow;
+                    l_sum *= alpha;
+                    rescale = true;
+                }
+                const float mref = m_used == -INFINITY ? 0.f : m_used;
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm2 = make_float2(-mref, -mref);
+                float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    uint32_t whi[16], wlo[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[i][2 * k]),
+                                                                 __uint_as_float(sv[i][2 * k + 1])),
+                                                     sc2, nm2);
+                        const float2 e = make_float2(cs_ex2(xx.x), cs_ex2(xx.y));
+                        acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
+                        whi[k] = tc::pack_bf16x2(e.x, e.y);
+                        const float hx = __uint_as_float(whi[k] << 16), hy = __uint_as_float(whi[k] & 0xffff0000u);
+                        wlo[k] = tc::pack_bf16x2(e.x - hx, e.y - hy);
+                    }
+                    // my keys: P columns 32*half + 16i (hi) and 64 + 32*half + 16i (lo)
+                    tc::tmem_st16(scol + 32 * half + 16 * i, whi);
+                    tc::tmem_st16(scol + 64 + 32 * half + 16 * i, wlo);
+                    // the other half's keys are not in this lane's row
+                    tc::tmem_st16(scol + 32 * (1 - half) + 16 * i, zero16);
+                    tc::tmem_st16(scol + 64 + 32 * (1 - half) + 16 * i, zero16);
+                }
+                l_sum += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y) + (acc2[2].x + acc2[2].y) +
+                         (acc2[3].x + acc2[3].y);
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // this lane's partial O holds PV(j-1) once that completes
+                    if (__any_sync(0xffffffffu, !mbar_wait(&bars->odone, (j - 1) & 1, p.err))) {
+                        bad_next = true;  // leave together at the next exchange
+                    } else {
+                        tc::fence_after_sync();
+#pragma unroll 1
+                        for (int i = 0; i < 8; ++i) {
+                            uint32_t v[16];
+                            const uint32_t oc = tmem + lane_base + kColO + 16 * i;
+                            tc::tmem_ld16(oc, v);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+                            tc::tmem_st16(oc, v);
+                        }
+                    }
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->pfull[sb]);  // one arrival per warp
+            }
+            // ---- epilogue: the two partial O rows of a query row are added
+            // (lane r + 64's through shared memory: the K ring is idle once
+            // every MMA has completed)
+            if (ok) ok = mbar_wait(&bars->done, 0, p.err);
+            tc::fence_after_sync();
+            float *xo = reinterpret_cast<float *>(sK);  // [64][128]
+            bars->xsum[qr][half] = l_sum;
+            if (half == 1) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + lane_base + kColO + 16 * i, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) xo[qr * kCsD + 16 * i + k] = __uint_as_float(v[k]);
+                }
+            }
+            const bool okay = !cs_bar_or(pair_bar, 64, !ok);
+            if (!okay) *abort_flag = 1;
+            if (half == 0) {
+                const float lrow = bars->xsum[qr][0] + bars->xsum[qr][1];
+                const bool write = okay && member >= 0 && lim > 0;
+                const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_splits + ps) * kCsD);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + lane_base + kColO + 16 * i, v);
+                    tc::tmem_wait_ld();
+                    if (write) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float *o2 = xo + qr * kCsD + 16 * i + 4 * k;
+                            dst[4 * i + k] = make_float4((__uint_as_float(v[4 * k]) + o2[0]) * inv,
+                                                         (__uint_as_float(v[4 * k + 1]) + o2[1]) * inv,
+                                                         (__uint_as_float(v[4 * k + 2]) + o2[2]) * inv,
+                                                         (__uint_as_float(v[4 * k + 3]) + o2[3]) * inv);
+                        }
+                    }
+                }
+                if (write) p.ws_lse[orow * p.max_splits + ps] = lrow > 0.f ? m_used + log2f(lrow) : -INFINITY;
+            }
+        } else {
         const bool warp_idle = __all_sync(0xffffffffu, lim == 0);  // padding rows only
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
@@ -468,6 +663,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         }
         if (write) p.ws_lse[orow * p.max_splits + ps] = l_sum > 0.f ? m_used + log2f(l_sum) : -INFINITY;
     }
+        }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kCsMmaWarp) {
@@ -597,11 +793,13 @@ kv_status paged_decode_attention_cascade(
         cp.max_splits = ps + ms;
         cp.ws_lse = cp.ws_o + (size_t)batch * num_q_heads * cp.max_splits * kCsD;
         cp.err = p->err;
-        if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
-                cascade_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsSmemBytes)))
+        // groups of at most 64 rows: duplicated rows, keys split over two threads
+        auto fn = (long long)group_size * g <= 64 ? cascade_prefix_kernel<true> : cascade_prefix_kernel<false>;
+        if (kv_status st0 = cuda_status(
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsSmemBytes)))
             return st0;
         const dim3 grid(ps, p->num_kv_heads, num_groups);
-        cascade_prefix_kernel<<<grid, kCsThreads, kCsSmemBytes, s>>>(p->tmap_k, p->tmap_v, cp);
+        fn<<<grid, kCsThreads, kCsSmemBytes, s>>>(p->tmap_k, p->tmap_v, cp);
         if (kv_status st1 = cuda_status(cudaGetLastError())) return st1;
     }
     return launch_decode(a, false);

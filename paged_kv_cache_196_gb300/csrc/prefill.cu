@@ -45,6 +45,10 @@
 #include "internal.h"
 #include "tc.cuh"
 
+#ifndef PKV_TMA_MULTILANE
+#define PKV_TMA_MULTILANE 1  // the boxes of a K/V tile are issued by eight lanes
+#endif
+
 namespace pkv {
 
 constexpr int kPfBM = 256;           // queries per CTA (two tensor-core tiles)
@@ -205,16 +209,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (lane == 0)
                 stop = *abort_flag || (t >= 2 && !mbar_wait(&empty[s], ((t - 2) >> 1) & 1, p.err));
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
-            int ys[8];
+            char *dst = ring + s * kPfTileBytes;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], kPfTileBytes);
+            __syncwarp();
+            if (PKV_TMA_MULTILANE) {
+                // lane b < 8 issues the two boxes of block b (its own table entry):
+                // one thread issuing all 16 boxes of a tile is the slower path
+                if (lane < 8) {
+                    tc::tma_load_2d(dst + lane * 2048, map, 0, y_cur, &full[s]);
+                    tc::tma_load_2d(dst + kPfHalfBytes + lane * 2048, map, 64, y_cur, &full[s]);
+                }
+            } else {
+                int ys[8];
 #pragma unroll
-            for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
-            if (lane == 0) {
-                char *dst = ring + s * kPfTileBytes;
-                mbar_arrive_expect_tx(&full[s], kPfTileBytes);
+                for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
+                if (lane == 0) {
 #pragma unroll
-                for (int bi = 0; bi < 8; ++bi) {
-                    tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
-                    tc::tma_load_2d(dst + kPfHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
+                    for (int bi = 0; bi < 8; ++bi) {
+                        tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
+                        tc::tma_load_2d(dst + kPfHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
+                    }
                 }
             }
             issued = t + 1;

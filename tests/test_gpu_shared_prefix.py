@@ -207,3 +207,18 @@ def test_shared_prefix_step_full_size():
     require_cuda()
     inp = W.shared_prefix_inputs()
     _check(inp, max_blocks=(2048 + 1 + 15) // 16)
+
+
+def test_cascade_groups_of_128_rows():
+    """16 sequences x 8 query heads per kv head fill all 128 rows of the
+    prefix kernel (groups of at most 64 rows take the duplicated-row path)."""
+    require_cuda()
+    inp = W.shared_prefix_inputs(batch=20, seed_offset=2)
+    B, d = len(inp["lens"]), inp["q"].shape[2]
+    inp["q"] = W.normal(W.rng(4242), (B, 64, d), "bf16")  # 64 q heads over 8 kv heads
+    out_s, lse_s, _, _, _, out_c, lse_c = build_and_step(inp, True, (2048 + 1 + 15) // 16, seed=93,
+                                                         prefix_splits=2)
+    ref, ref_lse = oracle_step(inp)
+    assert_close_scaled(out_s, ref, 2e-3, "plain decode, 8 heads per kv head")
+    assert_close_scaled(out_c, ref, 2e-3, "cascade decode, 128-row groups")
+    np.testing.assert_allclose(lse_c, ref_lse, atol=1e-3)
