@@ -15,7 +15,7 @@ Metric: KV bytes read by decode attention per second (valid tokens only:
 sum_b L_b * 2 * Hkv * D * 2 bytes) -- "value" -- plus decode tokens/s.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--splits S] [--impl reference]
+       [--splits S] [--plan grid|balanced] [--prefix-splits P] [--impl reference]
 Under torchrun each rank runs an independent replica (weak scaling).
 Prints exactly one JSON line on stdout (rank 0).
 """
@@ -257,12 +257,20 @@ def run_ours(args, rank, world, local_rank):
     ws_bytes = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, splits)
     ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
     part_blocks, max_splits = pk.kv_decode_split_plan(B, hkv, max_blocks, splits)
+    balanced = not contig and args.plan == "balanced"
     if not contig:
         d_slots = torch.from_numpy(slots).cuda()
         # the grid takes the sequences longest first (one wave loads the SMs evenly)
         h_order = np.zeros(B, np.int32)
         pk.kv_decode_order(lens.astype(np.int32), h_order)
         d_order = torch.from_numpy(h_order).cuda()
+        if balanced:
+            # or: one wave of CTAs with equal runs of blocks (host-made schedule)
+            h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks)
+            d_sched = torch.from_numpy(h_sched).cuda()
+            ws_bytes = pk.kv_decode_schedule_workspace_size(h_sched, hq, d)
+            ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
+            max_splits = int(h_sched[2])
     else:
         d_pos = torch.from_numpy(last.astype(np.int32)).cuda()
 
@@ -277,6 +285,11 @@ def run_ours(args, rank, world, local_rank):
         if contig:
             pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, pk.KV_BF16,
                                        None, splits, ws, ws_bytes)
+        elif balanced:
+            pk.paged_decode_attention_scheduled(pool, q, d_tables, max_blocks, d_lens, B, hq, scale,
+                                                h_sched, d_sched, out, pk.KV_BF16, None, ws,
+                                                ws_bytes, k_new=k_new, v_new=v_new,
+                                                slot_mapping=d_slots)
         else:
             pk.paged_append_and_decode(pool, q, k_new, v_new, d_slots, d_tables, max_blocks, d_lens,
                                        B, hq, scale, out, pk.KV_BF16, None, splits, ws, ws_bytes,
@@ -331,8 +344,8 @@ def run_ours(args, rank, world, local_rank):
     Ke = min(K, 2000)
     h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu(),
                torch.from_numpy(last.astype(np.int32) if contig else slots), torch.from_numpy(lens)]
-    if not contig:
-        h_parts.append(torch.from_numpy(h_order))  # recomputed on the host for every batch
+    if not contig:  # recomputed on the host for every batch
+        h_parts.append(torch.from_numpy(h_sched if balanced else h_order))
     offs, total = [], 0
     for t in h_parts:
         offs.append(total)
@@ -350,7 +363,9 @@ def run_ours(args, rank, world, local_rank):
     else:
         d_slots = views[3]
     d_lens = views[4]
-    if not contig:
+    if balanced:
+        d_sched = views[5]
+    elif not contig:
         d_order = views[5]
     h_out = torch.empty((B, hq, d), dtype=torch.int16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h_parts)
@@ -405,6 +420,8 @@ def run_ours(args, rank, world, local_rank):
             "num_splits": splits,
             "part_blocks": part_blocks,
             "max_splits": max_splits,
+            "plan": ("balanced schedule: %d CTAs of %d blocks" % (int(h_sched[0]), int(h_sched[3]))
+                     if balanced else "grid-indexed" + ("" if contig else ", longest first")),
             "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2); no flush",
             "parallelism": f"replicas x{world}",
@@ -744,7 +761,7 @@ def run_shared_prefix(args, rank, world, local_rank):
             k += 1
         shared[b] = k * 16
     prefix_blocks = P // 16
-    psplits = pk.kv_cascade_plan(groups, hkv, prefix_blocks, 0)
+    psplits = pk.kv_cascade_plan(groups, hkv, prefix_blocks, args.prefix_splits)
     suffix_lens = np.maximum(new_lens - (shared // 16) * 16, 1).astype(np.int32)
     csplits = args.splits if args.splits > 0 else pk.kv_decode_plan(suffix_lens, hkv, max_blocks)
     wsc_bytes = pk.kv_cascade_workspace_size(B, hq, hkv, d, max_blocks, csplits, psplits)
@@ -945,6 +962,11 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_decode", choices=sorted(DESCR))
     ap.add_argument("--splits", type=int, default=0,
                     help="0 = plan from the host-known lengths (kv_decode_plan)")
+    ap.add_argument("--plan", default="grid", choices=["grid", "balanced"],
+                    help="paged decode: grid-indexed split plan or balanced schedule")
+    ap.add_argument("--prefix-splits", type=int, default=0,
+                    help="shared-prefix step: key-range partitions of each group's prefix "
+                         "(0 = kv_cascade_plan)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

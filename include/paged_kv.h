@@ -345,6 +345,60 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
                                   void *out, kv_dtype out_dtype, float *lse_out, int num_splits,
                                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* Balanced work schedule for paged_decode_attention_scheduled (the pages fix
+ * no schedule: this is how this library spreads a decode step over the GPU).
+ * The grid-indexed plan gives every (sequence, kv head, split) its own CTA,
+ * so CTAs differ in length as the sequences do and a single wave ends with
+ * the longest.  Here the blocks of all (sequence, kv head) pairs are laid end
+ * to end and cut into C runs of equal length, one per CTA of a single wave
+ * (five CTAs per SM, or 2.4 per SM with the deep ring when every run has at
+ * least 256 blocks); a run that crosses pairs is several pieces, which the CTA
+ * streams one after the other.  A pair's pieces are its split-KV partitions
+ * (at most 32, merged inside the kernel).
+ *   host_seq_lens  host int32[batch]: the lengths the decode will see on the
+ *                  device (a decode step: after its append);
+ *   num_sms        SMs to plan for, 0 = the current device's;
+ *   schedule_out   host int32[capacity_ints]; *used_ints receives the words
+ *                  written (the caller copies that many to the device).
+ * Capacity: kv_decode_schedule_capacity's bound for this batch shape.  Host
+ * only.  KV_ERR_UNSUPPORTED when a sequence would need more than 32 pieces
+ * (more than 31 x 1024 blocks). */
+kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_blocks, int num_sms,
+                                      size_t *ints);
+kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
+                             int max_blocks, int num_sms, int32_t *schedule_out,
+                             size_t capacity_ints, size_t *used_ints);
+/* Workspace bytes paged_decode_attention_scheduled needs with this schedule
+ * (its host copy). */
+kv_status kv_decode_schedule_workspace_size(const int32_t *host_schedule, int num_q_heads,
+                                            int head_dim, size_t *bytes);
+
+/* Paged decode attention (and, with k_new non-NULL, the decode step's append
+ * of one token per sequence, as paged_append_and_decode) run on a balanced
+ * schedule from kv_decode_schedule.  Same maths as paged_decode_attention;
+ * the split points differ from the grid-indexed plan's, so results agree
+ * within rounding, not bit for bit (they are bit-identical from one call to
+ * the next with the same schedule).
+ *   host_schedule  the host array kv_decode_schedule filled (its header is
+ *                  read here);
+ *   schedule       its device copy, 16-byte aligned, all used words;
+ *   k_new, v_new, slot_mapping  as paged_append_and_decode, or k_new = NULL
+ *                  for no append.
+ * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16,
+ * head_dim 128, 3..8 query heads per kv head and batch * num_kv_heads <=
+ * 65536, else KV_ERR_UNSUPPORTED.  Device lengths that do not match the
+ * schedule's (a piece past a sequence's end, or a sequence's last piece
+ * stopping short of it) are recorded as KV_ERR_DEVICE_BOUNDS; nothing outside
+ * the sequence's table row and the pool is read. */
+kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const void *k_new,
+                                           const void *v_new, const int64_t *slot_mapping,
+                                           const int32_t *block_tables, int max_blocks,
+                                           const int32_t *seq_lens, int batch, int num_q_heads,
+                                           float scale, const int32_t *host_schedule,
+                                           const int32_t *schedule, void *out, kv_dtype out_dtype,
+                                           float *lse_out, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+
 /* paged_decode_attention without a workspace argument, for callers that
  * cannot allocate device memory where they run decode (a plugin whose host
  * framework owns all device memory; a serving loop that must not call

@@ -95,6 +95,11 @@ _SIGS = {
     "paged_append_and_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _f32,
                                 _vp, _i32, _vp, _i32, _vp, _sz, _vp],
     "kv_decode_order": [_vp, _i32, _vp],
+    "kv_decode_schedule_capacity": [_i32, _i32, _i32, _i32, _P(_sz)],
+    "kv_decode_schedule": [_vp, _i32, _i32, _i32, _i32, _vp, _sz, _P(_sz)],
+    "kv_decode_schedule_workspace_size": [_vp, _i32, _i32, _P(_sz)],
+    "paged_decode_attention_scheduled": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32,
+                                         _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _vp, _i32, _vp],
     "kv_cascade_plan": [_i32, _i32, _i32, _i32, _P(_i32)],
@@ -422,6 +427,55 @@ def paged_append_and_decode(p: int, q, k_new, v_new, slot_mapping, block_tables,
                                          num_q_heads, scale, _ptr(out), out_dtype, _ptr(lse_out),
                                          num_splits, _ptr(workspace), workspace_bytes,
                                          _stream(stream)), "paged_append_and_decode")
+
+
+def kv_decode_schedule_capacity(batch: int, num_kv_heads: int, max_blocks: int,
+                                num_sms: int = 0) -> int:
+    """int32 words a kv_decode_schedule of this batch shape may need."""
+    r = _sz()
+    _check(lib().kv_decode_schedule_capacity(batch, num_kv_heads, max_blocks, num_sms,
+                                             ctypes.byref(r)), "kv_decode_schedule_capacity")
+    return r.value
+
+
+def kv_decode_schedule(host_seq_lens, num_kv_heads: int, max_blocks: int, num_sms: int = 0):
+    """Balanced decode schedule for these host int32 lengths: an int32 numpy
+    array (header, first piece of each CTA, pieces) to copy to the device for
+    paged_decode_attention_scheduled.  num_sms = 0: the current device's."""
+    import numpy as _np
+    lens = _np.ascontiguousarray(host_seq_lens, dtype=_np.int32)
+    cap = kv_decode_schedule_capacity(len(lens), num_kv_heads, max_blocks, num_sms)
+    out = _np.zeros(cap, _np.int32)
+    used = _sz()
+    _check(lib().kv_decode_schedule(_ptr(lens), len(lens), num_kv_heads, max_blocks, num_sms,
+                                    _ptr(out), cap, ctypes.byref(used)), "kv_decode_schedule")
+    return out[:used.value].copy()
+
+
+def kv_decode_schedule_workspace_size(host_schedule, num_q_heads: int, head_dim: int) -> int:
+    r = _sz()
+    _check(lib().kv_decode_schedule_workspace_size(_ptr(host_schedule), num_q_heads, head_dim,
+                                                   ctypes.byref(r)),
+           "kv_decode_schedule_workspace_size")
+    return r.value
+
+
+def paged_decode_attention_scheduled(p: int, q, block_tables, max_blocks: int, seq_lens,
+                                     batch: int, num_q_heads: int, scale: float, host_schedule,
+                                     schedule, out, out_dtype: int, lse_out=None, workspace=None,
+                                     workspace_bytes: int = 0, stream=None, k_new=None, v_new=None,
+                                     slot_mapping=None):
+    """Decode (with the step's append when k_new is given) on a balanced
+    schedule: host_schedule is kv_decode_schedule's array, schedule its device
+    copy.  See the C header."""
+    _check(lib().paged_decode_attention_scheduled(p, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                                  _ptr(slot_mapping), _ptr(block_tables),
+                                                  max_blocks, _ptr(seq_lens), batch, num_q_heads,
+                                                  scale, _ptr(host_schedule), _ptr(schedule),
+                                                  _ptr(out), out_dtype, _ptr(lse_out),
+                                                  _ptr(workspace), workspace_bytes,
+                                                  _stream(stream)),
+           "paged_decode_attention_scheduled")
 
 
 def paged_decode_attention_noalloc(p: int, q, block_tables, max_blocks: int, seq_lens,

@@ -71,6 +71,15 @@ constexpr int kTcDeepBlocks = PKV_TC_DEEP_BLOCKS;
 // Splits per (sequence, kv head) merged inside the decode kernel by the last
 // CTA of that pair; longer plans leave the merge to merge_kernel.
 constexpr int kFuseMaxSplits = 32;
+// Balanced schedules (kv_decode_schedule), int32 words:
+//   [0] CTAs C, [1] pieces P, [2] most pieces of one (sequence, kv head),
+//   [3] most blocks of one CTA, [4] deep ring (1) or wide (0), [5] batch,
+//   [6] kv heads, [7] 0;
+//   [8, 8 + C] the first piece of each CTA, then P;
+//   from sched_piece_off(C) (a multiple of 4 words): P pieces of 4 words
+//   {b, h | split << 16, first block, blocks | pieces of the pair << 16}.
+constexpr int kSchedHeader = 8;
+inline size_t sched_piece_off(int ctas) { return ((size_t)kSchedHeader + ctas + 1 + 3) & ~size_t(3); }
 static_assert(kNStage % kNW == 0, "each stage must belong to one consumer warp");
 
 struct DecodeKParams {
@@ -104,6 +113,14 @@ struct DecodeKParams {
     // order in which the grid takes the sequences (a permutation of the
     // batch, e.g. longest first so a single wave loads the SMs evenly), or null
     const int32_t *seq_order;
+    // balanced schedule (tensor-core decode): CTA c runs pieces
+    // [sched_cta[c], sched_cta[c + 1]) of sched_pieces, each a run of blocks
+    // of one (sequence, kv head): {b, h | split << 16, first block,
+    // blocks | pieces of the pair << 16}; null for the grid-indexed plan
+    const int32_t *sched_cta;
+    const int4 *sched_pieces;
+    int sched_npieces;
+    int batch;
     void *out;
     int out_bf16;
     float *lse;
@@ -200,9 +217,14 @@ template <int G, int D>
 // Cascade: a sequence whose prefix was attended by the prefix kernel (pre > 0)
 // has pre more partial results in workspace slots [0, pre); this call's
 // partitions use slots part_base + split, and the merge takes both.
+//
+// w ([G][kFuseMaxSplits] floats) and flag hold the merge's weights and
+// decision.  With release set, the consumer warps meet the producer warp on
+// named barrier 2 as soon as sm_o / sm_m / sm_l have been read, so that the
+// producer may refill the ring they live in while the merge runs.
 KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const float *sm_m,
                                 const float *sm_l, int b, int h, int split, int nsplit, int pre,
-                                int tid) {
+                                int tid, float *w, int *flag, bool release) {
     const int ntot = pre + nsplit;
     constexpr float kLn2 = 0.6931471805599453f;
     for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
@@ -233,11 +255,10 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
             if (d == 0) p.ws_lse[row * p.max_splits + p.part_base + split] = lse2;
         }
     }
+    if (release) named_bar_sync(2, kDecodeThreads);
     if (ntot == 1 || !p.counters || ntot > kFuseMaxSplits) return;
 
     // ---- fused merge by the last-arriving CTA of this (sequence, kv head)
-    float *w = const_cast<float *>(sm_l) + kNW * G;  // [G][kFuseMaxSplits] weights, then a flag
-    int *flag = reinterpret_cast<int *>(w + G * kFuseMaxSplits);
     __threadfence();  // partial results visible device-wide before the arrival
     named_bar_sync(1, kNW * 32);
     if (tid == 0) {
@@ -576,7 +597,9 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel
     }
     named_bar_sync(1, kNW * 32);
 
-    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid);
+    float *mw = sm_l + kNW * G;  // merge weights, then a flag (still in the ring)
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid, mw,
+                           reinterpret_cast<int *>(mw + G * kFuseMaxSplits), false);
 }
 
 // ---------------------------------------------------------------------------
@@ -726,32 +749,58 @@ KV_DEVICE void tc_attend_block(const uint32_t (&qf)[8][2], uint32_t kt, uint32_t
 }
 
 
-// NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
-// compiled for MINB resident CTAs per SM.
-template <bool LINEAR, int NST, int MINB>
-__global__ void __launch_bounds__(kDecodeThreads, MINB)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
-                     const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
-    constexpr int G = 8, D = 128;
-    const int split = blockIdx.x, h = blockIdx.y;
-    const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
-    if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
-        if (threadIdx.x == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-        return;
-    }
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// One pass of the tensor-core decode's piece loop: blocks [blk0, blk0 + nloc)
+// of kv head h of sequence b, partial result `split` of the pair's nsplit
+// (after `pre` results of a cascade prefix).  run == 0: nothing to attend or
+// write (the same for every thread of the CTA).
+struct TcWork {
+    long long L;  // tokens of sequence b (clamped to what may be read)
+    int b, h, split, nsplit, blk0, nloc, nblk, pre;
+    int run;
+};
 
-    long long L = p.seq_lens[b];
-    const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
+// Resolves piece pc of a scheduled launch, or this CTA's grid position.  Only
+// the thread with report set records device errors.  LINEAR also selects the
+// request's K/V maps.
+template <bool LINEAR, bool SCHED>
+KV_DEVICE TcWork tc_work(const DecodeKParams &p, int pc, bool report, const CUtensorMap *&map_k,
+                         const CUtensorMap *&map_v) {
+    static_assert(!(LINEAR && SCHED), "schedules cover the paged path only");
+    TcWork w{};
+    if constexpr (SCHED) {
+        const int4 d = __ldg(p.sched_pieces + pc);
+        w.b = d.x;
+        w.h = d.y & 0xffff;
+        w.split = (int)((unsigned)d.y >> 16);
+        w.blk0 = d.z;
+        w.nloc = d.w & 0xffff;
+        w.nsplit = (int)((unsigned)d.w >> 16);
+        if (w.b < 0 || w.b >= p.batch || w.h >= p.num_kv_heads || w.nsplit < 1 ||
+            w.split >= w.nsplit || w.nsplit > p.max_splits || w.blk0 < 0 ||
+            w.nloc > p.part_blocks) {
+            if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+            return w;
+        }
+    } else {
+        w.split = blockIdx.x;
+        w.h = blockIdx.y;
+        w.b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
+        if (w.b < 0 || w.b >= (int)gridDim.z) {  // not a permutation of the batch
+            if (report && w.split == 0 && w.h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+            return w;
+        }
+    }
+    const bool first = report && w.split == 0 && w.h == 0;  // one report per sequence
+    long long L = p.seq_lens[w.b];
     if constexpr (LINEAR) {
-        const int req = p.req_ids[b];
+        const int req = p.req_ids[w.b];
         if (req < 0 || req >= p.max_requests || p.k_bases[req] == 0) {
-            if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+            if (first) atomicOr(p.err, KV_DEVERR_UNMAPPED);
             L = 0;
         } else {
             const long long mapped = p.mapped_tokens[req];
             if (L > mapped) {
-                if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+                if (first) atomicOr(p.err, KV_DEVERR_UNMAPPED);
                 L = mapped;
             }
             map_k = p.req_maps + 2 * req;
@@ -759,18 +808,58 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         }
     }
     if (L > (long long)p.max_blocks * kBS) {
-        if (tid == 0 && split == 0 && h == 0)
-            atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
+        if (first) atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
         L = (long long)p.max_blocks * kBS;
     }
     if (L < 0) L = 0;
-    const int nblk = (int)((L + kBS - 1) / kBS);
-    const int sblk = start_block(p, b, L);
-    const int pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
-    const int blk0 = sblk + split * p.part_blocks;
-    if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
-    const int nloc = max(0, min(p.part_blocks, nblk - blk0));
-    const int nsplit = max(1, (nblk - sblk + p.part_blocks - 1) / p.part_blocks);
+    w.nblk = (int)((L + kBS - 1) / kBS);
+    if constexpr (SCHED) {
+        // The schedule was made from host copies of the lengths: a piece past
+        // the end, or a last piece that stops short of it, means they differ.
+        const long long end = (long long)w.blk0 + w.nloc;
+        if (end > w.nblk || (w.split == w.nsplit - 1 && end != w.nblk)) {
+            if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+            w.nloc = (int)max(0LL, min((long long)w.nloc, (long long)w.nblk - w.blk0));
+        }
+    } else {
+        const int sblk = start_block(p, w.b, L);
+        w.pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
+        w.blk0 = sblk + w.split * p.part_blocks;
+        if (w.blk0 >= w.nblk && w.split > 0) return w;  // nothing for this split
+        w.nloc = max(0, min(p.part_blocks, w.nblk - w.blk0));
+        w.nsplit = max(1, (w.nblk - sblk + p.part_blocks - 1) / p.part_blocks);
+    }
+    w.L = L;
+    w.run = 1;
+    return w;
+}
+
+// NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
+// compiled for MINB resident CTAs per SM.
+//
+// Work: one partition named by the grid position, or, with a schedule, the
+// CTA's list of pieces.  The pieces of a list stream through the same ring one
+// after the other (ring position and barrier phases continue across them).
+// While the consumers finish a piece, the producer reads the next piece's
+// description and table slice; it refills the ring once the consumers have
+// read their merge scratch out of it (named barrier 2), so the split merge of
+// one piece overlaps the first copies of the next.
+template <bool LINEAR, bool SCHED, int NST, int MINB>
+__global__ void __launch_bounds__(kDecodeThreads, MINB)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
+                     const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
+    constexpr int G = 8, D = 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int pc0 = 0, pc1 = 1;
+    if constexpr (SCHED) {
+        pc0 = __ldg(p.sched_cta + blockIdx.x);
+        pc1 = __ldg(p.sched_cta + blockIdx.x + 1);
+        if (pc0 < 0 || pc1 < pc0 || pc1 > p.sched_npieces) {
+            if (tid == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+            return;
+        }
+        if (pc0 == pc1) return;
+    }
 
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -781,19 +870,29 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     uint64_t *empty = full + NST;
     int *stage_valid = reinterpret_cast<int *>(empty + NST);
     uint4 *newrow = reinterpret_cast<uint4 *>(stage_valid + NST);  // [32]: fused append's K, V rows
-    int32_t *tbl = reinterpret_cast<int32_t *>(newrow + 32);       // [part_blocks]
+    int32_t *tbl_buf = reinterpret_cast<int32_t *>(newrow + 32);   // [1 or 2][part_blocks]
+    __shared__ TcWork s_work[2];                      // this piece's and the next one's
+    __shared__ float s_mw[G * kFuseMaxSplits];        // split-merge weights
+    __shared__ int s_flag, s_abort;
 
+    // the producer's K/V maps: the pool's, or (LINEAR) the request's
+    const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
     if (warp == kNW) {
-        if constexpr (!LINEAR) {
-            const int32_t *row = p.tables + (size_t)b * p.max_blocks + blk0;
-            for (int i = lane; i < nloc; i += 32) tbl[i] = __ldg(row + i);
-        }
+        const TcWork w0 = tc_work<LINEAR, SCHED>(p, pc0, lane == 0, map_k, map_v);
         if (lane == 0) {
+            s_work[0] = w0;
+            s_abort = 0;
             for (int st = 0; st < NST; ++st) {
                 mbar_init(&full[st], 1);
                 mbar_init(&empty[st], 32);
             }
             mbar_init_fence();
+        }
+        if constexpr (!LINEAR) {
+            if (w0.run) {
+                const int32_t *row = p.tables + (size_t)w0.b * p.max_blocks + w0.blk0;
+                for (int i = lane; i < w0.nloc; i += 32) tbl_buf[i] = __ldg(row + i);
+            }
         }
     }
     __syncthreads();
@@ -804,146 +903,207 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
         }
         const uint64_t policy = l2_evict_first_policy();
-        int issued = 0;
-        for (int i = 0; i < nloc; ++i) {
-            const int st = i % NST, r = i / NST;
-            bool bad = false;
-            if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
-            if (__shfl_sync(0xffffffffu, bad, 0)) break;
-            int y;
-            bool valid = true;
-            if constexpr (LINEAR) {
-                y = (int)((long long)h * p.head_stride + (long long)(blk0 + i) * kBS);
-            } else {
-                const int id = tbl[i];
-                valid = id >= 0 && id < p.num_blocks;
-                y = ((valid ? id : 0) * p.num_kv_heads + h) * kBS;
-            }
-            char *dst = stages + st * 2 * kTcTile;
-            if (lane == 0) {
-                if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                stage_valid[st] = valid ? 1 : 0;
-                if (valid)
-                    mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
-                else
-                    mbar_arrive(&full[st]);
-            }
-            if (valid) {
-                if (PKV_TC_MULTILANE) {
-                    // lane x issues box x: K half 0, K half 1, V half 0, V half 1
-                    if (lane < 4)
-                        mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
-                                   lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
-                } else if (lane == 0) {
-                    mma::tma2d(dst, map_k, 0, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
+        int gi = 0;  // tiles issued so far: ring position across pieces
+        bool stop = false;
+        for (int pc = pc0; pc < pc1; ++pc) {
+            const int k = pc - pc0;
+            const TcWork w = s_work[k & 1];
+            const int32_t *tbl = tbl_buf + (k & 1) * p.part_blocks;
+            if (w.run && !stop) {
+                for (int i = 0; i < w.nloc; ++i) {
+                    const int st = gi % NST, r = gi / NST;
+                    bool bad = false;
+                    if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
+                    if (__shfl_sync(0xffffffffu, bad, 0)) {
+                        stop = true;
+                        break;
+                    }
+                    int y;
+                    bool valid = true;
+                    if constexpr (LINEAR) {
+                        y = (int)((long long)w.h * p.head_stride + (long long)(w.blk0 + i) * kBS);
+                    } else {
+                        const int id = tbl[i];
+                        valid = id >= 0 && id < p.num_blocks;
+                        y = ((valid ? id : 0) * p.num_kv_heads + w.h) * kBS;
+                    }
+                    char *dst = stages + st * 2 * kTcTile;
+                    if (lane == 0) {
+                        if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                        stage_valid[st] = valid ? 1 : 0;
+                        if (valid)
+                            mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
+                        else
+                            mbar_arrive(&full[st]);
+                    }
+                    if (valid) {
+                        if (PKV_TC_MULTILANE) {
+                            // lane x issues box x: K half 0, K half 1, V half 0, V half 1
+                            if (lane < 4)
+                                mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
+                                           lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st],
+                                           policy);
+                        } else if (lane == 0) {
+                            mma::tma2d(dst, map_k, 0, y, &full[st], policy);
+                            mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
+                            mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
+                            mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
+                        }
+                    }
+                    ++gi;
                 }
             }
-            issued = i + 1;
+            if (pc + 1 < pc1) {
+                // the next piece's description and table slice, read while the
+                // consumers finish this one
+                const CUtensorMap *mk = map_k, *mv = map_v;
+                const TcWork nx = tc_work<LINEAR, SCHED>(p, pc + 1, lane == 0, mk, mv);
+                if (lane == 0) {
+                    s_work[(k + 1) & 1] = nx;
+                    if (stop) s_abort = 1;
+                }
+                if constexpr (!LINEAR) {
+                    if (nx.run && !stop) {
+                        int32_t *t2 = tbl_buf + ((k + 1) & 1) * p.part_blocks;
+                        const int32_t *row = p.tables + (size_t)nx.b * p.max_blocks + nx.blk0;
+                        for (int i = lane; i < nx.nloc; i += 32) t2[i] = __ldg(row + i);
+                    }
+                }
+                named_bar_sync(2, kDecodeThreads);  // the consumers are out of the ring
+            }
         }
-        if (lane == 0)
-            for (int st = 0; st < NST && st < issued; ++st)
-                mbar_wait(&full[st], ((issued - 1 - st) / NST) & 1, p.err);
+        if (lane == 0)  // no copy may land after the CTA has exited
+            for (int st = 0; st < NST && st < gi; ++st)
+                mbar_wait(&full[st], ((gi - 1 - st) / NST) & 1, p.err);
         return;
     }
 
     // ---- consumer warps: lane = (g = lane / 4, t = lane % 4)
     const int g = lane >> 2, t = lane & 3;
-    // Fused append: the last split of (b, h) writes the new token's K/V row
-    // (head h) to its pool slot and, since the block holding it may have been
-    // copied before that write lands, patches the row into its own copy of
-    // the sequence's last block.  Lane x < 16 carries 16-byte chunk x of the
-    // K row, lane 16 + x chunk x of the V row.
-    const bool fuse = p.new_k != nullptr && split == nsplit - 1;
-    const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk;
-    if (fuse && warp == (patch ? (nloc - 1) % kNW : 0)) {
-        const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
-        const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
-        newrow[lane] = v;  // kept in shared memory until the last block arrives
-        const long long slot = p.new_slots[b];
-        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
-            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
-            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
-                         row * (D * 2 / 16) + (lane & 15);
-            *dst = v;
-        } else if (slot >= 0 && lane == 0) {
-            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
-        }
-    }
-    // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
-    uint32_t qf[8][2];
-    {
-        const bool live = g < p.g;
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-            reinterpret_cast<const uint16_t *>(p.q) + ((size_t)b * p.num_q_heads + h * p.g + (live ? g : 0)) * D);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
-            qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
-        }
-    }
-    // running state for heads 2t, 2t+1 (replicated over g)
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
     const uint32_t stage_base = smem_addr(stages);
-
-    for (int i = warp; i < nloc; i += kNW) {
-        const int st = i % NST, r = i / NST;
-        if (!mbar_wait(&full[st], r & 1, p.err)) break;
-        int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
-        if (!stage_valid[st]) ntok = 0;
-        const uint32_t kt = stage_base + st * 2 * kTcTile;
-        const uint32_t vt = kt + kTcTile;
-        if (patch && i == nloc - 1 && ntok > 0) {
-            // the new token is row (L - 1) % 16 of the sequence's last block
-            const int orow = (int)((L - 1) % kBS), c = lane & 15;
-            char *tile = stages + st * 2 * kTcTile + (lane < 16 ? 0 : kTcTile);
-            *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTcTile / 2) + orow * 128 +
-                                       (((c & 7) ^ (orow & 7)) << 4)) = newrow[lane];
-            __syncwarp();
+    int gbase = 0;  // ring position of this piece's first tile
+    for (int pc = pc0; pc < pc1; ++pc) {
+        const int k = pc - pc0;
+        const bool more = pc + 1 < pc1;
+        // this piece: from the producer (schedule), else worked out again
+        // here from the grid position (cheaper in registers than carrying it)
+        TcWork w;
+        if constexpr (SCHED) {
+            w = s_work[k & 1];
+        } else {
+            const CUtensorMap *mk = map_k, *mv = map_v;
+            w = tc_work<LINEAR, SCHED>(p, pc, false, mk, mv);
         }
-
-        tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
-        __syncwarp();
-        mbar_arrive(&empty[st]);
-    }
-
-    // ---- per-warp totals over the 8 token lanes (g)
+        if (!w.run) {
+            if (more) named_bar_sync(2, kDecodeThreads);  // in step with the producer
+            continue;
+        }
+        const int b = w.b, h = w.h, nloc = w.nloc, blk0 = w.blk0;
+        // tokens from this piece's first block on (at most nloc * 16), and the
+        // new token's row in the sequence's last block
+        const int rem = (int)(w.L - (long long)blk0 * kBS);
+        const int orow = (int)((w.L - 1) & (kBS - 1));
+        // Fused append: the last piece of (b, h) writes the new token's K/V
+        // row (head h) to its pool slot and, since the block holding it may
+        // have been copied before that write lands, patches the row into its
+        // own copy of the sequence's last block.  Lane x < 16 carries 16-byte
+        // chunk x of the K row, lane 16 + x chunk x of the V row.
+        const bool fuse = p.new_k != nullptr && w.split == w.nsplit - 1;
+        const bool patch = fuse && nloc > 0 && blk0 + nloc == w.nblk;
+        if (fuse && warp == (patch ? (gbase + nloc - 1) % kNW : 0)) {
+            const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
+            const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
+            newrow[lane] = v;  // kept in shared memory until the last block arrives
+            const long long slot = p.new_slots[b];
+            if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
+                const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
+                uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
+                             row * (D * 2 / 16) + (lane & 15);
+                *dst = v;
+            } else if (slot >= 0 && lane == 0) {
+                atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+            }
+        }
+        // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
+        uint32_t qf[8][2];
+        {
+            const bool live = g < p.g;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                reinterpret_cast<const uint16_t *>(p.q) + ((size_t)b * p.num_q_heads + h * p.g + (live ? g : 0)) * D);
 #pragma unroll
-    for (int x = 4; x <= 16; x <<= 1) {
-        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
-        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
-    }
-    named_bar_sync(1, kNW * 32);
-    float *sm_o = reinterpret_cast<float *>(stages);  // [kNW][G][D]
-    float *sm_m = sm_o + kNW * G * D;
-    float *sm_l = sm_m + kNW * G;
+            for (int kk = 0; kk < 8; ++kk) {
+                qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
+                qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
+            }
+        }
+        // running state for heads 2t, 2t+1 (replicated over g)
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        float o[8][4];
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        sm_o[(warp * G + 2 * t) * D + 16 * mt + g] = o[mt][0];
-        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g] = o[mt][1];
-        sm_o[(warp * G + 2 * t) * D + 16 * mt + g + 8] = o[mt][2];
-        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g + 8] = o[mt][3];
-    }
-    if (g == 0) {
-        sm_m[warp * G + 2 * t] = m_run[0];
-        sm_m[warp * G + 2 * t + 1] = m_run[1];
-        sm_l[warp * G + 2 * t] = l_run[0];
-        sm_l[warp * G + 2 * t + 1] = l_run[1];
-    }
-    named_bar_sync(1, kNW * 32);
+        for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid);
+        if (!s_abort) {
+            for (int i = ((warp - gbase) % kNW + kNW) % kNW; i < nloc; i += kNW) {
+                const int gi = gbase + i, st = gi % NST, r = gi / NST;
+                if (!mbar_wait(&full[st], r & 1, p.err)) {
+                    s_abort = 1;
+                    break;
+                }
+                int ntok = min(kBS, rem - i * kBS);
+                if (!stage_valid[st]) ntok = 0;
+                const uint32_t kt = stage_base + st * 2 * kTcTile;
+                const uint32_t vt = kt + kTcTile;
+                if (patch && i == nloc - 1 && ntok > 0) {
+                    // the new token is row orow of the sequence's last block
+                    const int c = lane & 15;
+                    char *tile = stages + st * 2 * kTcTile + (lane < 16 ? 0 : kTcTile);
+                    *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTcTile / 2) + orow * 128 +
+                                               (((c & 7) ^ (orow & 7)) << 4)) = newrow[lane];
+                    __syncwarp();
+                }
+
+                tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
+                __syncwarp();
+                mbar_arrive(&empty[st]);
+            }
+        }
+        gbase += nloc;
+
+        // ---- per-warp totals over the 8 token lanes (g)
+#pragma unroll
+        for (int x = 4; x <= 16; x <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
+        }
+        named_bar_sync(1, kNW * 32);
+        float *sm_o = reinterpret_cast<float *>(stages);  // [kNW][G][D]
+        float *sm_m = sm_o + kNW * G * D;
+        float *sm_l = sm_m + kNW * G;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            sm_o[(warp * G + 2 * t) * D + 16 * mt + g] = o[mt][0];
+            sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g] = o[mt][1];
+            sm_o[(warp * G + 2 * t) * D + 16 * mt + g + 8] = o[mt][2];
+            sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g + 8] = o[mt][3];
+        }
+        if (g == 0) {
+            sm_m[warp * G + 2 * t] = m_run[0];
+            sm_m[warp * G + 2 * t + 1] = m_run[1];
+            sm_l[warp * G + 2 * t] = l_run[0];
+            sm_l[warp * G + 2 * t + 1] = l_run[1];
+        }
+        named_bar_sync(1, kNW * 32);
+
+        if constexpr (SCHED) w = s_work[k & 1];  // not overwritten before barrier 2
+        finish_partition<G, D>(p, sm_o, sm_m, sm_l, w.b, w.h, w.split, w.nsplit, w.pre, tid, s_mw,
+                               &s_flag, more);
+    }
 }
 
-static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst) {
+static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst, int tables) {
     return 1024 + decode_ring_bytes<128, 8, true>(nst) + 2 * nst * sizeof(uint64_t) +
-           nst * sizeof(int) + 32 * sizeof(uint4) + (size_t)(linear ? 0 : part_blocks) * sizeof(int32_t);
+           nst * sizeof(int) + 32 * sizeof(uint4) +
+           (size_t)(linear ? 0 : tables * part_blocks) * sizeof(int32_t);
 }
 
 // Merges the per-split results of sequences cut into more than one split:
@@ -1073,7 +1233,13 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     if (reinterpret_cast<uintptr_t>(a.q) & 15) return KV_ERR_ARG;
     const int G = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
     int pb = 0, ms = 0;
-    split_plan(a.batch, a.num_kv_heads, a.max_blocks, a.num_splits, &pb, &ms);
+    if (a.sched) {
+        pb = a.sched_part_blocks;
+        ms = a.sched_max_splits;
+        if (a.part_base != 0 || a.start_tokens || a.seq_order) return KV_ERR_ARG;
+    } else {
+        split_plan(a.batch, a.num_kv_heads, a.max_blocks, a.num_splits, &pb, &ms);
+    }
     if (a.part_base < 0 || (a.part_base > 0 && !a.start_tokens)) return KV_ERR_ARG;
     const int slots = a.part_base + ms;  // workspace partial results per (sequence, query head)
     const size_t need = decode_workspace_bytes(a.batch, a.num_q_heads, a.head_dim, slots);
@@ -1106,6 +1272,12 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.new_v = static_cast<const uint4 *>(a.new_v);
     kp.new_slots = a.new_slots;
     kp.seq_order = a.seq_order;
+    kp.batch = a.batch;
+    if (a.sched) {
+        kp.sched_cta = a.sched + kSchedHeader;
+        kp.sched_pieces = reinterpret_cast<const int4 *>(a.sched + sched_piece_off(a.sched_ctas));
+        kp.sched_npieces = a.sched_pieces;
+    }
     kp.out = a.out;
     kp.out_bf16 = a.out_dtype == KV_BF16;
     kp.lse = a.lse;
@@ -1116,7 +1288,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.req_maps = a.req_maps;
     kp.counters = (a.counters && (long long)a.batch * a.num_kv_heads <= a.counter_slots) ? a.counters
                                                                                        : nullptr;
-    const dim3 grid(ms, a.num_kv_heads, a.batch);
+    const dim3 grid = a.sched ? dim3(a.sched_ctas, 1, 1) : dim3(ms, a.num_kv_heads, a.batch);
     kv_status st;
     const bool bf = a.dtype == KV_BF16;
     // Large head groups on bf16 / d128 go to the tensor-core variant when the
@@ -1124,19 +1296,22 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     const bool use_tc = bf && a.head_dim == 128 && g >= PKV_TC_MIN_G &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
     if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
+    // a schedule: paged tensor-core path, every merge inside the kernel
+    if (a.sched && (!use_tc || linear || (slots > 1 && !kp.counters))) return KV_ERR_UNSUPPORTED;
     if (use_tc) {
         // Long partitions: a deep ring (8 stages) and 3 CTAs per SM; short
         // ones: more CTAs at once (5 per SM) with 4 stages each.  Sweeps on
         // GB300 (Llama-3-8B shape, 129-block partitions: 5959 vs 5502 GB/s;
         // Yi-6B shape, 384-512-block partitions: 6288 vs 5965 GB/s).
-        const bool deep = pb >= kTcDeepBlocks;
+        const bool deep = a.sched ? a.sched_deep != 0 : pb >= kTcDeepBlocks;
         const int nst = deep ? 8 : 4;
-        const size_t smem = decode_tc_smem_bytes(linear, pb, nst);
+        const size_t smem = decode_tc_smem_bytes(linear, pb, nst, a.sched ? 2 : 1);
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = deep ? (linear ? decode_tc_kernel<true, 8, 3> : decode_tc_kernel<false, 8, 3>)
-                       : (linear ? decode_tc_kernel<true, 4, 5> : decode_tc_kernel<false, 4, 5>);
+        auto fn = a.sched ? (deep ? decode_tc_kernel<false, true, 8, 3> : decode_tc_kernel<false, true, 4, 5>)
+                  : deep ? (linear ? decode_tc_kernel<true, false, 8, 3> : decode_tc_kernel<false, false, 8, 3>)
+                         : (linear ? decode_tc_kernel<true, false, 4, 5> : decode_tc_kernel<false, false, 4, 5>);
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
@@ -1253,6 +1428,119 @@ kv_status kv_decode_plan(const int32_t *host_seq_lens, int batch, int num_kv_hea
     return KV_OK;
 }
 
+// ---- balanced schedule ------------------------------------------------------
+// One wave of CTAs that all stream the same number of blocks.  The blocks of
+// every (sequence, kv head) pair are laid end to end (sequence-major, heads
+// inside) and cut into C equal runs; a run that crosses pairs becomes several
+// pieces.  A pair's pieces are its split-KV partitions, merged by the last CTA
+// to finish one of them.
+static int sched_sms(int num_sms) { return num_sms > 0 ? num_sms : sm_count(); }
+
+kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_blocks, int num_sms,
+                                      size_t *ints) {
+    if (!ints || batch < 0 || num_kv_heads <= 0 || max_blocks < 0 || num_sms < 0)
+        return KV_ERR_ARG;
+    const long long total = (long long)batch * num_kv_heads * max_blocks;
+    long long c = 5LL * sched_sms(num_sms);
+    const long long c_long = (total + kMaxPartBlocks - 1) / kMaxPartBlocks;
+    if (c_long > c) c = c_long;
+    if (c > (1LL << 30)) return KV_ERR_UNSUPPORTED;
+    *ints = sched_piece_off((int)c) + 4 * (size_t)(c + (long long)batch * num_kv_heads);
+    return KV_OK;
+}
+
+kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
+                             int max_blocks, int num_sms, int32_t *schedule_out,
+                             size_t capacity_ints, size_t *used_ints) {
+    if (!schedule_out || batch < 0 || num_kv_heads <= 0 || max_blocks < 0 || num_sms < 0 ||
+        (batch > 0 && !host_seq_lens))
+        return KV_ERR_ARG;
+    if (num_kv_heads > 0xffff) return KV_ERR_UNSUPPORTED;
+    const int sms = sched_sms(num_sms);
+    std::vector<int> nb(batch);
+    long long T = 0;
+    int nbmax = 0;
+    for (int b = 0; b < batch; ++b) {
+        long long L = host_seq_lens[b];
+        if (L < 0) L = 0;
+        if (L > (long long)max_blocks * kBS) L = (long long)max_blocks * kBS;
+        nb[b] = (int)((L + kBS - 1) / kBS);
+        T += (long long)nb[b] * num_kv_heads;
+        if (nb[b] > nbmax) nbmax = nb[b];
+    }
+    // One wave: the deep ring (at most 2.4 CTAs per SM, the rate the
+    // grid-indexed plan found best) when every CTA gets at least
+    // kTcDeepBlocks blocks, else the wide kernel at five CTAs per SM.
+    const long long c_deep = (12LL * sms) / 5, c_wide = 5LL * sms;
+    long long W = (T + c_deep - 1) / c_deep;
+    if (W < kTcDeepBlocks) W = (T + c_wide - 1) / c_wide;
+    // A pair of n blocks spans at most ceil(n / W) + 1 runs; keep that within
+    // the merge done inside the kernel.
+    const long long w_pairs = (nbmax + kFuseMaxSplits - 2) / (kFuseMaxSplits - 1);
+    if (W < w_pairs) W = w_pairs;
+    if (W < 1) W = 1;
+    if (W > kMaxPartBlocks) W = kMaxPartBlocks;
+    if ((nbmax + W - 1) / W + 1 > kFuseMaxSplits) return KV_ERR_UNSUPPORTED;
+    const long long C = T > 0 ? (T + W - 1) / W : 1;
+    if (C > (1LL << 30)) return KV_ERR_UNSUPPORTED;
+    const size_t need = sched_piece_off((int)C) + 4 * (size_t)(C + (long long)batch * num_kv_heads);
+    if (used_ints) *used_ints = need;
+    if (capacity_ints < need) return KV_ERR_ARG;
+
+    int32_t *cta = schedule_out + kSchedHeader;
+    int32_t *pcs = schedule_out + sched_piece_off((int)C);
+    long long pos = 0, next_cta = 0;
+    int np = 0, most = 1;
+    auto open_to = [&](long long c) {  // CTAs up to c start at the next piece
+        while (next_cta <= c) cta[next_cta++] = np;
+    };
+    auto emit = [&](int b, int h, long long blk0, long long n, long long split, long long ns) {
+        int32_t *q = pcs + 4 * (size_t)np++;
+        q[0] = b;
+        q[1] = h | (int32_t)(split << 16);
+        q[2] = (int32_t)blk0;
+        q[3] = (int32_t)n | (int32_t)(ns << 16);
+    };
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const long long n = nb[b];
+            if (n == 0) {  // an empty pair still writes out = 0, lse = -inf
+                open_to(std::min(pos / W, C - 1));
+                emit(b, h, 0, 0, 0, 1);
+                continue;
+            }
+            const long long s0 = pos / W, s1 = (pos + n - 1) / W, ns = s1 - s0 + 1;
+            if (ns > most) most = (int)ns;
+            for (long long c = s0; c <= s1; ++c) {
+                const long long lo = std::max(pos, c * W), hi = std::min(pos + n, (c + 1) * W);
+                open_to(c);
+                emit(b, h, lo - pos, hi - lo, c - s0, ns);
+            }
+            pos += n;
+        }
+    }
+    open_to(C);  // CTAs without pieces of their own, then the end marker
+    schedule_out[0] = (int32_t)C;
+    schedule_out[1] = np;
+    schedule_out[2] = most;
+    schedule_out[3] = (int32_t)W;
+    schedule_out[4] = W >= kTcDeepBlocks ? 1 : 0;
+    schedule_out[5] = batch;
+    schedule_out[6] = num_kv_heads;
+    schedule_out[7] = 0;
+    if (used_ints) *used_ints = sched_piece_off((int)C) + 4 * (size_t)np;
+    return KV_OK;
+}
+
+kv_status kv_decode_schedule_workspace_size(const int32_t *host_schedule, int num_q_heads,
+                                            int head_dim, size_t *bytes) {
+    if (!host_schedule || !bytes || num_q_heads <= 0 || head_dim <= 0 || host_schedule[5] < 0 ||
+        host_schedule[2] < 1)
+        return KV_ERR_ARG;
+    *bytes = decode_workspace_bytes(host_schedule[5], num_q_heads, head_dim, host_schedule[2]);
+    return KV_OK;
+}
+
 kv_status kv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                    int max_blocks, int num_splits, size_t *bytes) {
     if (!bytes || batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks < 0)
@@ -1350,6 +1638,66 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
     if (kv_status st1 = kv_append(p, k_new, v_new, slot_mapping, batch, stream)) return st1;
     a.new_k = a.new_v = nullptr;
     a.new_slots = nullptr;
+    return launch_decode(a, false);
+}
+
+kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const void *k_new,
+                                           const void *v_new, const int64_t *slot_mapping,
+                                           const int32_t *block_tables, int max_blocks,
+                                           const int32_t *seq_lens, int batch, int num_q_heads,
+                                           float scale, const int32_t *host_schedule,
+                                           const int32_t *schedule, void *out, kv_dtype out_dtype,
+                                           float *lse_out, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    if (!p || batch < 0 || max_blocks < 0 || !host_schedule || !schedule ||
+        (batch > 0 && max_blocks > 0 && !block_tables))
+        return KV_ERR_ARG;
+    if (batch == 0) return KV_OK;
+    const int32_t *hs = host_schedule;
+    if (hs[0] < 1 || hs[1] < 0 || hs[2] < 1 || hs[2] > kFuseMaxSplits || hs[3] < 1 ||
+        hs[3] > kMaxPartBlocks || (hs[4] != 0 && hs[4] != 1) || hs[5] != batch ||
+        hs[6] != p->num_kv_heads)
+        return KV_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(schedule) & 15) return KV_ERR_ARG;
+    if (k_new && (!v_new || !slot_mapping)) return KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+        return KV_ERR_ARG;
+    if (p->dtype != KV_BF16 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+    if (kv_status st = pool_tensor_maps(p)) return st;
+    DecodeArgs a{};
+    a.q = q;
+    a.k_pool = p->k;
+    a.v_pool = p->v;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.num_blocks = p->num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.head_dim = p->head_dim;
+    a.dtype = p->dtype;
+    a.scale = scale;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse_out;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.err = p->err;
+    a.counters = p->counters;
+    a.counter_slots = kv_pool::kCounterSlots;
+    a.stream = as_stream(stream);
+    a.pool_map_k = &p->tmap_k;
+    a.pool_map_v = &p->tmap_v;
+    a.new_k = k_new;
+    a.new_v = v_new;
+    a.new_slots = k_new ? slot_mapping : nullptr;
+    a.sched = schedule;
+    a.sched_ctas = hs[0];
+    a.sched_pieces = hs[1];
+    a.sched_max_splits = hs[2];
+    a.sched_part_blocks = hs[3];
+    a.sched_deep = hs[4];
     return launch_decode(a, false);
 }
 

@@ -100,6 +100,10 @@ struct DecodeArgs {
     const void *new_v;
     const int64_t *new_slots;
     const int32_t *seq_order;  // device permutation of the batch: grid order, or null
+    // balanced schedule (kv_decode_schedule): its device copy, or null, and
+    // the header values read from the host copy
+    const int32_t *sched;
+    int sched_ctas, sched_pieces, sched_max_splits, sched_part_blocks, sched_deep;
     int *counters;
     long long counter_slots;
     void *workspace;

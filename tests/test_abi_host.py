@@ -258,3 +258,92 @@ def test_batched_planner_changes_nothing_on_failure():
     assert pk.kv_allocator_num_free(a) == before[2]
     for blk in t[0, :3]:
         assert pk.kv_allocator_refcount(a, int(blk)) == 2
+
+
+def _parse_schedule(s):
+    C, P, most, W, deep, B, hkv = (int(x) for x in s[:7])
+    cta = s[8:8 + C + 1]
+    off = (8 + C + 1 + 3) // 4 * 4
+    pcs = s[off:off + 4 * P].reshape(P, 4)
+    pieces = [dict(b=int(x[0]), h=int(x[1]) & 0xffff, split=int(x[1]) >> 16, blk0=int(x[2]),
+                   n=int(x[3]) & 0xffff, ns=int(x[3]) >> 16) for x in pcs]
+    return dict(C=C, P=P, most=most, W=W, deep=deep, B=B, hkv=hkv, cta=cta, pieces=pieces)
+
+
+@pytest.mark.parametrize("case", ["llama", "yi", "ragged", "one_long", "all_empty"])
+def test_decode_schedule_covers_every_block_once_in_equal_runs(case):
+    """The balanced schedule cuts the blocks of all (sequence, kv head) pairs,
+    laid end to end, into runs of equal length: every block of every pair in
+    exactly one piece, each pair's pieces numbered 0..n-1 in block order, every
+    CTA but the last holding exactly W blocks."""
+    g = W.rng(4040)
+    hkv, max_blocks = 8, 256
+    if case == "llama":
+        lens = W.decode_lengths("llama3_8b_decode") + 1
+    elif case == "yi":
+        lens, hkv, max_blocks = W.decode_lengths("yi6b_long_decode"), 4, 12288
+    elif case == "ragged":
+        lens = np.concatenate([[0, 1, 15, 16, 17, 4096, 0], g.integers(1, 4096, 40)])
+    elif case == "one_long":
+        lens, hkv, max_blocks = np.array([196608]), 1, 12288
+    else:
+        lens = np.zeros(5, np.int64)
+    lens = np.asarray(lens, np.int32)
+    s = _parse_schedule(pk.kv_decode_schedule(lens, hkv, max_blocks, num_sms=152))
+    nb = -(-lens.astype(np.int64) // 16)
+    T = int(nb.sum()) * hkv
+    assert s["B"] == len(lens) and s["hkv"] == hkv
+    C, Wd = s["C"], s["W"]
+    assert C == max(1, -(-T // Wd))
+    # one wave: five CTAs per SM, or 2.4 with the deep ring (runs >= 256 blocks)
+    assert s["deep"] == (Wd >= 256)
+    assert C <= (364 if s["deep"] else 760)
+    if case == "llama":
+        assert not s["deep"] and Wd == -(-T // 760)
+    if case == "yi":
+        assert s["deep"] and Wd == -(-T // 364)
+    # per-pair coverage
+    seen = {}
+    per_cta = np.zeros(C, np.int64)
+    cta = s["cta"]
+    assert cta[0] == 0 and cta[-1] == s["P"] and np.all(np.diff(cta) >= 0)
+    for c in range(C):
+        last = -1
+        for i in range(cta[c], cta[c + 1]):
+            q = s["pieces"][i]
+            key = (q["b"], q["h"])
+            gpos = (q["b"] * hkv + q["h"]) * 10**6 + q["blk0"]
+            assert gpos >= last  # pieces of a CTA in end-to-end order
+            last = gpos
+            seen.setdefault(key, []).append(q)
+            per_cta[c] += q["n"]
+    assert sorted(seen) == [(b, h) for b in range(len(lens)) for h in range(hkv)]
+    most = 1
+    for (b, h), qs in seen.items():
+        qs.sort(key=lambda q: q["split"])
+        ns = qs[0]["ns"]
+        most = max(most, ns)
+        assert ns <= 32 and [q["split"] for q in qs] == list(range(ns))
+        assert all(q["ns"] == ns for q in qs)
+        pos = 0
+        for q in qs:
+            assert q["blk0"] == pos and 0 <= q["n"] <= Wd
+            pos += q["n"]
+        assert pos == nb[b]
+        if nb[b] == 0:
+            assert ns == 1 and qs[0]["n"] == 0
+    assert s["most"] == most
+    # equal runs
+    assert np.all(per_cta[:-1] == Wd) and 0 <= per_cta[-1] <= Wd and per_cta.sum() == T
+
+
+def test_decode_schedule_workspace_and_limits():
+    lens = np.full(3, 4096, np.int32)
+    s = pk.kv_decode_schedule(lens, 8, 256, num_sms=152)
+    most = int(s[2])
+    assert pk.kv_decode_schedule_workspace_size(s, 32, 128) == (
+        0 if most == 1 else 3 * 32 * most * (128 + 1) * 4)
+    # a sequence that would need more than 32 pieces of at most 1024 blocks
+    with pytest.raises(pk.KVError) as e:
+        pk.kv_decode_schedule(np.array([33 * 1024 * 16], np.int32), 1, 33 * 1024, num_sms=152)
+    assert e.value.status == -3
