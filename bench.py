@@ -266,7 +266,8 @@ def run_ours(args, rank, world, local_rank):
         d_order = torch.from_numpy(h_order).cuda()
         if balanced:
             # or: one wave of CTAs with equal runs of blocks (host-made schedule)
-            h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks)
+            h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks,
+                                            num_ctas=args.sched_ctas, ring_stages=args.sched_ring)
             d_sched = torch.from_numpy(h_sched).cuda()
             ws_bytes = pk.kv_decode_schedule_workspace_size(h_sched, hq, d)
             ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
@@ -420,7 +421,8 @@ def run_ours(args, rank, world, local_rank):
             "num_splits": splits,
             "part_blocks": part_blocks,
             "max_splits": max_splits,
-            "plan": ("balanced schedule: %d CTAs of %d blocks" % (int(h_sched[0]), int(h_sched[3]))
+            "plan": ("balanced schedule: %d CTAs of %d blocks, %d-stage ring"
+                     % (int(h_sched[0]), int(h_sched[3]), 8 if int(h_sched[4]) else 4)
                      if balanced else "grid-indexed" + ("" if contig else ", longest first")),
             "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2); no flush",
@@ -964,6 +966,10 @@ def main():
                     help="0 = plan from the host-known lengths (kv_decode_plan)")
     ap.add_argument("--plan", default="grid", choices=["grid", "balanced"],
                     help="paged decode: grid-indexed split plan or balanced schedule")
+    ap.add_argument("--sched-ctas", type=int, default=0,
+                    help="balanced plan: CTAs (0 = kv_decode_schedule's rule)")
+    ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],
+                    help="balanced plan: ring stages (0 = kv_decode_schedule's rule)")
     ap.add_argument("--prefix-splits", type=int, default=0,
                     help="shared-prefix step: key-range partitions of each group's prefix "
                          "(0 = kv_cascade_plan)")

@@ -358,6 +358,10 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
  *   host_seq_lens  host int32[batch]: the lengths the decode will see on the
  *                  device (a decode step: after its append);
  *   num_sms        SMs to plan for, 0 = the current device's;
+ *   num_ctas       0 = the rule above; else this many CTAs (at most one wave:
+ *                  5 per SM with 4 ring stages, 3 per SM with 8);
+ *   ring_stages    0 = the rule above; else 4 (the wide kernel) or 8 (the
+ *                  deep ring);
  *   schedule_out   host int32[capacity_ints]; *used_ints receives the words
  *                  written (the caller copies that many to the device).
  * Capacity: kv_decode_schedule_capacity's bound for this batch shape.  Host
@@ -366,8 +370,8 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
 kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_blocks, int num_sms,
                                       size_t *ints);
 kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
-                             int max_blocks, int num_sms, int32_t *schedule_out,
-                             size_t capacity_ints, size_t *used_ints);
+                             int max_blocks, int num_sms, int num_ctas, int ring_stages,
+                             int32_t *schedule_out, size_t capacity_ints, size_t *used_ints);
 /* Workspace bytes paged_decode_attention_scheduled needs with this schedule
  * (its host copy). */
 kv_status kv_decode_schedule_workspace_size(const int32_t *host_schedule, int num_q_heads,

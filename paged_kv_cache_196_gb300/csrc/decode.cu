@@ -749,58 +749,32 @@ KV_DEVICE void tc_attend_block(const uint32_t (&qf)[8][2], uint32_t kt, uint32_t
 }
 
 
-// One pass of the tensor-core decode's piece loop: blocks [blk0, blk0 + nloc)
-// of kv head h of sequence b, partial result `split` of the pair's nsplit
-// (after `pre` results of a cascade prefix).  run == 0: nothing to attend or
-// write (the same for every thread of the CTA).
-struct TcWork {
-    long long L;  // tokens of sequence b (clamped to what may be read)
-    int b, h, split, nsplit, blk0, nloc, nblk, pre;
-    int run;
-};
-
-// Resolves piece pc of a scheduled launch, or this CTA's grid position.  Only
-// the thread with report set records device errors.  LINEAR also selects the
-// request's K/V maps.
-template <bool LINEAR, bool SCHED>
-KV_DEVICE TcWork tc_work(const DecodeKParams &p, int pc, bool report, const CUtensorMap *&map_k,
-                         const CUtensorMap *&map_v) {
-    static_assert(!(LINEAR && SCHED), "schedules cover the paged path only");
-    TcWork w{};
-    if constexpr (SCHED) {
-        const int4 d = __ldg(p.sched_pieces + pc);
-        w.b = d.x;
-        w.h = d.y & 0xffff;
-        w.split = (int)((unsigned)d.y >> 16);
-        w.blk0 = d.z;
-        w.nloc = d.w & 0xffff;
-        w.nsplit = (int)((unsigned)d.w >> 16);
-        if (w.b < 0 || w.b >= p.batch || w.h >= p.num_kv_heads || w.nsplit < 1 ||
-            w.split >= w.nsplit || w.nsplit > p.max_splits || w.blk0 < 0 ||
-            w.nloc > p.part_blocks) {
-            if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-            return w;
-        }
-    } else {
-        w.split = blockIdx.x;
-        w.h = blockIdx.y;
-        w.b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
-        if (w.b < 0 || w.b >= (int)gridDim.z) {  // not a permutation of the batch
-            if (report && w.split == 0 && w.h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-            return w;
-        }
+// NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
+// compiled for MINB resident CTAs per SM.
+template <bool LINEAR, int NST, int MINB>
+__global__ void __launch_bounds__(kDecodeThreads, MINB)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
+                     const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
+    constexpr int G = 8, D = 128;
+    const int split = blockIdx.x, h = blockIdx.y;
+    const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
+    if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
+        if (threadIdx.x == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        return;
     }
-    const bool first = report && w.split == 0 && w.h == 0;  // one report per sequence
-    long long L = p.seq_lens[w.b];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    long long L = p.seq_lens[b];
+    const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
     if constexpr (LINEAR) {
-        const int req = p.req_ids[w.b];
+        const int req = p.req_ids[b];
         if (req < 0 || req >= p.max_requests || p.k_bases[req] == 0) {
-            if (first) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+            if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
             L = 0;
         } else {
             const long long mapped = p.mapped_tokens[req];
             if (L > mapped) {
-                if (first) atomicOr(p.err, KV_DEVERR_UNMAPPED);
+                if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
                 L = mapped;
             }
             map_k = p.req_maps + 2 * req;
@@ -808,58 +782,18 @@ KV_DEVICE TcWork tc_work(const DecodeKParams &p, int pc, bool report, const CUte
         }
     }
     if (L > (long long)p.max_blocks * kBS) {
-        if (first) atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
+        if (tid == 0 && split == 0 && h == 0)
+            atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
         L = (long long)p.max_blocks * kBS;
     }
     if (L < 0) L = 0;
-    w.nblk = (int)((L + kBS - 1) / kBS);
-    if constexpr (SCHED) {
-        // The schedule was made from host copies of the lengths: a piece past
-        // the end, or a last piece that stops short of it, means they differ.
-        const long long end = (long long)w.blk0 + w.nloc;
-        if (end > w.nblk || (w.split == w.nsplit - 1 && end != w.nblk)) {
-            if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-            w.nloc = (int)max(0LL, min((long long)w.nloc, (long long)w.nblk - w.blk0));
-        }
-    } else {
-        const int sblk = start_block(p, w.b, L);
-        w.pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
-        w.blk0 = sblk + w.split * p.part_blocks;
-        if (w.blk0 >= w.nblk && w.split > 0) return w;  // nothing for this split
-        w.nloc = max(0, min(p.part_blocks, w.nblk - w.blk0));
-        w.nsplit = max(1, (w.nblk - sblk + p.part_blocks - 1) / p.part_blocks);
-    }
-    w.L = L;
-    w.run = 1;
-    return w;
-}
-
-// NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
-// compiled for MINB resident CTAs per SM.
-//
-// Work: one partition named by the grid position, or, with a schedule, the
-// CTA's list of pieces.  The pieces of a list stream through the same ring one
-// after the other (ring position and barrier phases continue across them).
-// While the consumers finish a piece, the producer reads the next piece's
-// description and table slice; it refills the ring once the consumers have
-// read their merge scratch out of it (named barrier 2), so the split merge of
-// one piece overlaps the first copies of the next.
-template <bool LINEAR, bool SCHED, int NST, int MINB>
-__global__ void __launch_bounds__(kDecodeThreads, MINB)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
-                     const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
-    constexpr int G = 8, D = 128;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int pc0 = 0, pc1 = 1;
-    if constexpr (SCHED) {
-        pc0 = __ldg(p.sched_cta + blockIdx.x);
-        pc1 = __ldg(p.sched_cta + blockIdx.x + 1);
-        if (pc0 < 0 || pc1 < pc0 || pc1 > p.sched_npieces) {
-            if (tid == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-            return;
-        }
-        if (pc0 == pc1) return;
-    }
+    const int nblk = (int)((L + kBS - 1) / kBS);
+    const int sblk = start_block(p, b, L);
+    const int pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
+    const int blk0 = sblk + split * p.part_blocks;
+    if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
+    const int nloc = max(0, min(p.part_blocks, nblk - blk0));
+    const int nsplit = max(1, (nblk - sblk + p.part_blocks - 1) / p.part_blocks);
 
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -870,29 +804,19 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     uint64_t *empty = full + NST;
     int *stage_valid = reinterpret_cast<int *>(empty + NST);
     uint4 *newrow = reinterpret_cast<uint4 *>(stage_valid + NST);  // [32]: fused append's K, V rows
-    int32_t *tbl_buf = reinterpret_cast<int32_t *>(newrow + 32);   // [1 or 2][part_blocks]
-    __shared__ TcWork s_work[2];                      // this piece's and the next one's
-    __shared__ float s_mw[G * kFuseMaxSplits];        // split-merge weights
-    __shared__ int s_flag, s_abort;
+    int32_t *tbl = reinterpret_cast<int32_t *>(newrow + 32);       // [part_blocks]
 
-    // the producer's K/V maps: the pool's, or (LINEAR) the request's
-    const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
     if (warp == kNW) {
-        const TcWork w0 = tc_work<LINEAR, SCHED>(p, pc0, lane == 0, map_k, map_v);
+        if constexpr (!LINEAR) {
+            const int32_t *row = p.tables + (size_t)b * p.max_blocks + blk0;
+            for (int i = lane; i < nloc; i += 32) tbl[i] = __ldg(row + i);
+        }
         if (lane == 0) {
-            s_work[0] = w0;
-            s_abort = 0;
             for (int st = 0; st < NST; ++st) {
                 mbar_init(&full[st], 1);
                 mbar_init(&empty[st], 32);
             }
             mbar_init_fence();
-        }
-        if constexpr (!LINEAR) {
-            if (w0.run) {
-                const int32_t *row = p.tables + (size_t)w0.b * p.max_blocks + w0.blk0;
-                for (int i = lane; i < w0.nloc; i += 32) tbl_buf[i] = __ldg(row + i);
-            }
         }
     }
     __syncthreads();
@@ -903,11 +827,255 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
         }
         const uint64_t policy = l2_evict_first_policy();
+        int issued = 0;
+        for (int i = 0; i < nloc; ++i) {
+            const int st = i % NST, r = i / NST;
+            bool bad = false;
+            if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
+            if (__shfl_sync(0xffffffffu, bad, 0)) break;
+            int y;
+            bool valid = true;
+            if constexpr (LINEAR) {
+                y = (int)((long long)h * p.head_stride + (long long)(blk0 + i) * kBS);
+            } else {
+                const int id = tbl[i];
+                valid = id >= 0 && id < p.num_blocks;
+                y = ((valid ? id : 0) * p.num_kv_heads + h) * kBS;
+            }
+            char *dst = stages + st * 2 * kTcTile;
+            if (lane == 0) {
+                if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+                stage_valid[st] = valid ? 1 : 0;
+                if (valid)
+                    mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
+                else
+                    mbar_arrive(&full[st]);
+            }
+            if (valid) {
+                if (PKV_TC_MULTILANE) {
+                    // lane x issues box x: K half 0, K half 1, V half 0, V half 1
+                    if (lane < 4)
+                        mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
+                                   lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
+                } else if (lane == 0) {
+                    mma::tma2d(dst, map_k, 0, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
+                    mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
+                }
+            }
+            issued = i + 1;
+        }
+        if (lane == 0)
+            for (int st = 0; st < NST && st < issued; ++st)
+                mbar_wait(&full[st], ((issued - 1 - st) / NST) & 1, p.err);
+        return;
+    }
+
+    // ---- consumer warps: lane = (g = lane / 4, t = lane % 4)
+    const int g = lane >> 2, t = lane & 3;
+    // Fused append: the last split of (b, h) writes the new token's K/V row
+    // (head h) to its pool slot and, since the block holding it may have been
+    // copied before that write lands, patches the row into its own copy of
+    // the sequence's last block.  Lane x < 16 carries 16-byte chunk x of the
+    // K row, lane 16 + x chunk x of the V row.
+    const bool fuse = p.new_k != nullptr && split == nsplit - 1;
+    const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk;
+    if (fuse && warp == (patch ? (nloc - 1) % kNW : 0)) {
+        const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
+        const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
+        newrow[lane] = v;  // kept in shared memory until the last block arrives
+        const long long slot = p.new_slots[b];
+        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
+            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
+            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
+                         row * (D * 2 / 16) + (lane & 15);
+            *dst = v;
+        } else if (slot >= 0 && lane == 0) {
+            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+        }
+    }
+    // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
+    uint32_t qf[8][2];
+    {
+        const bool live = g < p.g;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            reinterpret_cast<const uint16_t *>(p.q) + ((size_t)b * p.num_q_heads + h * p.g + (live ? g : 0)) * D);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
+            qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
+        }
+    }
+    // running state for heads 2t, 2t+1 (replicated over g)
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const uint32_t stage_base = smem_addr(stages);
+
+    for (int i = warp; i < nloc; i += kNW) {
+        const int st = i % NST, r = i / NST;
+        if (!mbar_wait(&full[st], r & 1, p.err)) break;
+        int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
+        if (!stage_valid[st]) ntok = 0;
+        const uint32_t kt = stage_base + st * 2 * kTcTile;
+        const uint32_t vt = kt + kTcTile;
+        if (patch && i == nloc - 1 && ntok > 0) {
+            // the new token is row (L - 1) % 16 of the sequence's last block
+            const int orow = (int)((L - 1) % kBS), c = lane & 15;
+            char *tile = stages + st * 2 * kTcTile + (lane < 16 ? 0 : kTcTile);
+            *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTcTile / 2) + orow * 128 +
+                                       (((c & 7) ^ (orow & 7)) << 4)) = newrow[lane];
+            __syncwarp();
+        }
+
+        tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
+        __syncwarp();
+        mbar_arrive(&empty[st]);
+    }
+
+    // ---- per-warp totals over the 8 token lanes (g)
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
+    }
+    named_bar_sync(1, kNW * 32);
+    float *sm_o = reinterpret_cast<float *>(stages);  // [kNW][G][D]
+    float *sm_m = sm_o + kNW * G * D;
+    float *sm_l = sm_m + kNW * G;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        sm_o[(warp * G + 2 * t) * D + 16 * mt + g] = o[mt][0];
+        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g] = o[mt][1];
+        sm_o[(warp * G + 2 * t) * D + 16 * mt + g + 8] = o[mt][2];
+        sm_o[(warp * G + 2 * t + 1) * D + 16 * mt + g + 8] = o[mt][3];
+    }
+    if (g == 0) {
+        sm_m[warp * G + 2 * t] = m_run[0];
+        sm_m[warp * G + 2 * t + 1] = m_run[1];
+        sm_l[warp * G + 2 * t] = l_run[0];
+        sm_l[warp * G + 2 * t + 1] = l_run[1];
+    }
+    named_bar_sync(1, kNW * 32);
+
+    float *mw = sm_l + kNW * G;  // merge weights, then a flag (still in the ring)
+    finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid, mw,
+                           reinterpret_cast<int *>(mw + G * kFuseMaxSplits), false);
+}
+
+// One piece of a balanced schedule: blocks [blk0, blk0 + nloc) of kv head h
+// of sequence b, partial result `split` of the pair's nsplit.  run == 0:
+// nothing to attend or write (the same for every thread of the CTA).
+struct TcPiece {
+    long long L;  // tokens of sequence b (clamped to what may be read)
+    int b, h, split, nsplit, blk0, nloc, nblk;
+    int run;
+};
+
+// Reads and checks piece pc of the schedule against the device lengths.  Only
+// the thread with report set records device errors.
+KV_DEVICE TcPiece tc_piece(const DecodeKParams &p, int pc, bool report) {
+    TcPiece w{};
+    const int4 d = __ldg(p.sched_pieces + pc);
+    w.b = d.x;
+    w.h = d.y & 0xffff;
+    w.split = (int)((unsigned)d.y >> 16);
+    w.blk0 = d.z;
+    w.nloc = d.w & 0xffff;
+    w.nsplit = (int)((unsigned)d.w >> 16);
+    if (w.b < 0 || w.b >= p.batch || w.h >= p.num_kv_heads || w.nsplit < 1 ||
+        w.split >= w.nsplit || w.nsplit > p.max_splits || w.blk0 < 0 || w.nloc > p.part_blocks) {
+        if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        return w;
+    }
+    long long L = p.seq_lens[w.b];
+    if (L > (long long)p.max_blocks * kBS) {
+        if (report && w.split == 0 && w.h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        L = (long long)p.max_blocks * kBS;
+    }
+    if (L < 0) L = 0;
+    w.nblk = (int)((L + kBS - 1) / kBS);
+    // The schedule was made from host copies of the lengths: a piece past the
+    // end, or a last piece that stops short of it, means they differ.
+    const long long end = (long long)w.blk0 + w.nloc;
+    if (end > w.nblk || (w.split == w.nsplit - 1 && end != w.nblk)) {
+        if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        w.nloc = (int)max(0LL, min((long long)w.nloc, (long long)w.nblk - w.blk0));
+    }
+    w.L = L;
+    w.run = 1;
+    return w;
+}
+
+// decode_tc_kernel's attention on a balanced schedule (kv_decode_schedule):
+// CTA c runs the pieces [sched_cta[c], sched_cta[c + 1]), runs of blocks of
+// several (sequence, kv head) pairs, one after the other through the same
+// ring (ring position and barrier phases continue across pieces).  While the
+// consumers finish a piece, the producer reads the next piece and its table
+// slice; it refills the ring as soon as the consumers have read their merge
+// scratch out of it (named barrier 2), so the split merge of one piece
+// overlaps the first copies of the next.  NST ring stages, MINB CTAs per SM.
+template <int NST, int MINB>
+__global__ void __launch_bounds__(kDecodeThreads, MINB)
+    decode_tc_sched_kernel(const __grid_constant__ CUtensorMap pool_k_map,
+                           const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
+    constexpr int G = 8, D = 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pc0 = __ldg(p.sched_cta + blockIdx.x);
+    const int pc1 = __ldg(p.sched_cta + blockIdx.x + 1);
+    if (pc0 < 0 || pc1 < pc0 || pc1 > p.sched_npieces) {
+        if (tid == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        return;
+    }
+    if (pc0 == pc1) return;
+
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    char *stages = smem;  // NST x (K tile, V tile), swizzled
+    constexpr size_t kRing = decode_ring_bytes<D, G, true>(NST);
+    static_assert(NST % kNW == 0, "each stage must belong to one consumer warp");
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
+    uint64_t *empty = full + NST;
+    int *stage_valid = reinterpret_cast<int *>(empty + NST);
+    uint4 *newrow = reinterpret_cast<uint4 *>(stage_valid + NST);  // [32]: fused append's K, V rows
+    int32_t *tbl_buf = reinterpret_cast<int32_t *>(newrow + 32);   // [2][part_blocks]
+    __shared__ TcPiece s_work[2];                     // this piece and the next one
+    __shared__ float s_mw[G * kFuseMaxSplits];        // split-merge weights
+    __shared__ int s_flag, s_abort;
+
+    if (warp == kNW) {
+        const TcPiece w0 = tc_piece(p, pc0, lane == 0);
+        if (lane == 0) {
+            s_work[0] = w0;
+            s_abort = 0;
+            for (int st = 0; st < NST; ++st) {
+                mbar_init(&full[st], 1);
+                mbar_init(&empty[st], 32);
+            }
+            mbar_init_fence();
+        }
+        if (w0.run) {
+            const int32_t *row = p.tables + (size_t)w0.b * p.max_blocks + w0.blk0;
+            for (int i = lane; i < w0.nloc; i += 32) tbl_buf[i] = __ldg(row + i);
+        }
+    }
+    __syncthreads();
+
+    if (warp == kNW) {
+        const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(map_k) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
+        }
+        const uint64_t policy = l2_evict_first_policy();
         int gi = 0;  // tiles issued so far: ring position across pieces
         bool stop = false;
         for (int pc = pc0; pc < pc1; ++pc) {
             const int k = pc - pc0;
-            const TcWork w = s_work[k & 1];
+            const TcPiece w = s_work[k & 1];
             const int32_t *tbl = tbl_buf + (k & 1) * p.part_blocks;
             if (w.run && !stop) {
                 for (int i = 0; i < w.nloc; ++i) {
@@ -918,15 +1086,9 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                         stop = true;
                         break;
                     }
-                    int y;
-                    bool valid = true;
-                    if constexpr (LINEAR) {
-                        y = (int)((long long)w.h * p.head_stride + (long long)(w.blk0 + i) * kBS);
-                    } else {
-                        const int id = tbl[i];
-                        valid = id >= 0 && id < p.num_blocks;
-                        y = ((valid ? id : 0) * p.num_kv_heads + w.h) * kBS;
-                    }
+                    const int id = tbl[i];
+                    const bool valid = id >= 0 && id < p.num_blocks;
+                    const int y = ((valid ? id : 0) * p.num_kv_heads + w.h) * kBS;
                     char *dst = stages + st * 2 * kTcTile;
                     if (lane == 0) {
                         if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
@@ -936,38 +1098,25 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                         else
                             mbar_arrive(&full[st]);
                     }
-                    if (valid) {
-                        if (PKV_TC_MULTILANE) {
-                            // lane x issues box x: K half 0, K half 1, V half 0, V half 1
-                            if (lane < 4)
-                                mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
-                                           lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st],
-                                           policy);
-                        } else if (lane == 0) {
-                            mma::tma2d(dst, map_k, 0, y, &full[st], policy);
-                            mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
-                            mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
-                            mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
-                        }
-                    }
+                    // lane x issues box x: K half 0, K half 1, V half 0, V half 1
+                    if (valid && lane < 4)
+                        mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
+                                   lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
                     ++gi;
                 }
             }
             if (pc + 1 < pc1) {
-                // the next piece's description and table slice, read while the
-                // consumers finish this one
-                const CUtensorMap *mk = map_k, *mv = map_v;
-                const TcWork nx = tc_work<LINEAR, SCHED>(p, pc + 1, lane == 0, mk, mv);
+                // the next piece and its table slice, read while the consumers
+                // finish this one
+                const TcPiece nx = tc_piece(p, pc + 1, lane == 0);
                 if (lane == 0) {
                     s_work[(k + 1) & 1] = nx;
                     if (stop) s_abort = 1;
                 }
-                if constexpr (!LINEAR) {
-                    if (nx.run && !stop) {
-                        int32_t *t2 = tbl_buf + ((k + 1) & 1) * p.part_blocks;
-                        const int32_t *row = p.tables + (size_t)nx.b * p.max_blocks + nx.blk0;
-                        for (int i = lane; i < nx.nloc; i += 32) t2[i] = __ldg(row + i);
-                    }
+                if (nx.run && !stop) {
+                    int32_t *t2 = tbl_buf + ((k + 1) & 1) * p.part_blocks;
+                    const int32_t *row = p.tables + (size_t)nx.b * p.max_blocks + nx.blk0;
+                    for (int i = lane; i < nx.nloc; i += 32) t2[i] = __ldg(row + i);
                 }
                 named_bar_sync(2, kDecodeThreads);  // the consumers are out of the ring
             }
@@ -985,31 +1134,23 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     for (int pc = pc0; pc < pc1; ++pc) {
         const int k = pc - pc0;
         const bool more = pc + 1 < pc1;
-        // this piece: from the producer (schedule), else worked out again
-        // here from the grid position (cheaper in registers than carrying it)
-        TcWork w;
-        if constexpr (SCHED) {
-            w = s_work[k & 1];
-        } else {
-            const CUtensorMap *mk = map_k, *mv = map_v;
-            w = tc_work<LINEAR, SCHED>(p, pc, false, mk, mv);
-        }
-        if (!w.run) {
+        if (!s_work[k & 1].run) {
             if (more) named_bar_sync(2, kDecodeThreads);  // in step with the producer
             continue;
         }
-        const int b = w.b, h = w.h, nloc = w.nloc, blk0 = w.blk0;
+        const int b = s_work[k & 1].b, h = s_work[k & 1].h, nloc = s_work[k & 1].nloc;
+        const int blk0 = s_work[k & 1].blk0;
         // tokens from this piece's first block on (at most nloc * 16), and the
         // new token's row in the sequence's last block
-        const int rem = (int)(w.L - (long long)blk0 * kBS);
-        const int orow = (int)((w.L - 1) & (kBS - 1));
+        const int rem = (int)(s_work[k & 1].L - (long long)blk0 * kBS);
+        const int orow = (int)((s_work[k & 1].L - 1) & (kBS - 1));
         // Fused append: the last piece of (b, h) writes the new token's K/V
         // row (head h) to its pool slot and, since the block holding it may
         // have been copied before that write lands, patches the row into its
         // own copy of the sequence's last block.  Lane x < 16 carries 16-byte
         // chunk x of the K row, lane 16 + x chunk x of the V row.
-        const bool fuse = p.new_k != nullptr && w.split == w.nsplit - 1;
-        const bool patch = fuse && nloc > 0 && blk0 + nloc == w.nblk;
+        const bool fuse = p.new_k != nullptr && s_work[k & 1].split == s_work[k & 1].nsplit - 1;
+        const bool patch = fuse && nloc > 0 && blk0 + nloc == s_work[k & 1].nblk;
         if (fuse && warp == (patch ? (gbase + nloc - 1) % kNW : 0)) {
             const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
             const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
@@ -1094,9 +1235,11 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         }
         named_bar_sync(1, kNW * 32);
 
-        if constexpr (SCHED) w = s_work[k & 1];  // not overwritten before barrier 2
-        finish_partition<G, D>(p, sm_o, sm_m, sm_l, w.b, w.h, w.split, w.nsplit, w.pre, tid, s_mw,
-                               &s_flag, more);
+        // the piece is re-read here: the producer overwrites its slot only
+        // after barrier 2, inside finish_partition
+        finish_partition<G, D>(p, sm_o, sm_m, sm_l, s_work[k & 1].b, s_work[k & 1].h,
+                               s_work[k & 1].split, s_work[k & 1].nsplit, 0, tid, s_mw, &s_flag,
+                               more);
     }
 }
 
@@ -1309,9 +1452,9 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = a.sched ? (deep ? decode_tc_kernel<false, true, 8, 3> : decode_tc_kernel<false, true, 4, 5>)
-                  : deep ? (linear ? decode_tc_kernel<true, false, 8, 3> : decode_tc_kernel<false, false, 8, 3>)
-                         : (linear ? decode_tc_kernel<true, false, 4, 5> : decode_tc_kernel<false, false, 4, 5>);
+        auto fn = a.sched ? (deep ? decode_tc_sched_kernel<8, 3> : decode_tc_sched_kernel<4, 5>)
+                  : deep ? (linear ? decode_tc_kernel<true, 8, 3> : decode_tc_kernel<false, 8, 3>)
+                         : (linear ? decode_tc_kernel<true, 4, 5> : decode_tc_kernel<false, 4, 5>);
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
@@ -1450,9 +1593,10 @@ kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_block
 }
 
 kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
-                             int max_blocks, int num_sms, int32_t *schedule_out,
-                             size_t capacity_ints, size_t *used_ints) {
+                             int max_blocks, int num_sms, int num_ctas, int ring_stages,
+                             int32_t *schedule_out, size_t capacity_ints, size_t *used_ints) {
     if (!schedule_out || batch < 0 || num_kv_heads <= 0 || max_blocks < 0 || num_sms < 0 ||
+        num_ctas < 0 || (ring_stages != 0 && ring_stages != 4 && ring_stages != 8) ||
         (batch > 0 && !host_seq_lens))
         return KV_ERR_ARG;
     if (num_kv_heads > 0xffff) return KV_ERR_UNSUPPORTED;
@@ -1472,8 +1616,18 @@ kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv
     // grid-indexed plan found best) when every CTA gets at least
     // kTcDeepBlocks blocks, else the wide kernel at five CTAs per SM.
     const long long c_deep = (12LL * sms) / 5, c_wide = 5LL * sms;
-    long long W = (T + c_deep - 1) / c_deep;
-    if (W < kTcDeepBlocks) W = (T + c_wide - 1) / c_wide;
+    long long W;
+    if (num_ctas > 0) {  // the caller's CTA count
+        if (num_ctas > (ring_stages == 8 ? 3 : 5) * sms) return KV_ERR_ARG;  // one wave
+        W = (T + num_ctas - 1) / num_ctas;
+    } else if (ring_stages == 8) {
+        W = (T + c_deep - 1) / c_deep;
+    } else if (ring_stages == 4) {
+        W = (T + c_wide - 1) / c_wide;
+    } else {
+        W = (T + c_deep - 1) / c_deep;
+        if (W < kTcDeepBlocks) W = (T + c_wide - 1) / c_wide;
+    }
     // A pair of n blocks spans at most ceil(n / W) + 1 runs; keep that within
     // the merge done inside the kernel.
     const long long w_pairs = (nbmax + kFuseMaxSplits - 2) / (kFuseMaxSplits - 1);
@@ -1524,7 +1678,7 @@ kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv
     schedule_out[1] = np;
     schedule_out[2] = most;
     schedule_out[3] = (int32_t)W;
-    schedule_out[4] = W >= kTcDeepBlocks ? 1 : 0;
+    schedule_out[4] = ring_stages ? (ring_stages == 8 ? 1 : 0) : (W >= kTcDeepBlocks ? 1 : 0);
     schedule_out[5] = batch;
     schedule_out[6] = num_kv_heads;
     schedule_out[7] = 0;
