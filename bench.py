@@ -15,7 +15,7 @@ Metric: KV bytes read by decode attention per second (valid tokens only:
 sum_b L_b * 2 * Hkv * D * 2 bytes) -- "value" -- plus decode tokens/s.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--splits S] [--plan grid|balanced] [--prefix-splits P] [--impl reference]
+       [--splits S] [--plan auto|grid|balanced] [--prefix-splits P] [--impl reference]
 Under torchrun each rank runs an independent replica (weak scaling).
 Prints exactly one JSON line on stdout (rank 0).
 """
@@ -257,17 +257,19 @@ def run_ours(args, rank, world, local_rank):
     ws_bytes = pk.kv_decode_workspace_size(B, hq, hkv, d, max_blocks, splits)
     ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
     part_blocks, max_splits = pk.kv_decode_split_plan(B, hkv, max_blocks, splits)
-    balanced = not contig and args.plan == "balanced"
+    balanced = False
     if not contig:
         d_slots = torch.from_numpy(slots).cuda()
         # the grid takes the sequences longest first (one wave loads the SMs evenly)
         h_order = np.zeros(B, np.int32)
         pk.kv_decode_order(lens.astype(np.int32), h_order)
         d_order = torch.from_numpy(h_order).cuda()
+        # or: one wave of CTAs with equal runs of blocks (host-made schedule);
+        # "auto" takes it when its runs are long enough for the deep ring
+        h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks,
+                                        num_ctas=args.sched_ctas, ring_stages=args.sched_ring)
+        balanced = args.plan == "balanced" or (args.plan == "auto" and int(h_sched[4]) == 1)
         if balanced:
-            # or: one wave of CTAs with equal runs of blocks (host-made schedule)
-            h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks,
-                                            num_ctas=args.sched_ctas, ring_stages=args.sched_ring)
             d_sched = torch.from_numpy(h_sched).cuda()
             ws_bytes = pk.kv_decode_schedule_workspace_size(h_sched, hq, d)
             ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
@@ -398,6 +400,8 @@ def run_ours(args, rank, world, local_rank):
                       "paged_kv_cache_196_gb300/csrc/common.cuh")
     # bf16 / head_dim 128 with >= 3 query heads per kv head runs the tensor-core kernel
     kname = "decode_tc_kernel" if (hq // hkv >= 3 and d == 128) else "decode_kernel"
+    if balanced:
+        kname = "decode_tc_sched_kernel"
     traffic = recorded_traffic(kname, args.workload, src)
     line = {
         "metric": METRIC,
@@ -431,8 +435,9 @@ def run_ours(args, rank, world, local_rank):
         "decode_tokens_per_s": round(tokens_per_s, 1),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("contig_decode_attention" if contig else "paged_append_and_decode")
-                      + f" ({kname}" + ("" if contig or kname != "decode_tc_kernel" else
+            "kernel": ("contig_decode_attention" if contig else
+                       "paged_decode_attention_scheduled" if balanced else "paged_append_and_decode")
+                      + f" ({kname}" + ("" if contig or kname == "decode_kernel" else
                                          ", the append fused")
                       + (" + split merge kernel)" if max_splits > 32 else ")"),
             "achieved": round(achieved, 1),
@@ -964,8 +969,9 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_decode", choices=sorted(DESCR))
     ap.add_argument("--splits", type=int, default=0,
                     help="0 = plan from the host-known lengths (kv_decode_plan)")
-    ap.add_argument("--plan", default="grid", choices=["grid", "balanced"],
-                    help="paged decode: grid-indexed split plan or balanced schedule")
+    ap.add_argument("--plan", default="auto", choices=["auto", "grid", "balanced"],
+                    help="paged decode: grid-indexed split plan, balanced schedule, or auto "
+                         "(balanced when its runs take the deep ring: long contexts)")
     ap.add_argument("--sched-ctas", type=int, default=0,
                     help="balanced plan: CTAs (0 = kv_decode_schedule's rule)")
     ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],

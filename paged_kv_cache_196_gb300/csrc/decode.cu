@@ -977,9 +977,7 @@ struct TcPiece {
 };
 
 // Reads and checks piece pc of the schedule against the device lengths.  Only
-// the thread with report set records device errors.  PER: workspace slots a
-// piece fills (1, or one per consumer warp).
-template <int PER>
+// the thread with report set records device errors.
 KV_DEVICE TcPiece tc_piece(const DecodeKParams &p, int pc, bool report) {
     TcPiece w{};
     const int4 d = __ldg(p.sched_pieces + pc);
@@ -990,8 +988,7 @@ KV_DEVICE TcPiece tc_piece(const DecodeKParams &p, int pc, bool report) {
     w.nloc = d.w & 0xffff;
     w.nsplit = (int)((unsigned)d.w >> 16);
     if (w.b < 0 || w.b >= p.batch || w.h >= p.num_kv_heads || w.nsplit < 1 ||
-        w.split >= w.nsplit || w.nsplit * PER > p.max_splits || w.blk0 < 0 ||
-        w.nloc > p.part_blocks) {
+        w.split >= w.nsplit || w.nsplit > p.max_splits || w.blk0 < 0 || w.nloc > p.part_blocks) {
         if (report) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
         return w;
     }
@@ -1051,7 +1048,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     __shared__ int s_flag, s_abort;
 
     if (warp == kNW) {
-        const TcPiece w0 = tc_piece<1>(p, pc0, lane == 0);
+        const TcPiece w0 = tc_piece(p, pc0, lane == 0);
         if (lane == 0) {
             s_work[0] = w0;
             s_abort = 0;
@@ -1112,7 +1109,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             if (pc + 1 < pc1) {
                 // the next piece and its table slice, read while the consumers
                 // finish this one
-                const TcPiece nx = tc_piece<1>(p, pc + 1, lane == 0);
+                const TcPiece nx = tc_piece(p, pc + 1, lane == 0);
                 if (lane == 0) {
                     s_work[(k + 1) & 1] = nx;
                     if (stop) s_abort = 1;
@@ -1245,313 +1242,6 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                                s_work[k & 1].split, s_work[k & 1].nsplit, 0, tid, s_mw, &s_flag,
                                more);
     }
-}
-
-// Merges the nparts partial results of (sequence b, kv head h) left in the
-// workspace by the streaming decode: o = sum_s 2^(lse_s - M) o_s / sum_s
-// 2^(lse_s - M) in a fixed order, one warp, lanes over head_dim.
-KV_DEVICE void warp_merge_parts(const DecodeKParams &p, int b, int h, int nparts, int lane) {
-    constexpr int D = 128;
-    constexpr float kLn2 = 0.6931471805599453f;
-    for (int j = 0; j < p.g; ++j) {
-        const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
-        const float *ls = p.ws_lse + row * p.max_splits;
-        float M = -INFINITY;
-        for (int s = lane; s < nparts; s += 32) M = fmaxf(M, __ldcg(ls + s));
-#pragma unroll
-        for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-        float den = 0.f;
-        if (M != -INFINITY)
-            for (int s = lane; s < nparts; s += 32) den += exp2f(__ldcg(ls + s) - M);
-#pragma unroll
-        for (int x = 16; x >= 1; x >>= 1) den += __shfl_xor_sync(0xffffffffu, den, x);
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + row * p.max_splits * D) + lane;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < nparts; ++s) {
-            const float wgt = M == -INFINITY ? 0.f : exp2f(__ldcg(ls + s) - M) * inv;
-            const float4 v = __ldcg(src + (size_t)s * (D / 4));
-            acc.x += wgt * v.x;
-            acc.y += wgt * v.y;
-            acc.z += wgt * v.z;
-            acc.w += wgt * v.w;
-        }
-        if (p.out_bf16) {
-            uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + row * D + 4 * lane;
-            o[0] = float_to_bf16_rn(acc.x);
-            o[1] = float_to_bf16_rn(acc.y);
-            o[2] = float_to_bf16_rn(acc.z);
-            o[3] = float_to_bf16_rn(acc.w);
-        } else {
-            reinterpret_cast<float4 *>(p.out)[(row * D) / 4 + lane] = acc;
-        }
-        if (p.lse && lane == 0) p.lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
-    }
-}
-
-// decode_tc_sched_kernel without the cross-warp merge: every consumer warp
-// writes its own partial result for each piece (slot split * kNW + warp of the
-// pair), so no consumer waits for another and the producer never drains the
-// ring between pieces; the last of a pair's nsplit * kNW arrivals merges them
-// (one warp).  Piece descriptions reach the consumers through a two-slot ring
-// of their own (pfull / pempty).  Used with the wide ring, where a CTA's run
-// crosses pairs often and each drain would cost a memory round trip.
-template <int NST, int MINB>
-__global__ void __launch_bounds__(kDecodeThreads, MINB)
-    decode_tc_stream_kernel(const __grid_constant__ CUtensorMap pool_k_map,
-                            const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
-    constexpr int G = 8, D = 128;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pc0 = __ldg(p.sched_cta + blockIdx.x);
-    const int pc1 = __ldg(p.sched_cta + blockIdx.x + 1);
-    if (pc0 < 0 || pc1 < pc0 || pc1 > p.sched_npieces) {
-        if (tid == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-        return;
-    }
-    if (pc0 == pc1) return;
-
-    extern __shared__ __align__(1024) char smem_raw[];
-    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    char *stages = smem;  // NST x (K tile, V tile), swizzled
-    constexpr size_t kRing = decode_ring_bytes<D, G, true>(NST);
-    static_assert(NST % kNW == 0, "each stage must belong to one consumer warp");
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
-    uint64_t *empty = full + NST;
-    uint64_t *pfull = empty + NST;   // [2] a piece description is ready
-    uint64_t *pempty = pfull + 2;    // [2] every consumer warp has read it
-    int *stage_valid = reinterpret_cast<int *>(pempty + 2);
-    uint4 *newrow = reinterpret_cast<uint4 *>(stage_valid + NST);      // [kNW][32]: fused append rows
-    int32_t *tbl_buf = reinterpret_cast<int32_t *>(newrow + kNW * 32);  // [2][part_blocks]
-    __shared__ TcPiece s_work[2];  // published pieces
-    __shared__ TcPiece s_next;     // the producer's next piece, before it is published
-    __shared__ int s_abort;
-
-    if (warp == kNW && lane == 0) {
-        for (int st = 0; st < NST; ++st) {
-            mbar_init(&full[st], 1);
-            mbar_init(&empty[st], 32);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&pfull[s], 1);
-            mbar_init(&pempty[s], kNW);
-        }
-        s_abort = 0;
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    if (warp == kNW) {
-        const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(map_k) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
-        }
-        const uint64_t policy = l2_evict_first_policy();
-        // a piece into s_next and its table slice into tbl_buf[buf] (both
-        // read by this warp only)
-        auto fetch = [&](int pc, int buf) {
-            const TcPiece w = tc_piece<kNW>(p, pc, lane == 0);
-            if (w.run) {
-                const int32_t *row = p.tables + (size_t)w.b * p.max_blocks + w.blk0;
-                int32_t *t2 = tbl_buf + buf * p.part_blocks;
-                for (int i = lane; i < w.nloc; i += 32) t2[i] = __ldg(row + i);
-            }
-            if (lane == 0) s_next = w;
-            __syncwarp();
-        };
-        int gi = 0;  // tiles issued so far: ring position across pieces
-        bool stop = false;
-        fetch(pc0, 0);
-        for (int pc = pc0; pc < pc1; ++pc) {
-            const int k = pc - pc0, slot = k & 1;
-            if (lane == 0) {
-                // the slot is free once every consumer warp is done with piece k - 2
-                if (k >= 2 && !mbar_wait(&pempty[slot], ((k >> 1) - 1) & 1, p.err)) stop = true;
-                s_work[slot] = s_next;
-                if (stop) s_abort = 1;
-                mbar_arrive(&pfull[slot]);
-            }
-            __syncwarp();
-            stop = __shfl_sync(0xffffffffu, stop, 0);
-            const bool more = pc + 1 < pc1;
-            bool fetched = false;
-            const int32_t *tbl = tbl_buf + slot * p.part_blocks;
-            const int hh = s_work[slot].h;
-            const int n = (s_work[slot].run && !stop) ? s_work[slot].nloc : 0;
-            for (int i = 0; i < n; ++i) {
-                const int st = gi % NST, r = gi / NST;
-                bool bad = false;
-                if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
-                if (__shfl_sync(0xffffffffu, bad, 0)) {
-                    stop = true;
-                    if (lane == 0) s_abort = 1;
-                    break;
-                }
-                const int id = tbl[i];
-                const bool valid = id >= 0 && id < p.num_blocks;
-                const int y = ((valid ? id : 0) * p.num_kv_heads + hh) * kBS;
-                char *dst = stages + st * 2 * kTcTile;
-                if (lane == 0) {
-                    if (!valid) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
-                    stage_valid[st] = valid ? 1 : 0;
-                    if (valid)
-                        mbar_arrive_expect_tx(&full[st], 2 * kTcTile);
-                    else
-                        mbar_arrive(&full[st]);
-                }
-                // lane x issues box x: K half 0, K half 1, V half 0, V half 1
-                if (valid && lane < 4)
-                    mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
-                               lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
-                ++gi;
-                // with the ring full of this piece, read the next one
-                if (more && i == NST - 1) {
-                    fetch(pc + 1, slot ^ 1);
-                    fetched = true;
-                }
-            }
-            if (more && !fetched) fetch(pc + 1, slot ^ 1);
-        }
-        if (lane == 0)  // no copy may land after the CTA has exited
-            for (int st = 0; st < NST && st < gi; ++st)
-                mbar_wait(&full[st], ((gi - 1 - st) / NST) & 1, p.err);
-        return;
-    }
-
-    // ---- consumer warps, each on its own: lane = (g = lane / 4, t = lane % 4).
-    // A piece's description stays in its slot until every warp is done with
-    // the piece (pempty arrives at the end), so it is read from shared memory
-    // where needed rather than held in registers across the block loop.
-    const int g = lane >> 2, t = lane & 3;
-    const uint32_t stage_base = smem_addr(stages);
-    uint4 *nr = newrow + warp * 32;
-    int gbase = 0;  // ring position of this piece's first tile
-    for (int pc = pc0; pc < pc1; ++pc) {
-        const int k = pc - pc0, slot = k & 1;
-        const TcPiece *wp = &s_work[slot];
-        if (!mbar_wait(&pfull[slot], (k >> 1) & 1, p.err)) break;  // no description: stop
-        if (!wp->run) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[slot]);
-            continue;
-        }
-        const int nloc = wp->nloc;
-        // Fused append: the last piece of (b, h) writes the new token's K/V
-        // row (head h) to its pool slot and, since the block holding it may
-        // have been copied before that write lands, patches the row into its
-        // own copy of the sequence's last block.  Lane x < 16 carries 16-byte
-        // chunk x of the K row, lane 16 + x chunk x of the V row.
-        {
-            const bool fuse = p.new_k != nullptr && wp->split == wp->nsplit - 1;
-            const bool patch = fuse && nloc > 0 && wp->blk0 + nloc == wp->nblk;
-            if (fuse && warp == (patch ? (gbase + nloc - 1) % kNW : 0)) {
-                const int b = wp->b, h = wp->h;
-                const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
-                const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
-                nr[lane] = v;  // kept in shared memory until the last block arrives
-                const long long slot_id = p.new_slots[b];
-                if (slot_id >= 0 && slot_id < (long long)p.num_blocks * kBS) {
-                    const long long row = ((slot_id / kBS) * p.num_kv_heads + h) * kBS + slot_id % kBS;
-                    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
-                                 row * (D * 2 / 16) + (lane & 15);
-                    *dst = v;
-                } else if (slot_id >= 0 && lane == 0) {
-                    atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
-                }
-            }
-        }
-        // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
-        uint32_t qf[8][2];
-        {
-            const bool live = g < p.g;
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                reinterpret_cast<const uint16_t *>(p.q) +
-                ((size_t)wp->b * p.num_q_heads + wp->h * p.g + (live ? g : 0)) * D);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
-                qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
-            }
-        }
-        // tokens from this piece's first block on (at most nloc * 16)
-        const int rem = (int)(wp->L - (long long)wp->blk0 * kBS);
-        // running state for heads 2t, 2t+1 (replicated over g)
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        float o[8][4];
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-        if (!s_abort) {
-            for (int i = ((warp - gbase) % kNW + kNW) % kNW; i < nloc; i += kNW) {
-                const int gi = gbase + i, st = gi % NST, r = gi / NST;
-                if (!mbar_wait(&full[st], r & 1, p.err)) {
-                    s_abort = 1;
-                    break;
-                }
-                int ntok = min(kBS, rem - i * kBS);
-                if (!stage_valid[st]) ntok = 0;
-                const uint32_t kt = stage_base + st * 2 * kTcTile;
-                const uint32_t vt = kt + kTcTile;
-                if (i == nloc - 1 && ntok > 0 && p.new_k != nullptr && wp->split == wp->nsplit - 1 &&
-                    wp->blk0 + nloc == wp->nblk) {
-                    // the new token is row (L - 1) % 16 of the sequence's last block
-                    const int orow = (int)((wp->L - 1) & (kBS - 1)), c = lane & 15;
-                    char *tile = stages + st * 2 * kTcTile + (lane < 16 ? 0 : kTcTile);
-                    *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTcTile / 2) + orow * 128 +
-                                               (((c & 7) ^ (orow & 7)) << 4)) = nr[lane];
-                    __syncwarp();
-                }
-
-                tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
-                __syncwarp();
-                mbar_arrive(&empty[st]);
-            }
-        }
-        gbase += nloc;
-
-        // ---- this warp's partial result: sum over the 8 token lanes, then
-        // o / l and lse = m + log2 l for the live heads 2t, 2t + 1
-#pragma unroll
-        for (int x = 4; x <= 16; x <<= 1) {
-            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
-            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
-        }
-        const int b = wp->b, h = wp->h;
-        const int nparts = wp->nsplit * kNW, part = wp->split * kNW + warp;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[slot]);  // done with the description
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int j = 2 * t + c;
-            if (j < p.g) {
-                const float inv = l_run[c] > 0.f ? 1.f / l_run[c] : 0.f;
-                const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
-                float *dst = p.ws_o + (row * p.max_splits + part) * D;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    dst[16 * mt + g] = o[mt][c] * inv;
-                    dst[16 * mt + g + 8] = o[mt][c + 2] * inv;
-                }
-                if (g == 0)
-                    p.ws_lse[row * p.max_splits + part] =
-                        l_run[c] > 0.f ? m_run[c] + log2f(l_run[c]) : -INFINITY;
-            }
-        }
-        __threadfence();  // this lane's partial visible device-wide before the arrival
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(p.counters + (size_t)b * p.num_kv_heads + h, 1) == nparts - 1;
-        if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
-            warp_merge_parts(p, b, h, nparts, lane);
-            if (lane == 0) p.counters[(size_t)b * p.num_kv_heads + h] = 0;  // ready for the next call
-        }
-    }
-}
-
-static size_t decode_tc_stream_smem_bytes(int part_blocks, int nst) {
-    return 1024 + decode_ring_bytes<128, 8, true>(nst) + (2 * nst + 4) * sizeof(uint64_t) +
-           nst * sizeof(int) + kNW * 32 * sizeof(uint4) + 2 * (size_t)part_blocks * sizeof(int32_t);
 }
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst, int tables) {
@@ -1759,14 +1449,11 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         // Yi-6B shape, 384-512-block partitions: 6288 vs 5965 GB/s).
         const bool deep = a.sched ? a.sched_deep != 0 : pb >= kTcDeepBlocks;
         const int nst = deep ? 8 : 4;
-        // schedules: the deep ring merges inside the CTA; the wide one streams
-        // per-warp partial results (decode_tc_stream_kernel)
-        const size_t smem = a.sched && !deep ? decode_tc_stream_smem_bytes(pb, nst)
-                                             : decode_tc_smem_bytes(linear, pb, nst, a.sched ? 2 : 1);
+        const size_t smem = decode_tc_smem_bytes(linear, pb, nst, a.sched ? 2 : 1);
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = a.sched ? (deep ? decode_tc_sched_kernel<8, 3> : decode_tc_stream_kernel<4, 5>)
+        auto fn = a.sched ? (deep ? decode_tc_sched_kernel<8, 3> : decode_tc_sched_kernel<4, 5>)
                   : deep ? (linear ? decode_tc_kernel<true, 8, 3> : decode_tc_kernel<false, 8, 3>)
                          : (linear ? decode_tc_kernel<true, 4, 5> : decode_tc_kernel<false, 4, 5>);
         if (kv_status st0 = cuda_status(
@@ -1996,9 +1683,7 @@ kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv
     schedule_out[4] = deep;
     schedule_out[5] = batch;
     schedule_out[6] = num_kv_heads;
-    // partial results per (sequence, query head): one per piece (deep ring,
-    // merged inside the CTA), or one per piece and consumer warp (wide)
-    schedule_out[7] = deep ? most : kNW * most;
+    schedule_out[7] = most;  // partial results per (sequence, query head)
     if (used_ints) *used_ints = sched_piece_off((int)C) + 4 * (size_t)np;
     return KV_OK;
 }
@@ -2127,7 +1812,7 @@ kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const voi
     const int32_t *hs = host_schedule;
     if (hs[0] < 1 || hs[1] < 0 || hs[2] < 1 || hs[2] > kFuseMaxSplits || hs[3] < 1 ||
         hs[3] > kMaxPartBlocks || (hs[4] != 0 && hs[4] != 1) || hs[5] != batch ||
-        hs[6] != p->num_kv_heads || hs[7] != (hs[4] ? hs[2] : kNW * hs[2]))
+        hs[6] != p->num_kv_heads || hs[7] != hs[2])
         return KV_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(schedule) & 15) return KV_ERR_ARG;
     if (k_new && (!v_new || !slot_mapping)) return KV_ERR_ARG;

@@ -340,14 +340,10 @@ def test_decode_schedule_covers_every_block_once_in_equal_runs(case):
 def test_decode_schedule_workspace_and_limits():
     lens = np.full(3, 4096, np.int32)
     s = pk.kv_decode_schedule(lens, 8, 256, num_sms=152)
-    most, deep, slots = int(s[2]), int(s[4]), int(s[7])
-    # partial results per (sequence, query head): one per piece with the deep
-    # ring (merged inside the CTA), one per piece and consumer warp otherwise
-    assert slots == (most if deep else 4 * most)
+    most, slots = int(s[2]), int(s[7])
+    assert slots == most  # partial results per (sequence, query head): one per piece
     assert pk.kv_decode_schedule_workspace_size(s, 32, 128) == (
         0 if slots == 1 else 3 * 32 * slots * (128 + 1) * 4)
-    assert int(pk.kv_decode_schedule(lens, 8, 256, num_sms=152, ring_stages=8)[7]) == int(
-        pk.kv_decode_schedule(lens, 8, 256, num_sms=152, ring_stages=8)[2])
     # a sequence that would need more than 32 pieces of at most 1024 blocks
     with pytest.raises(pk.KVError) as e:
         pk.kv_decode_schedule(np.array([33 * 1024 * 16], np.int32), 1, 33 * 1024, num_sms=152)
