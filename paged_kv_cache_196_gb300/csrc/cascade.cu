@@ -158,6 +158,9 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                           const __grid_constant__ CUtensorMap tm_v, const CascadeParams p) {
     const int ps = blockIdx.x, h = blockIdx.y, grp = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the suffix decode, launched after this kernel, may start on the SM room
+    // this grid leaves (it waits for this grid only where it merges)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -772,7 +775,12 @@ kv_status paged_decode_attention_cascade(
     if (out_dtype != KV_F32 && out_dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
 
     // prefix first: its partial results must be in place before the suffix's
-    // merge reads them (same stream)
+    // merge reads them.  The suffix decode may overlap it (a programmatic
+    // dependent launch): its CTAs attend their own blocks meanwhile, and a
+    // merging CTA waits for the prefix grid before it reads the prefix slots.
+    // That needs every merge inside the decode kernel (fused merge).
+    const bool fused_merges = ps + ms <= kFuseMaxSplits &&
+                              (long long)batch * p->num_kv_heads <= kv_pool::kCounterSlots;
     if (num_groups > 0 && group_size > 0 && tiles > 0) {
         CascadeParams cp{};
         cp.q = static_cast<const uint16_t *>(q);
@@ -801,6 +809,7 @@ kv_status paged_decode_attention_cascade(
         const dim3 grid(ps, p->num_kv_heads, num_groups);
         fn<<<grid, kCsThreads, kCsSmemBytes, s>>>(p->tmap_k, p->tmap_v, cp);
         if (kv_status st1 = cuda_status(cudaGetLastError())) return st1;
+        a.overlap_previous = fused_merges;
     }
     return launch_decode(a, false);
 }

@@ -68,9 +68,6 @@ constexpr int kBS = 16;                  // tokens per block
 constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
 constexpr int kNStage = PKV_DECODE_STAGES;  // pipeline depth (a multiple of kNW)
 constexpr int kTcDeepBlocks = PKV_TC_DEEP_BLOCKS;
-// Splits per (sequence, kv head) merged inside the decode kernel by the last
-// CTA of that pair; longer plans leave the merge to merge_kernel.
-constexpr int kFuseMaxSplits = 32;
 // Balanced schedules (kv_decode_schedule), int32 words:
 //   [0] CTAs C, [1] pieces P, [2] most pieces of one (sequence, kv head),
 //   [3] most blocks of one CTA, [4] deep ring (1) or wide (0), [5] batch,
@@ -122,6 +119,10 @@ struct DecodeKParams {
     const int4 *sched_pieces;
     int sched_npieces;
     int batch;
+    // launched to overlap the previous kernel in the stream (the cascade's
+    // prefix kernel): no CTA exits before that kernel has completed, so
+    // nothing after this grid can start before it either
+    int overlap;
     void *out;
     int out_bf16;
     float *lse;
@@ -200,6 +201,12 @@ constexpr size_t decode_ring_bytes(int nstage = kNStage) {
 // Blocks of sequence b before this call's part of it: its first
 // start_tokens[b] tokens (clamped to [0, L], whole blocks) were attended by
 // the cascade's prefix kernel.
+// With p.overlap, holds the CTA (its thread 0) until the previous kernel in
+// the stream has completed.
+KV_DEVICE void overlap_exit(const DecodeKParams &p) {
+    if (p.overlap && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 KV_DEVICE int start_block(const DecodeKParams &p, int b, long long L) {
     if (!p.start_tokens) return 0;
     long long st = p.start_tokens[b];
@@ -269,6 +276,9 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
     named_bar_sync(1, kNW * 32);
     if (!*flag) return;
     __threadfence();
+    // The cascade's prefix kernel may still be running when this grid was
+    // launched to overlap it: its partial results are complete once it is.
+    if (pre > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     // split weights per head: 2^(lse_s - M) / sum
     for (int j = tid; j < p.g; j += kNW * 32) {
         const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
@@ -761,6 +771,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
     if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
         if (threadIdx.x == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_BLOCK_RANGE);
+        overlap_exit(p);
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -792,7 +803,10 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     const int sblk = start_block(p, b, L);
     const int pre = sblk > 0 ? p.part_base : 0;  // partial results of the cascade's prefix
     const int blk0 = sblk + split * p.part_blocks;
-    if (blk0 >= nblk && split > 0) return;  // nothing for this split (uniform across the CTA)
+    if (blk0 >= nblk && split > 0) {  // nothing for this split (uniform across the CTA)
+        overlap_exit(p);
+        return;
+    }
     const int nloc = max(0, min(p.part_blocks, nblk - blk0));
     const int nsplit = max(1, (nblk - sblk + p.part_blocks - 1) / p.part_blocks);
 
@@ -965,6 +979,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     float *mw = sm_l + kNW * G;  // merge weights, then a flag (still in the ring)
     finish_partition<G, D>(p, sm_o, sm_m, sm_l, b, h, split, nsplit, pre, tid, mw,
                            reinterpret_cast<int *>(mw + G * kFuseMaxSplits), false);
+    overlap_exit(p);
 }
 
 // One piece of a balanced schedule: blocks [blk0, blk0 + nloc) of kv head h
@@ -1417,6 +1432,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.new_slots = a.new_slots;
     kp.seq_order = a.seq_order;
     kp.batch = a.batch;
+    kp.overlap = a.overlap_previous ? 1 : 0;
     if (a.sched) {
         kp.sched_cta = a.sched + kSchedHeader;
         kp.sched_pieces = reinterpret_cast<const int4 *>(a.sched + sched_piece_off(a.sched_ctas));
@@ -1442,6 +1458,14 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
     // a schedule: paged tensor-core path, every merge inside the kernel
     if (a.sched && (!use_tc || linear || (slots > 1 && !kp.counters))) return KV_ERR_UNSUPPORTED;
+    // an overlapping launch: the grid-indexed tensor-core kernel, merges inside it
+    if (a.overlap_previous && (!use_tc || a.sched || (slots > kFuseMaxSplits) ||
+                               (slots > 1 && !kp.counters))) {
+        kp.overlap = 0;
+        DecodeArgs b2 = a;
+        b2.overlap_previous = false;
+        return launch_decode(b2, linear);
+    }
     if (use_tc) {
         // Long partitions: a deep ring (8 stages) and 3 CTAs per SM; short
         // ones: more CTAs at once (5 per SM) with 4 stages each.  Sweeps on
@@ -1459,8 +1483,23 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
-        fn<<<grid, kDecodeThreads, smem, a.stream>>>(mk, mv, kp);
-        st = cuda_status(cudaGetLastError());
+        if (a.overlap_previous) {
+            // may start while the previous kernel in the stream still runs
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(kDecodeThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = a.stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            st = cuda_status(cudaLaunchKernelEx(&cfg, fn, mk, mv, kp));
+        } else {
+            fn<<<grid, kDecodeThreads, smem, a.stream>>>(mk, mv, kp);
+            st = cuda_status(cudaGetLastError());
+        }
     } else if (a.head_dim == 128) {
         st = bf ? (linear ? launch_g<128, true, true>(G, kp, grid, a.stream)
                           : launch_g<128, true, false>(G, kp, grid, a.stream))

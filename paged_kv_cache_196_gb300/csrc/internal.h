@@ -104,6 +104,11 @@ struct DecodeArgs {
     // the header values read from the host copy
     const int32_t *sched;
     int sched_ctas, sched_pieces, sched_max_splits, sched_part_blocks, sched_deep;
+    // cascade suffix: the tensor-core decode may start while the prefix kernel
+    // (the previous launch in the stream) still runs; only its merges wait
+    // for that kernel (griddepcontrol.wait), and every merge must then be
+    // inside the decode kernel
+    bool overlap_previous;
     int *counters;
     long long counter_slots;
     void *workspace;
@@ -111,6 +116,10 @@ struct DecodeArgs {
     int *err;
     cudaStream_t stream;
 };
+
+// Splits per (sequence, kv head) merged inside the decode kernel by the last
+// CTA of that pair; longer plans leave the merge to merge_kernel.
+constexpr int kFuseMaxSplits = 32;
 
 void split_plan(int batch, int num_kv_heads, int max_blocks, int num_splits, int *part_blocks,
                 int *max_splits);
