@@ -220,6 +220,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- device state: the cache (paged pool or per-request virtual ranges)
     if not contig:
         pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+        if args.launch_overlap:
+            pk.kv_pool_set_launch_overlap(pool, True)
         kp, vp = pk.kv_pool_ptrs(pool)
         _fill(kp, torch.from_numpy(inp["pool_k"].view(np.int16)))
         _fill(vp, torch.from_numpy(inp["pool_v"].view(np.int16)))
@@ -474,6 +476,7 @@ def run_ours(args, rank, world, local_rank):
             "num_splits": splits,
             "part_blocks": part_blocks,
             "max_splits": max_splits,
+            "launch_overlap": bool(args.launch_overlap and not contig),
             "plan": ("balanced schedule: %d CTAs of %d blocks, %d-stage ring"
                      % (int(h_sched[0]), int(h_sched[3]), 8 if int(h_sched[4]) else 4)
                      if balanced else "grid-indexed" + ("" if contig else ", longest first")),
@@ -1037,6 +1040,8 @@ def main():
                     help="balanced plan: CTAs (0 = kv_decode_schedule's rule)")
     ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],
                     help="balanced plan: ring stages (0 = kv_decode_schedule's rule)")
+    ap.add_argument("--launch-overlap", action="store_true",
+                    help="paged decode: back-to-back launches may overlap (kv_pool_set_launch_overlap)")
     ap.add_argument("--prefix-splits", type=int, default=0,
                     help="shared-prefix step: key-range partitions of each group's prefix "
                          "(0 = kv_cascade_plan)")

@@ -209,6 +209,15 @@ kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool);
 /* The pool's allocator (borrowed; destroyed with the pool). */
 kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out);
 
+/* enable = 1: the tensor-core decode launches on this pool (paged decode,
+ * the fused decode step, the scheduled decode) may begin while the previous
+ * kernel in their stream is still running (a programmatic dependent launch);
+ * each waits for that kernel to complete before it reads or writes any
+ * memory, so results are unchanged and only the launch latency between
+ * back-to-back steps is hidden.  enable = 0 (the default): ordinary launches.
+ * Host only; takes effect from the next call. */
+kv_status kv_pool_set_launch_overlap(kv_pool_t p, int enable);
+
 /* Block manager calls on the pool's own allocator ("Makale Bulteni --
  * PagedAttention ve vLLM", "Iddia ve Gerceklik": blocks come from a free
  * pool on demand, are shared between sequences by reference and are copied

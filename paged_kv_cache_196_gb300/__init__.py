@@ -78,6 +78,7 @@ _SIGS = {
     "kv_pool_destroy": [_vp],
     "kv_pool_ptrs": [_vp, _P(_vp), _P(_vp)],
     "kv_pool_allocator": [_vp, _P(_vp)],
+    "kv_pool_set_launch_overlap": [_vp, _i32],
     "kv_alloc_blocks": [_vp, _i32, _vp],
     "kv_share_blocks": [_vp, _i32, _vp],
     "kv_free_blocks": [_vp, _i32, _vp],
@@ -317,6 +318,12 @@ def kv_pool_ptrs(p: int):
     k, v = _vp(), _vp()
     _check(lib().kv_pool_ptrs(p, ctypes.byref(k), ctypes.byref(v)), "kv_pool_ptrs")
     return k.value, v.value
+
+
+def kv_pool_set_launch_overlap(p: int, enable: bool):
+    """Let this pool's tensor-core decode launches overlap the previous kernel
+    in their stream (each waits for it before touching memory)."""
+    _check(lib().kv_pool_set_launch_overlap(p, 1 if enable else 0), "kv_pool_set_launch_overlap")
 
 
 def kv_pool_allocator(p: int) -> int:

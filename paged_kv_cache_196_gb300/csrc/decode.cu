@@ -123,6 +123,9 @@ struct DecodeKParams {
     // prefix kernel): no CTA exits before that kernel has completed, so
     // nothing after this grid can start before it either
     int overlap;
+    // launched to overlap the previous kernel in the stream: every CTA waits
+    // for it before touching memory, and lets the next launch begin at once
+    int chain;
     void *out;
     int out_bf16;
     float *lse;
@@ -201,6 +204,15 @@ constexpr size_t decode_ring_bytes(int nstage = kNStage) {
 // Blocks of sequence b before this call's part of it: its first
 // start_tokens[b] tokens (clamped to [0, L], whole blocks) were attended by
 // the cascade's prefix kernel.
+// With p.chain: lets the next launch in the stream begin, then waits for the
+// previous kernel to complete (its writes visible) before anything else.
+KV_DEVICE void chain_entry(const DecodeKParams &p) {
+    if (p.chain) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+}
+
 // With p.overlap, holds the CTA (its thread 0) until the previous kernel in
 // the stream has completed.
 KV_DEVICE void overlap_exit(const DecodeKParams &p) {
@@ -767,6 +779,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
     constexpr int G = 8, D = 128;
+    chain_entry(p);
     const int split = blockIdx.x, h = blockIdx.y;
     const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
     if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
@@ -1039,6 +1052,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_sched_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                            const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
     constexpr int G = 8, D = 128;
+    chain_entry(p);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pc0 = __ldg(p.sched_cta + blockIdx.x);
     const int pc1 = __ldg(p.sched_cta + blockIdx.x + 1);
@@ -1433,6 +1447,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     kp.seq_order = a.seq_order;
     kp.batch = a.batch;
     kp.overlap = a.overlap_previous ? 1 : 0;
+    kp.chain = a.chain && !a.overlap_previous ? 1 : 0;
     if (a.sched) {
         kp.sched_cta = a.sched + kSchedHeader;
         kp.sched_pieces = reinterpret_cast<const int4 *>(a.sched + sched_piece_off(a.sched_ctas));
@@ -1483,7 +1498,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
-        if (a.overlap_previous) {
+        if (a.overlap_previous || kp.chain) {
             // may start while the previous kernel in the stream still runs
             cudaLaunchConfig_t cfg{};
             cfg.gridDim = grid;
@@ -1773,6 +1788,7 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;
+    a.chain = p->launch_overlap;
     a.counters = p->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
@@ -1816,6 +1832,7 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;
+    a.chain = p->launch_overlap;
     a.counters = p->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
@@ -1879,6 +1896,7 @@ kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const voi
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.err = p->err;
+    a.chain = p->launch_overlap;
     a.counters = p->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);

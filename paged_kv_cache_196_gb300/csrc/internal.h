@@ -25,6 +25,9 @@ struct kv_pool {
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
     bool tmaps_ready = false;
+    // decode launches may overlap the previous kernel in the stream
+    // (kv_pool_set_launch_overlap)
+    bool launch_overlap = false;
 };
 
 namespace pkv {
@@ -109,6 +112,9 @@ struct DecodeArgs {
     // for that kernel (griddepcontrol.wait), and every merge must then be
     // inside the decode kernel
     bool overlap_previous;
+    // any decode: launched to overlap the previous kernel in the stream, the
+    // kernel waits for it (griddepcontrol.wait) before touching memory
+    bool chain;
     int *counters;
     long long counter_slots;
     void *workspace;

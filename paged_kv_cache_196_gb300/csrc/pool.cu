@@ -199,6 +199,12 @@ kv_status kv_pool_ptrs(kv_pool_t p, void **k_pool, void **v_pool) {
     return KV_OK;
 }
 
+kv_status kv_pool_set_launch_overlap(kv_pool_t p, int enable) {
+    if (!p || (enable != 0 && enable != 1)) return KV_ERR_ARG;
+    p->launch_overlap = enable != 0;
+    return KV_OK;
+}
+
 kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out) {
     if (!p || !out) return KV_ERR_ARG;
     *out = p->alloc;

@@ -106,3 +106,70 @@ def test_sequence_order_changes_no_result():
         b = _run(True, *case, splits=splits, order=order)
         for x, y in zip(a, b):
             np.testing.assert_array_equal(x.view(np.uint32) if x.dtype == np.float32 else x, y.view(np.uint32) if y.dtype == np.float32 else y)
+
+
+def test_launch_overlap_keeps_step_order():
+    """With kv_pool_set_launch_overlap, back-to-back decode steps may start
+    before the previous one has finished; each waits for it before touching
+    memory.  Two steps: the second attends the token the first appended (its
+    slot held NaN before), so a step that read early would show it.  Output,
+    lse and pool bytes bit-identical to ordinary launches, and the oracle."""
+    require_cuda()
+    g = W.rng(77)
+    hq, hkv, d = 32, 8, 128
+    lens2 = np.array([1025, 17, 300, 2000, 16, 47, 511, 1024], np.int32)  # after both steps
+    lens1 = lens2 - 1
+    nb = sum(oracle.blocks_needed(int(L), 16) for L in lens2) + 5
+    maxb = max(oracle.blocks_needed(int(L), 16) for L in lens2)
+    tables = oracle.build_block_tables(lens2, 16, W.permutation(g, nb), maxb)
+    pool_k = W.normal(g, (nb, hkv, 16, d), "bf16")
+    pool_v = W.normal(g, (nb, hkv, 16, d), "bf16")
+
+    def slot(b, pos):
+        return int(tables[b, pos // 16]) * 16 + pos % 16
+
+    s1 = np.array([slot(b, int(L) - 1) for b, L in enumerate(lens1)], np.int64)
+    s2 = np.array([slot(b, int(L) - 1) for b, L in enumerate(lens2)], np.int64)
+    for s in np.concatenate([s1, s2]):  # both new slots hold NaN before the steps
+        pool_k.view(np.uint16)[s // 16, :, s % 16, :] = W.NAN_BF16
+        pool_v.view(np.uint16)[s // 16, :, s % 16, :] = W.NAN_BF16
+    kn = [W.normal(g, (len(lens2), hkv, d), "bf16") for _ in range(2)]
+    vn = [W.normal(g, (len(lens2), hkv, d), "bf16") for _ in range(2)]
+    q = [W.normal(g, (len(lens2), hq, d), "bf16") for _ in range(2)]
+
+    def run(overlap):
+        pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+        pk.kv_pool_set_launch_overlap(pool, overlap)
+        kv, vv = pool_views(pool, nb, hkv, d, True)
+        kv.copy_(dev(pool_k))
+        vv.copy_(dev(pool_v))
+        B = len(lens2)
+        wsb = pk.kv_decode_workspace_size(B, hq, hkv, d, maxb, 0)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+        outs = [torch.empty((B, hq, d), dtype=torch.float32, device="cuda") for _ in range(2)]
+        lses = [torch.empty((B, hq), dtype=torch.float32, device="cuda") for _ in range(2)]
+        args = [(dev(q[i]), dev(kn[i]), dev(vn[i]), dev(s), dev(tables), maxb, dev(L))
+                for i, (s, L) in enumerate(((s1, lens1), (s2, lens2)))]
+        torch.cuda.synchronize()
+        for i in range(2):  # back to back on one stream
+            qq, kk, vvv, ss, tt, mb, ll = args[i]
+            pk.paged_append_and_decode(pool, qq, kk, vvv, ss, tt, mb, ll, B, hq, 1 / math.sqrt(d),
+                                       outs[i], pk.KV_F32, lses[i], 0, ws, wsb)
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error(pool) == 0
+        res = [host(o) for o in outs] + [host(x) for x in lses] + [host(kv, like_bf16=True),
+                                                                   host(vv, like_bf16=True)]
+        pk.kv_pool_destroy(pool)
+        return res
+
+    a, b = run(False), run(True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x.view(np.uint32) if x.dtype == np.float32 else x,
+                                      y.view(np.uint32) if y.dtype == np.float32 else y)
+    pk_, pv_ = pool_k.copy(), pool_v.copy()
+    oracle.append(pk_, pv_, kn[0], vn[0], s1)
+    oracle.append(pk_, pv_, kn[1], vn[1], s2)
+    np.testing.assert_array_equal(b[4], pk_)
+    ref, ref_lse = oracle.paged_decode(pk_, pv_, tables, lens2, q[1], 1 / math.sqrt(d))
+    assert_close_scaled(b[1], ref, 2e-3, "second step with launch overlap")
+    np.testing.assert_allclose(b[3], ref_lse, atol=1e-3)
