@@ -1040,8 +1040,9 @@ def main():
                     help="balanced plan: CTAs (0 = kv_decode_schedule's rule)")
     ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],
                     help="balanced plan: ring stages (0 = kv_decode_schedule's rule)")
-    ap.add_argument("--launch-overlap", action="store_true",
-                    help="paged decode: back-to-back launches may overlap (kv_pool_set_launch_overlap)")
+    ap.add_argument("--launch-overlap", action=argparse.BooleanOptionalAction, default=True,
+                    help="paged decode: back-to-back launches may overlap "
+                         "(kv_pool_set_launch_overlap; on by default)")
     ap.add_argument("--prefix-splits", type=int, default=0,
                     help="shared-prefix step: key-range partitions of each group's prefix "
                          "(0 = kv_cascade_plan)")
