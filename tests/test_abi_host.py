@@ -348,3 +348,11 @@ def test_decode_schedule_workspace_and_limits():
     with pytest.raises(pk.KVError) as e:
         pk.kv_decode_schedule(np.array([33 * 1024 * 16], np.int32), 1, 33 * 1024, num_sms=152)
     assert e.value.status == -3
+
+
+def test_pool_calls_reject_a_null_pool():
+    for call in (lambda: pk.kv_pool_set_launch_overlap(0, True),
+                 lambda: pk.kv_pool_allocator(0)):
+        with pytest.raises(pk.KVError) as e:
+            call()
+        assert e.value.status == -1
