@@ -269,7 +269,8 @@ def run_ours(args, rank, world, local_rank):
         # or: one wave of CTAs with equal runs of blocks (host-made schedule);
         # "auto" takes it when its runs are long enough for the deep ring
         h_sched = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks,
-                                        num_ctas=args.sched_ctas, ring_stages=args.sched_ring)
+                                        num_ctas=args.sched_ctas, ring_stages=args.sched_ring,
+                                        flags=pk.KV_SCHED_WHOLE_PIECES if args.sched_whole else 0)
         balanced = args.plan == "balanced" or (args.plan == "auto" and int(h_sched[4]) == 1)
         if balanced:
             d_sched = torch.from_numpy(h_sched).cuda()
@@ -477,8 +478,9 @@ def run_ours(args, rank, world, local_rank):
             "part_blocks": part_blocks,
             "max_splits": max_splits,
             "launch_overlap": bool(args.launch_overlap and not contig),
-            "plan": ("balanced schedule: %d CTAs of %d blocks, %d-stage ring"
-                     % (int(h_sched[0]), int(h_sched[3]), 8 if int(h_sched[4]) else 4)
+            "plan": ("balanced schedule%s: %d CTAs of up to %d blocks, %d-stage ring"
+                     % (" (whole pieces, longest first)" if args.sched_whole else "",
+                        int(h_sched[0]), int(h_sched[3]), 8 if int(h_sched[4]) else 4)
                      if balanced else "grid-indexed" + ("" if contig else ", longest first")),
             "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2); no flush",
@@ -1038,6 +1040,8 @@ def main():
                          "(balanced when its runs take the deep ring: long contexts)")
     ap.add_argument("--sched-ctas", type=int, default=0,
                     help="balanced plan: CTAs (0 = kv_decode_schedule's rule)")
+    ap.add_argument("--sched-whole", action="store_true",
+                    help="balanced plan: one piece per CTA (KV_SCHED_WHOLE_PIECES)")
     ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],
                     help="balanced plan: ring stages (0 = kv_decode_schedule's rule)")
     ap.add_argument("--launch-overlap", action=argparse.BooleanOptionalAction, default=True,

@@ -371,6 +371,11 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
  *                  5 per SM with 4 ring stages, 3 per SM with 8);
  *   ring_stages    0 = the rule above; else 4 (the wide kernel) or 8 (the
  *                  deep ring);
+ *   flags          0, or KV_SCHED_WHOLE_PIECES: instead of equal runs, each
+ *                  (sequence, kv head) is cut into ceil(n / W) pieces of
+ *                  near-equal length, one CTA per piece, the CTAs ordered
+ *                  longest piece first (no CTA streams two pieces; the grid
+ *                  is then a little more than one wave);
  *   schedule_out   host int32[capacity_ints]; *used_ints receives the words
  *                  written (the caller copies that many to the device).
  * Capacity: kv_decode_schedule_capacity's bound for this batch shape.  Host
@@ -378,8 +383,9 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
  * (more than 31 x 1024 blocks). */
 kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_blocks, int num_sms,
                                       size_t *ints);
+#define KV_SCHED_WHOLE_PIECES 1
 kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
-                             int max_blocks, int num_sms, int num_ctas, int ring_stages,
+                             int max_blocks, int num_sms, int num_ctas, int ring_stages, int flags,
                              int32_t *schedule_out, size_t capacity_ints, size_t *used_ints);
 /* Workspace bytes paged_decode_attention_scheduled needs with this schedule
  * (its host copy). */

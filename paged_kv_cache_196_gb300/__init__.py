@@ -97,7 +97,7 @@ _SIGS = {
                                 _vp, _i32, _vp, _i32, _vp, _sz, _vp],
     "kv_decode_order": [_vp, _i32, _vp],
     "kv_decode_schedule_capacity": [_i32, _i32, _i32, _i32, _P(_sz)],
-    "kv_decode_schedule": [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _P(_sz)],
+    "kv_decode_schedule": [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _P(_sz)],
     "kv_decode_schedule_workspace_size": [_vp, _i32, _i32, _P(_sz)],
     "paged_decode_attention_scheduled": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32,
                                          _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
@@ -445,8 +445,11 @@ def kv_decode_schedule_capacity(batch: int, num_kv_heads: int, max_blocks: int,
     return r.value
 
 
+KV_SCHED_WHOLE_PIECES = 1
+
+
 def kv_decode_schedule(host_seq_lens, num_kv_heads: int, max_blocks: int, num_sms: int = 0,
-                       num_ctas: int = 0, ring_stages: int = 0):
+                       num_ctas: int = 0, ring_stages: int = 0, flags: int = 0):
     """Balanced decode schedule for these host int32 lengths: an int32 numpy
     array (header, first piece of each CTA, pieces) to copy to the device for
     paged_decode_attention_scheduled.  num_sms = 0: the current device's;
@@ -457,7 +460,7 @@ def kv_decode_schedule(host_seq_lens, num_kv_heads: int, max_blocks: int, num_sm
     out = _np.zeros(cap, _np.int32)
     used = _sz()
     _check(lib().kv_decode_schedule(_ptr(lens), len(lens), num_kv_heads, max_blocks, num_sms,
-                                    num_ctas, ring_stages, _ptr(out), cap, ctypes.byref(used)),
+                                    num_ctas, ring_stages, flags, _ptr(out), cap, ctypes.byref(used)),
            "kv_decode_schedule")
     return out[:used.value].copy()
 

@@ -1642,17 +1642,18 @@ kv_status kv_decode_schedule_capacity(int batch, int num_kv_heads, int max_block
     long long c = 5LL * sched_sms(num_sms);
     const long long c_long = (total + kMaxPartBlocks - 1) / kMaxPartBlocks;
     if (c_long > c) c = c_long;
+    c += (long long)batch * num_kv_heads;  // whole pieces: up to one more CTA per pair
     if (c > (1LL << 30)) return KV_ERR_UNSUPPORTED;
     *ints = sched_piece_off((int)c) + 4 * (size_t)(c + (long long)batch * num_kv_heads);
     return KV_OK;
 }
 
 kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv_heads,
-                             int max_blocks, int num_sms, int num_ctas, int ring_stages,
+                             int max_blocks, int num_sms, int num_ctas, int ring_stages, int flags,
                              int32_t *schedule_out, size_t capacity_ints, size_t *used_ints) {
     if (!schedule_out || batch < 0 || num_kv_heads <= 0 || max_blocks < 0 || num_sms < 0 ||
         num_ctas < 0 || (ring_stages != 0 && ring_stages != 4 && ring_stages != 8) ||
-        (batch > 0 && !host_seq_lens))
+        (flags & ~KV_SCHED_WHOLE_PIECES) || (batch > 0 && !host_seq_lens))
         return KV_ERR_ARG;
     if (num_kv_heads > 0xffff) return KV_ERR_UNSUPPORTED;
     const int sms = sched_sms(num_sms);
@@ -1696,6 +1697,55 @@ kv_status kv_decode_schedule(const int32_t *host_seq_lens, int batch, int num_kv
     if (used_ints) *used_ints = need;
     if (capacity_ints < need) return KV_ERR_ARG;
 
+    if (flags & KV_SCHED_WHOLE_PIECES) {
+        // Each pair cut into ceil(n / W) pieces of near-equal length, one CTA
+        // per piece, CTAs ordered longest piece first: the in-order dispatch
+        // of the grid then does longest-first list scheduling over slightly
+        // more than one wave, and no CTA streams more than one piece.
+        struct Pc { int b, h, split, ns, blk0, n; };
+        std::vector<Pc> all;
+        int most_w = 1, longest = 1;
+        for (int b = 0; b < batch; ++b) {
+            const int n = nb[b];
+            const int ns = n == 0 ? 1 : (int)((n + W - 1) / W);
+            if (ns > most_w) most_w = ns;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                int blk0 = 0;
+                for (int sp = 0; sp < ns; ++sp) {
+                    const int len = n / ns + (sp < n % ns ? 1 : 0);
+                    all.push_back({b, h, sp, ns, blk0, len});
+                    if (len > longest) longest = len;
+                    blk0 += len;
+                }
+            }
+        }
+        if (most_w > kFuseMaxSplits) return KV_ERR_UNSUPPORTED;
+        std::stable_sort(all.begin(), all.end(), [](const Pc &x, const Pc &y) { return x.n > y.n; });
+        const long long Cw = std::max<long long>(1, (long long)all.size());
+        const size_t need_w = sched_piece_off((int)Cw) + 4 * (size_t)all.size();
+        if (used_ints) *used_ints = need_w;
+        if (capacity_ints < need_w) return KV_ERR_ARG;
+        int32_t *cta_w = schedule_out + kSchedHeader;
+        int32_t *pcs_w = schedule_out + sched_piece_off((int)Cw);
+        for (long long c = 0; c <= Cw; ++c) cta_w[c] = (int32_t)std::min<long long>(c, all.size());
+        for (size_t i = 0; i < all.size(); ++i) {
+            int32_t *q = pcs_w + 4 * i;
+            q[0] = all[i].b;
+            q[1] = all[i].h | (all[i].split << 16);
+            q[2] = all[i].blk0;
+            q[3] = all[i].n | (all[i].ns << 16);
+        }
+        const int deep_w = ring_stages ? (ring_stages == 8 ? 1 : 0) : (W >= kTcDeepBlocks ? 1 : 0);
+        schedule_out[0] = (int32_t)Cw;
+        schedule_out[1] = (int32_t)all.size();
+        schedule_out[2] = most_w;
+        schedule_out[3] = longest;
+        schedule_out[4] = deep_w;
+        schedule_out[5] = batch;
+        schedule_out[6] = num_kv_heads;
+        schedule_out[7] = most_w;
+        return KV_OK;
+    }
     int32_t *cta = schedule_out + kSchedHeader;
     int32_t *pcs = schedule_out + sched_piece_off((int)C);
     long long pos = 0, next_cta = 0;

@@ -356,3 +356,39 @@ def test_pool_calls_reject_a_null_pool():
         with pytest.raises(pk.KVError) as e:
             call()
         assert e.value.status == -1
+
+
+@pytest.mark.parametrize("case", ["llama", "yi", "ragged"])
+def test_decode_schedule_whole_pieces(case):
+    """KV_SCHED_WHOLE_PIECES: every pair cut into near-equal pieces (lengths
+    differ by at most one block), one piece per CTA, CTAs longest first."""
+    g = W.rng(4041)
+    hkv, max_blocks = 8, 256
+    if case == "llama":
+        lens = W.decode_lengths("llama3_8b_decode") + 1
+    elif case == "yi":
+        lens, hkv, max_blocks = W.decode_lengths("yi6b_long_decode"), 4, 12288
+    else:
+        lens = np.concatenate([[0, 1, 15, 16, 17, 4096, 0], g.integers(1, 4096, 40)])
+    lens = np.asarray(lens, np.int32)
+    s = _parse_schedule(pk.kv_decode_schedule(lens, hkv, max_blocks, num_sms=152,
+                                              flags=pk.KV_SCHED_WHOLE_PIECES))
+    nb = -(-lens.astype(np.int64) // 16)
+    assert s["C"] == s["P"] and list(s["cta"]) == list(range(s["C"] + 1))
+    n = [q["n"] for q in s["pieces"]]
+    assert n == sorted(n, reverse=True) and max(n) == s["W"]
+    seen = {}
+    for q in s["pieces"]:
+        seen.setdefault((q["b"], q["h"]), []).append(q)
+    assert len(seen) == len(lens) * hkv
+    for (b, h), qs in seen.items():
+        qs.sort(key=lambda q: q["split"])
+        ns = qs[0]["ns"]
+        assert [q["split"] for q in qs] == list(range(ns)) and ns <= 32
+        pos = 0
+        for q in qs:
+            assert q["blk0"] == pos
+            pos += q["n"]
+        assert pos == nb[b]
+        assert max(q["n"] for q in qs) - min(q["n"] for q in qs) <= 1
+    assert s["most"] == max(q["ns"] for q in s["pieces"])

@@ -23,11 +23,11 @@ from test_gpu_decode import TOL, _full_decode_case, _sample_items, random_case
 pytestmark = pytest.mark.gpu
 
 
-def _sched_run(case, num_sms, lens_dev=None, expect_err=0, step=None):
+def _sched_run(case, num_sms, lens_dev=None, expect_err=0, flags=0):
     """Scheduled decode of a test_gpu_decode Case (no append)."""
     hq, hkv, d = case.hq, case.hkv, case.d
     maxb = case.tables.shape[1]
-    s = pk.kv_decode_schedule(case.lens, hkv, maxb, num_sms)
+    s = pk.kv_decode_schedule(case.lens, hkv, maxb, num_sms, flags=flags)
     wsb = pk.kv_decode_schedule_workspace_size(s, hq, d)
     ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
     out = torch.empty((case.B, hq, d), dtype=torch.float32, device="cuda")
@@ -66,6 +66,22 @@ def test_scheduled_decode_matches_oracle(num_sms):
     # and the grid-indexed decode, within rounding
     g_out, g_lse = c.run(0)
     assert_close_scaled(out, g_out, 1e-5, "scheduled vs grid-indexed")
+    c.close()
+
+
+@pytest.mark.parametrize("num_sms", [0, 3])
+def test_whole_piece_schedule_matches_oracle(num_sms):
+    """One piece per CTA, pieces of near-equal length, longest first."""
+    require_cuda()
+    lens = [1, 16, 17, 33, 300, 511, 1024, 1025, 2000, 47, 0, 4096, 5]
+    c = random_case(lens, 32, 8, 128, "bf16", seed=730 + num_sms)
+    out, lse, s = _sched_run(c, num_sms, flags=pk.KV_SCHED_WHOLE_PIECES)
+    assert s[0] == s[1]  # one piece per CTA
+    ref, ref_lse = c.oracle()
+    assert_close_scaled(out, ref, TOL["bf16"], "whole-piece schedule")
+    live = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[live], ref_lse[live], atol=1e-3)
+    assert np.all(out[10] == 0) and np.all(np.isneginf(lse[10]))
     c.close()
 
 
