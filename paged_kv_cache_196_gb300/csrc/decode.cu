@@ -688,12 +688,25 @@ KV_DEVICE void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *
 
 constexpr int kTcTile = 16 * 128 * 2;  // one (block, head) tile: 4 KiB, two 2 KiB swizzled halves
 
+// The Q^T fragment of k-step kk for this lane: held in registers, or staged
+// in shared memory as [kk][lane] pairs of words (one copy for all warps).
+KV_DEVICE void q_fragment(const uint32_t (&qf)[8][2], int kk, int, uint32_t &q0, uint32_t &q1) {
+    q0 = qf[kk][0];
+    q1 = qf[kk][1];
+}
+KV_DEVICE void q_fragment(const uint2 *qs, int kk, int lane, uint32_t &q0, uint32_t &q1) {
+    const uint2 v = qs[kk * 32 + lane];
+    q0 = v.x;
+    q1 = v.y;
+}
+
 // One 16-token block for the 8 (padded) query heads of a warp: S^T = K Q^T
 // on mma.sync, online softmax in the log2 domain, O^T += V^T P^T with P split
 // into bf16 hi + lo parts.  kt / vt: shared addresses of the block's swizzled
 // K and V tiles; ntok: valid tokens in the block (the rest are masked, their V
 // lanes zeroed).  State (m_run, l_run, o) is this lane's share.
-KV_DEVICE void tc_attend_block(const uint32_t (&qf)[8][2], uint32_t kt, uint32_t vt, int ntok,
+template <typename QF>
+KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
                                float scale_log2, int lane, float (&m_run)[2], float (&l_run)[2],
                                float (&o)[8][4]) {
     const int g = lane >> 2, t = lane & 3;
@@ -708,7 +721,9 @@ KV_DEVICE void tc_attend_block(const uint32_t (&qf)[8][2], uint32_t kt, uint32_t
         const uint32_t addr = kt + (kk >> 2) * (kTcTile / 2) + rowA * 128 + ((chunk ^ (rowA & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         mma::ldsm_x4(addr, a0, a1, a2, a3);
-        mma::mma_bf16(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        uint32_t q0, q1;
+        q_fragment(qf, kk, lane, q0, q1);
+        mma::mma_bf16(c, a0, a1, a2, a3, q0, q1);
     }
     // c0,c1: token g, heads 2t,2t+1; c2,c3: token g+8
     const bool v0 = g < ntok, v1 = g + 8 < ntok;
@@ -923,18 +938,21 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
         }
     }
-    // Q^T fragments for the 8 k-steps: head g, dims 16kk + 2t (+1) and +8 (+9).
-    uint32_t qf[8][2];
-    {
+    // Q^T fragments for the 8 k-steps (head g, dims 16kk + 2t (+1) and +8
+    // (+9)), staged once in shared memory by warp 0 and read per block: held
+    // in registers they cost the 4-stage instantiation spills at its
+    // 72-register budget.
+    __shared__ uint2 s_q[8 * 32];
+    if (warp == 0) {
         const bool live = g < p.g;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
             reinterpret_cast<const uint16_t *>(p.q) + ((size_t)b * p.num_q_heads + h * p.g + (live ? g : 0)) * D);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            qf[kk][0] = live ? __ldg(qrow + 8 * kk + t) : 0u;
-            qf[kk][1] = live ? __ldg(qrow + 8 * kk + 4 + t) : 0u;
-        }
+        for (int kk = 0; kk < 8; ++kk)
+            s_q[kk * 32 + lane] = make_uint2(live ? __ldg(qrow + 8 * kk + t) : 0u,
+                                             live ? __ldg(qrow + 8 * kk + 4 + t) : 0u);
     }
+    named_bar_sync(1, kNW * 32);
     // running state for heads 2t, 2t+1 (replicated over g)
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[8][4];
@@ -959,7 +977,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             __syncwarp();
         }
 
-        tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
+        tc_attend_block(s_q, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
         __syncwarp();
         mbar_arrive(&empty[st]);
     }
