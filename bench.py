@@ -229,6 +229,8 @@ def run_ours(args, rank, world, local_rank):
         slots = tables[np.arange(B), last // 16].astype(np.int64) * 16 + last % 16
     else:
         ctx = pk.kv_contig_create(B, cfg["len_hi"], hkv, d, pk.KV_BF16)
+        if args.launch_overlap:
+            pk.kv_contig_set_launch_overlap(ctx, True)
         t0 = time.time()
         for b, L in enumerate(lens):
             pk.kv_contig_reserve(ctx, b)
@@ -477,7 +479,7 @@ def run_ours(args, rank, world, local_rank):
             "num_splits": splits,
             "part_blocks": part_blocks,
             "max_splits": max_splits,
-            "launch_overlap": bool(args.launch_overlap and not contig),
+            "launch_overlap": bool(args.launch_overlap),
             "plan": ("balanced schedule%s: %d CTAs of up to %d blocks, %d-stage ring"
                      % (" (whole pieces, longest first)" if args.sched_whole else "",
                         int(h_sched[0]), int(h_sched[3]), 8 if int(h_sched[4]) else 4)
@@ -1045,8 +1047,8 @@ def main():
     ap.add_argument("--sched-ring", type=int, default=0, choices=[0, 4, 8],
                     help="balanced plan: ring stages (0 = kv_decode_schedule's rule)")
     ap.add_argument("--launch-overlap", action=argparse.BooleanOptionalAction, default=True,
-                    help="paged decode: back-to-back launches may overlap "
-                         "(kv_pool_set_launch_overlap; on by default)")
+                    help="decode: back-to-back launches may overlap (kv_pool_set_launch_overlap, "
+                         "kv_contig_set_launch_overlap; on by default)")
     ap.add_argument("--prefix-splits", type=int, default=0,
                     help="shared-prefix step: key-range partitions of each group's prefix "
                          "(0 = kv_cascade_plan)")

@@ -605,6 +605,12 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
 
 kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream);
 
+/* As kv_pool_set_launch_overlap for a contiguous context: kv_contig_append and
+ * the tensor-core contig_decode_attention may begin while the previous kernel
+ * in their stream still runs, and wait for it before touching memory.  Off by
+ * default.  Host only. */
+kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable);
+
 #ifdef __cplusplus
 }
 #endif

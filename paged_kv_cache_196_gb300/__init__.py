@@ -126,6 +126,7 @@ _SIGS = {
     "contig_decode_attention": [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32, _vp,
                                 _sz, _vp],
     "kv_contig_get_device_error": [_vp, _P(_i32), _vp],
+    "kv_contig_set_launch_overlap": [_vp, _i32],
 }
 _RESTYPE = {"kv_status_string": ctypes.c_char_p, "kv_last_cuda_error": ctypes.c_char_p}
 
@@ -622,6 +623,12 @@ def contig_decode_attention(c: int, q, req_ids, seq_lens, batch: int, num_q_head
                                          num_splits, _ptr(workspace), workspace_bytes,
                                          _stream(stream)),
            "contig_decode_attention")
+
+
+def kv_contig_set_launch_overlap(c: int, enable: bool):
+    """Let this context's appends and decodes overlap the previous kernel in
+    their stream (each waits for it before touching memory)."""
+    _check(lib().kv_contig_set_launch_overlap(c, 1 if enable else 0), "kv_contig_set_launch_overlap")
 
 
 def kv_contig_get_device_error(c: int, stream=None) -> int:

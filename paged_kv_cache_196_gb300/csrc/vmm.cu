@@ -74,7 +74,11 @@ __global__ void __launch_bounds__(256) contig_append_kernel(
     const long long *__restrict__ mapped, const uint4 *__restrict__ k_new,
     const uint4 *__restrict__ v_new, const int32_t *__restrict__ req_ids,
     const int32_t *__restrict__ positions, long long total_chunks, int hkv, int row_chunks,
-    long long head_stride, int max_requests, int *err) {
+    long long head_stride, int max_requests, int *err, int chain) {
+    if (chain) {  // an overlapping launch: let the next one begin, wait for the previous
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     const int per_token = hkv * row_chunks;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total_chunks;
          i += (long long)gridDim.x * blockDim.x) {
@@ -140,6 +144,9 @@ struct kv_contig {
         double map_ns = 0, unmap_ns = 0;
         long long maps = 0, unmaps = 0;
     } pp;
+    // appends and decodes may overlap the previous kernel in the stream
+    // (kv_contig_set_launch_overlap)
+    bool launch_overlap = false;
 };
 
 static CUmemAllocationProp page_prop(int device) {
@@ -503,9 +510,25 @@ kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)sm_count() * 16;
     if (blocks > cap) blocks = cap;
+    if (c->launch_overlap) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = as_stream(stream);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cuda_status(cudaLaunchKernelEx(
+            &cfg, contig_append_kernel, (const unsigned long long *)c->d_kbase,
+            (const unsigned long long *)c->d_vbase, (const long long *)c->d_mapped,
+            (const uint4 *)k_new, (const uint4 *)v_new, req_ids, positions, total, c->hkv, row_chunks,
+            c->head_stride, c->max_requests, c->err, 1));
+    }
     contig_append_kernel<<<(int)blocks, 256, 0, as_stream(stream)>>>(
         c->d_kbase, c->d_vbase, c->d_mapped, (const uint4 *)k_new, (const uint4 *)v_new, req_ids,
-        positions, total, c->hkv, row_chunks, c->head_stride, c->max_requests, c->err);
+        positions, total, c->hkv, row_chunks, c->head_stride, c->max_requests, c->err, 0);
     return cuda_status(cudaGetLastError());
 }
 
@@ -542,7 +565,14 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
     a.counters = c->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
+    a.chain = c->launch_overlap;
     return launch_decode(a, true);
+}
+
+kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable) {
+    if (!c || (enable != 0 && enable != 1)) return KV_ERR_ARG;
+    c->launch_overlap = enable != 0;
+    return KV_OK;
 }
 
 kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream) {

@@ -196,3 +196,57 @@ def test_page_pool_prefetches_and_recycles_pages():
     pk.kv_contig_page_pool(ctx, 0, 0)                      # stop the thread, drop spare pages
     assert pk.kv_contig_page_stats(ctx)["spare"] == 0
     pk.kv_contig_destroy(ctx)
+
+
+def test_contig_launch_overlap_keeps_step_order():
+    """kv_contig_set_launch_overlap: two append + decode steps back to back on
+    one stream (the second step attends the token the first appended);
+    outputs bit-identical to ordinary launches, and the oracle."""
+    require_cuda()
+    lens = [35, 17, 300, 777, 64, 1]
+    B, hq, hkv, d = len(lens), 32, 4, 128
+    g = W.rng(45)
+    kn = [W.normal(g, (B, hkv, d), "bf16") for _ in range(2)]
+    vn = [W.normal(g, (B, hkv, d), "bf16") for _ in range(2)]
+    res = []
+    for overlap in (False, True):
+        c = ContigCase(lens, 800, hq=hq, hkv=hkv, d=d, dtype="bf16", seed=44)
+        pk.kv_contig_set_launch_overlap(c.ctx, overlap)
+        for b, L in enumerate(lens):
+            pk.kv_contig_ensure(c.ctx, int(c.req[b]), int(L) + 2)
+        maxb = -(-c.max_tokens // 16)
+        wsb = pk.kv_decode_workspace_size(B, hq, hkv, d, maxb, 0)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+        args = [(dev(kn[i]), dev(vn[i]), dev(c.req), dev((c.lens + i).astype(np.int32)),
+                 dev(c.q), dev((c.lens + i + 1).astype(np.int32))) for i in range(2)]
+        outs = [torch.empty((B, hq, d), dtype=torch.float32, device="cuda") for _ in range(2)]
+        lses = [torch.empty((B, hq), dtype=torch.float32, device="cuda") for _ in range(2)]
+        torch.cuda.synchronize()
+        for i in range(2):  # back to back, nothing else in the stream between the launches
+            k_, v_, req, pos, q, ln = args[i]
+            pk.kv_contig_append(c.ctx, k_, v_, req, pos, B)
+            pk.contig_decode_attention(c.ctx, q, req, ln, B, hq, 1 / math.sqrt(d), outs[i],
+                                       pk.KV_F32, lses[i], 0, ws, wsb)
+        torch.cuda.synchronize()
+        assert pk.kv_contig_get_device_error(c.ctx) == 0
+        res.append([host(o) for o in outs] + [host(x) for x in lses])
+        q_case = c.q
+        K2 = [np.concatenate([c.K[b], kn[0][b:b + 1], kn[1][b:b + 1]]) for b in range(B)]
+        V2 = [np.concatenate([c.V[b], vn[0][b:b + 1], vn[1][b:b + 1]]) for b in range(B)]
+        c.close()
+    for x, y in zip(res[0], res[1]):
+        np.testing.assert_array_equal(x.view(np.uint32), y.view(np.uint32))
+    # the oracle's linear-layout decode over each request's content after both steps
+    n = int(max(lens)) + 2
+    kb, vb = [], []
+    for k, v in zip(K2, V2):
+        kp = np.zeros((hkv, n, d), k.dtype)
+        vp = np.zeros((hkv, n, d), v.dtype)
+        kp[:, :len(k)] = k.transpose(1, 0, 2)
+        vp[:, :len(v)] = v.transpose(1, 0, 2)
+        kb.append(kp)
+        vb.append(vp)
+    lens2 = np.asarray(lens, np.int32) + 2
+    ref, ref_lse = oracle.linear_decode(kb, vb, np.arange(B), lens2, q_case, 1 / math.sqrt(d))
+    assert_close_scaled(res[1][1], ref, 2e-3, "second contiguous step with launch overlap")
+    np.testing.assert_allclose(res[1][3], ref_lse, atol=1e-3)
