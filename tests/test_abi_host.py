@@ -392,3 +392,20 @@ def test_decode_schedule_whole_pieces(case):
         assert pos == nb[b]
         assert max(q["n"] for q in qs) - min(q["n"] for q in qs) <= 1
     assert s["most"] == max(q["ns"] for q in s["pieces"])
+
+
+def test_decode_schedule_arguments():
+    lens = np.array([4096, 100, 17], np.int32)
+    # a forced CTA count must fit one wave: 5 per SM (4 stages) or 3 per SM (8 stages)
+    s = _parse_schedule(pk.kv_decode_schedule(lens, 8, 256, num_sms=4, num_ctas=20, ring_stages=4))
+    assert s["C"] <= 20 and s["deep"] == 0
+    s = _parse_schedule(pk.kv_decode_schedule(lens, 8, 256, num_sms=4, num_ctas=12, ring_stages=8))
+    assert s["C"] <= 12 and s["deep"] == 1
+    for kw in (dict(num_ctas=21, ring_stages=4), dict(num_ctas=13, ring_stages=8),
+               dict(ring_stages=6), dict(flags=2), dict(num_ctas=-1)):
+        with pytest.raises(pk.KVError) as e:
+            pk.kv_decode_schedule(lens, 8, 256, num_sms=4, **kw)
+        assert e.value.status == -1, kw
+    # lengths past the table width are clamped to it (the device flags them)
+    s = _parse_schedule(pk.kv_decode_schedule(np.array([10**6], np.int32), 1, 64, num_sms=4))
+    assert sum(q["n"] for q in s["pieces"]) == 64
