@@ -25,6 +25,11 @@
  *     range, a pipeline wait that timed out) skip the offending element, let
  *     the kernel finish, and set bits in a device error word that
  *     kv_get_device_error / kv_contig_get_device_error read and clear.
+ *   - A pool or contiguous context lives on the device that was current
+ *     when it was created.  Every call that launches work or copies memory
+ *     for it checks that this device is current; a call made while another
+ *     device is current returns KV_ERR_ARG and launches nothing.  The
+ *     destroy calls switch to the object's device to free it and switch back.
  *   - Element types: KV_F32 (IEEE fp32) or KV_BF16 (bfloat16).  q, k_new and
  *     v_new use the pool's type; out may be KV_F32 or the pool's type.
  *   - head_dim must be 64 or 128, block_size must be 16, num_q_heads must be

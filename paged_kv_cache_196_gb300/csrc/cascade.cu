@@ -44,10 +44,6 @@
 #include "internal.h"
 #include "tc.cuh"
 
-#ifndef PKV_TMA_MULTILANE
-#define PKV_TMA_MULTILANE 1  // the boxes of a K/V tile are issued by eight lanes
-#endif
-
 namespace pkv {
 namespace {
 
@@ -284,24 +280,11 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             char *dst = ring + s * kCsTileBytes;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], kCsTileBytes);
             __syncwarp();
-            if (PKV_TMA_MULTILANE) {
-                // lane b < 8 issues the two boxes of block b (its own table entry):
-                // one thread issuing all 16 boxes of a tile is the slower path
-                if (lane < 8) {
-                    tc::tma_load_2d(dst + lane * 2048, map, 0, y_cur, &full[s]);
-                    tc::tma_load_2d(dst + kCsHalfBytes + lane * 2048, map, 64, y_cur, &full[s]);
-                }
-            } else {
-                int ys[8];
-#pragma unroll
-                for (int bi = 0; bi < 8; ++bi) ys[bi] = __shfl_sync(0xffffffffu, y_cur, bi);
-                if (lane == 0) {
-#pragma unroll
-                    for (int bi = 0; bi < 8; ++bi) {
-                        tc::tma_load_2d(dst + bi * 2048, map, 0, ys[bi], &full[s]);
-                        tc::tma_load_2d(dst + kCsHalfBytes + bi * 2048, map, 64, ys[bi], &full[s]);
-                    }
-                }
+            // lane b < 8 issues the two boxes of block b (its own table entry):
+            // one thread issuing all 16 boxes of a tile is the slower path
+            if (lane < 8) {
+                tc::tma_load_2d(dst + lane * 2048, map, 0, y_cur, &full[s]);
+                tc::tma_load_2d(dst + kCsHalfBytes + lane * 2048, map, 64, y_cur, &full[s]);
             }
             issued = t + 1;
             y_cur = y_nxt;
@@ -722,6 +705,7 @@ kv_status paged_decode_attention_cascade(
     if (!p || batch < 0 || max_blocks < 0 || num_q_heads <= 0 || num_groups < 0 || group_size < 0 ||
         max_prefix_blocks < 0 || prefix_splits < 0 || num_splits < 0)
         return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if (p->dtype != KV_BF16 || p->head_dim != kCsD) return KV_ERR_UNSUPPORTED;
     if (num_q_heads % p->num_kv_heads) return KV_ERR_ARG;
     const int g = num_q_heads / p->num_kv_heads;

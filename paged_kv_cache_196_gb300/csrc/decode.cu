@@ -41,33 +41,14 @@
 
 namespace pkv {
 
-#ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 4
-#endif
-#ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 8
-#endif
-#ifndef PKV_DECODE_MINB
-#define PKV_DECODE_MINB 3
-#endif
-#ifndef PKV_DECODE_HS8
-#define PKV_DECODE_HS8 2
-#endif
-#ifndef PKV_TC_MIN_G
-#define PKV_TC_MIN_G 3   // smallest head group routed to the tensor-core decode
-#endif
-#ifndef PKV_TC_DEEP_BLOCKS
-#define PKV_TC_DEEP_BLOCKS 256  // partitions this long use the deep-ring tensor-core decode
-#endif
-#ifndef PKV_TC_MULTILANE
-#define PKV_TC_MULTILANE 1  // the four boxes of a K/V block are issued by four producer lanes
-#endif
-constexpr int kNW = PKV_DECODE_WARPS;    // consumer warps per CTA
+constexpr int kNW = 4;                   // consumer warps per CTA
 constexpr int kDecodeThreads = (kNW + 1) * 32;
 constexpr int kBS = 16;                  // tokens per block
 constexpr int kMaxPartBlocks = 1024;     // blocks per split (bounds the table slice in smem)
-constexpr int kNStage = PKV_DECODE_STAGES;  // pipeline depth (a multiple of kNW)
-constexpr int kTcDeepBlocks = PKV_TC_DEEP_BLOCKS;
+constexpr int kNStage = 8;               // pipeline depth (a multiple of kNW)
+constexpr int kDecodeMinBlocks = 3;      // CTAs per SM the CUDA-core decode is built for
+constexpr int kTcMinGroup = 3;           // smallest head group routed to the tensor-core decode
+constexpr int kTcDeepBlocks = 256;       // partitions this long use the deep-ring tensor-core decode
 // Balanced schedules (kv_decode_schedule), int32 words:
 //   [0] CTAs C, [1] pieces P, [2] most pieces of one (sequence, kv head),
 //   [3] most blocks of one CTA, [4] deep ring (1) or wide (0), [5] batch,
@@ -339,7 +320,7 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
 // lane carries all G heads.  HS = 2: both halves take the same token and each
 // carries G/2 heads (half the q and accumulator registers, for large G).
 template <int D, int G, int HS, bool BF16, bool LINEAR>
-__global__ void __launch_bounds__(kDecodeThreads, PKV_DECODE_MINB) decode_kernel(const DecodeKParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kernel(const DecodeKParams p) {
     using S = TileShape<D, BF16>;
     constexpr int kTile = S::kBytes;
     constexpr int kPairs = S::kPairs;
@@ -895,17 +876,10 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                     mbar_arrive(&full[st]);
             }
             if (valid) {
-                if (PKV_TC_MULTILANE) {
-                    // lane x issues box x: K half 0, K half 1, V half 0, V half 1
-                    if (lane < 4)
-                        mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
-                                   lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
-                } else if (lane == 0) {
-                    mma::tma2d(dst, map_k, 0, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile / 2, map_k, 64, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile, map_v, 0, y, &full[st], policy);
-                    mma::tma2d(dst + kTcTile + kTcTile / 2, map_v, 64, y, &full[st], policy);
-                }
+                // lane x issues box x: K half 0, K half 1, V half 0, V half 1
+                if (lane < 4)
+                    mma::tma2d(dst + (lane >> 1) * kTcTile + (lane & 1) * (kTcTile / 2),
+                               lane < 2 ? map_k : map_v, (lane & 1) * 64, y, &full[st], policy);
             }
             issued = i + 1;
         }
@@ -1392,7 +1366,7 @@ template <int D, int G, bool BF16, bool LINEAR>
 static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
     const size_t smem = decode_smem_bytes<D, G, BF16, LINEAR>(kp.part_blocks);
     // Large head groups split their heads across the two half-warps (register pressure).
-    constexpr int HS = (G >= 8 && D == 128) ? PKV_DECODE_HS8 : 1;
+    constexpr int HS = (G >= 8 && D == 128) ? 2 : 1;
     auto fn = decode_kernel<D, G, HS, BF16, LINEAR>;
     if (kv_status st0 = cuda_status(
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
@@ -1486,7 +1460,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     const bool bf = a.dtype == KV_BF16;
     // Large head groups on bf16 / d128 go to the tensor-core variant when the
     // tiled-TMA maps of the K/V storage are available.
-    const bool use_tc = bf && a.head_dim == 128 && g >= PKV_TC_MIN_G &&
+    const bool use_tc = bf && a.head_dim == 128 && g >= kTcMinGroup &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
     if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
     // a schedule: paged tensor-core path, every merge inside the kernel
@@ -1836,6 +1810,7 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
                                  size_t workspace_bytes, void *stream) {
     if (!p || max_blocks < 0 || (batch > 0 && max_blocks > 0 && !block_tables)) return KV_ERR_ARG;
     DecodeArgs a{};
+    if (kv_status st = require_device(p->device)) return st;
     a.q = q;
     a.k_pool = p->k;
     a.v_pool = p->v;
@@ -1878,6 +1853,7 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
         return KV_ERR_ARG;
     if (batch == 0) return KV_OK;
     if (!k_new || !v_new || !slot_mapping) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return KV_ERR_ARG;
     DecodeArgs a{};
     a.q = q;
@@ -1932,6 +1908,7 @@ kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const voi
     if (!p || batch < 0 || max_blocks < 0 || !host_schedule || !schedule ||
         (batch > 0 && max_blocks > 0 && !block_tables))
         return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if (batch == 0) return KV_OK;
     const int32_t *hs = host_schedule;
     if (hs[0] < 1 || hs[1] < 0 || hs[2] < 1 || hs[2] > kFuseMaxSplits || hs[3] < 1 ||
@@ -2008,11 +1985,11 @@ constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 constexpr int kStaticMaxDevices = 64;
 static __device__ __align__(256) float g_decode_scratch[kStaticScratchBytes / sizeof(float)];
 
-static kv_status static_scratch(void **ptr) {
+// The scratch address on `dev`, which must be the current device (the
+// caller checks that it is the pool's).
+static kv_status static_scratch(int dev, void **ptr) {
     static std::mutex mu;
     static void *addr[kStaticMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
     if (dev < 0 || dev >= kStaticMaxDevices) return KV_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
@@ -2033,13 +2010,14 @@ kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32
                                          kv_dtype out_dtype, float *lse_out, int num_splits,
                                          void *stream) {
     if (!p || batch < 0 || num_q_heads <= 0 || max_blocks < 0) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     int pb = 0, ms = 0;
     split_plan(batch, p->num_kv_heads, max_blocks, num_splits, &pb, &ms);
     const size_t need = decode_workspace_bytes(batch, num_q_heads, p->head_dim, ms);
     if (need > kStaticScratchBytes) return KV_ERR_UNSUPPORTED;  // beyond the fixed scratch array
     void *ws = nullptr;
     if (need > 0) {
-        const kv_status st = static_scratch(&ws);
+        const kv_status st = static_scratch(p->device, &ws);
         if (st != KV_OK) return st;
     }
     return paged_decode_attention(p, q, block_tables, max_blocks, seq_lens, batch, num_q_heads,

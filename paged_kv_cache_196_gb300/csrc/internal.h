@@ -39,6 +39,13 @@ inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s
 // Remembers the text of the last CUDA error seen by this thread.
 void note_cuda_error(cudaError_t e);
 
+// A pool or contiguous context keeps its memory on the device that was
+// current when it was created, and its kernels must run there.  Returns
+// KV_OK when that device is current, KV_ERR_ARG when another one is (the
+// call then launches nothing), KV_ERR_CUDA when the current device cannot be
+// read.
+kv_status require_device(int device);
+
 // Maps a CUDA runtime error to a status.
 inline kv_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return KV_OK;

@@ -25,6 +25,15 @@ void note_cuda_error(cudaError_t e) {
              cudaGetErrorString(e));
 }
 
+kv_status require_device(int device) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return KV_ERR_CUDA;
+    }
+    return cur == device ? KV_OK : KV_ERR_ARG;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -183,10 +192,15 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
 
 kv_status kv_pool_destroy(kv_pool_t p) {
     if (!p) return KV_ERR_ARG;
+    // free on the pool's own device, then give the caller its device back
+    int cur = -1;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != p->device &&
+                          cudaSetDevice(p->device) == cudaSuccess;
     if (p->k) cudaFree(p->k);
     if (p->v) cudaFree(p->v);
     if (p->err) cudaFree(p->err);
     if (p->counters) cudaFree(p->counters);
+    if (switched) cudaSetDevice(cur);
     if (p->alloc) kv_allocator_destroy(p->alloc);
     delete p;
     return KV_OK;
@@ -228,6 +242,7 @@ kv_status kv_free_blocks(kv_pool_t p, int n, const int32_t *ids) {
 
 kv_status kv_cow_if_shared(kv_pool_t p, int32_t *block_id_inout, int *copied, void *stream) {
     if (!p || !block_id_inout || !copied) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     *copied = 0;
     const int32_t old = *block_id_inout;
     int rc = 0;
@@ -251,6 +266,7 @@ kv_status kv_cow_if_shared(kv_pool_t p, int32_t *block_id_inout, int *copied, vo
 kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
                     const int64_t *slot_mapping, int num_tokens, void *stream) {
     if (!p || num_tokens < 0) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if (num_tokens == 0) return KV_OK;
     if (!k_new || !v_new || !slot_mapping) return KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
@@ -267,6 +283,7 @@ kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
 kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, int n,
                          void *stream) {
     if (!p || n < 0) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if (n == 0) return KV_OK;
     if (!src || !dst) return KV_ERR_ARG;
     const int block_chunks = p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype) / 16;
@@ -277,6 +294,7 @@ kv_status kv_copy_blocks(kv_pool_t p, const int32_t *src, const int32_t *dst, in
 
 static kv_status swap(kv_pool_t p, const int32_t *ids, int n, void *host, int dir, void *stream) {
     if (!p || n < 0) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     if (n == 0) return KV_OK;
     if (!ids || !host || (reinterpret_cast<uintptr_t>(host) & 15)) return KV_ERR_ARG;
     const int block_chunks = p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype) / 16;
@@ -304,6 +322,7 @@ kv_status kv_swap_bytes(kv_pool_t p, int n, size_t *bytes) {
 
 kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream) {
     if (!p || !code) return KV_ERR_ARG;
+    if (kv_status st = require_device(p->device)) return st;
     int h = 0;
     cudaStream_t s = as_stream(stream);
     if (cudaMemcpyAsync(&h, p->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||

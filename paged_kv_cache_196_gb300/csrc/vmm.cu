@@ -321,6 +321,7 @@ kv_status kv_contig_layout(kv_contig_t c, int64_t *head_stride, int64_t *page_by
 
 kv_status kv_contig_reserve(kv_contig_t c, int req) {
     if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     kv_contig::Req &r = c->reqs[req];
     if (r.base) return KV_ERR_STATE;
     DriverVmm &d = driver();
@@ -340,6 +341,7 @@ kv_status kv_contig_reserve(kv_contig_t c, int req) {
 kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
     if (!c || req < 0 || req >= c->max_requests || n_tokens < 0 || n_tokens > c->max_tokens)
         return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     kv_contig::Req &r = c->reqs[req];
     if (!r.base) return KV_ERR_STATE;
     const long long need = (n_tokens + c->tokens_per_page - 1) / c->tokens_per_page;
@@ -397,6 +399,7 @@ kv_status kv_contig_ensure(kv_contig_t c, int req, int64_t n_tokens) {
 
 kv_status kv_contig_release(kv_contig_t c, int req) {
     if (!c || req < 0 || req >= c->max_requests) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     kv_contig::Req &r = c->reqs[req];
     if (!r.base) return KV_OK;
     DriverVmm &d = driver();
@@ -427,6 +430,11 @@ kv_status kv_contig_release(kv_contig_t c, int req) {
 
 kv_status kv_contig_destroy(kv_contig_t c) {
     if (!c) return KV_ERR_ARG;
+    // unmap and free on the context's own device, then give the caller its
+    // device back
+    int cur = -1;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != c->device &&
+                          cudaSetDevice(c->device) == cudaSuccess;
     stop_page_worker(c);
     c->pp.high = 0;  // released pages are not kept any more
     for (int r = 0; r < c->max_requests; ++r)
@@ -439,6 +447,7 @@ kv_status kv_contig_destroy(kv_contig_t c) {
     if (c->err) cudaFree(c->err);
     if (c->counters) cudaFree(c->counters);
     if (c->d_maps) cudaFree(c->d_maps);
+    if (switched) cudaSetDevice(cur);
     delete c;
     return KV_OK;
 }
@@ -501,6 +510,7 @@ kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
                            const int32_t *req_ids, const int32_t *positions, int num_tokens,
                            void *stream) {
     if (!c || num_tokens < 0) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     if (num_tokens == 0) return KV_OK;
     if (!k_new || !v_new || !req_ids || !positions) return KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
@@ -538,6 +548,7 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
                                   int num_splits, void *workspace, size_t workspace_bytes,
                                   void *stream) {
     if (!c || (batch > 0 && !req_ids)) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     DecodeArgs a{};
     a.q = q;
     a.max_blocks = (c->max_tokens + 15) / 16;  // the split plan of an equal-width block table
@@ -577,6 +588,7 @@ kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable) {
 
 kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream) {
     if (!c || !code) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
     int h = 0;
     cudaStream_t s = as_stream(stream);
     if (cudaMemcpyAsync(&h, c->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||

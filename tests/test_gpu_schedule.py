@@ -171,8 +171,9 @@ def test_scheduled_step_fuses_the_append(num_sms):
 
 
 def test_llama3_8b_scheduled_full_size_sampled():
-    """The Llama-3-8B-shaped decode at full size on the device's own schedule
-    (the benchmark's launch configuration), sampled against the oracle."""
+    """The Llama-3-8B-shaped decode at full size on a balanced schedule,
+    sampled against the oracle.  (The benchmark runs this shape on the
+    grid-indexed plan; it takes the schedule for long contexts.)"""
     c = _full_decode_case("llama3_8b_decode")
     out, lse, s = _sched_run(c, 0)
     items = _sample_items(c.B, c.hq, 96, 3)

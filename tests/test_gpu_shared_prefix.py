@@ -164,16 +164,23 @@ def _check(inp, max_blocks, prefix_splits=0):
     np.testing.assert_array_equal(lse_s, lse_p)
     assert ncow_p == 0
     lens, G, P = inp["lens"], inp["group_size"], inp["prefix_len"]
-    # a write into a shared block copied it: exactly the sequences whose new
-    # token falls inside a partly used shared prefix block (L < prefix, L % 16 != 0)
+    # A write into a shared block copies it first.  The writers of prefix block
+    # k are the sequences whose new token lands inside it (L < prefix,
+    # L % 16 != 0, L // 16 == k); its holders are the sequences whose shared
+    # part reaches into it.  Planned in sequence order, each copy drops one
+    # reference, so every writer copies unless it is the last holder left:
+    # w copies when some holder does not write, w - 1 when all of them do.
     expect_cow = 0
     for g0 in range(0, len(lens), G):
-        grp = lens[g0:g0 + G]
+        grp = [int(x) for x in lens[g0:g0 + G]]
+        writers = {}
         for L in grp:
             if L < P and L % BS:
-                sharers = np.sum(np.minimum(grp, P) > (L // BS) * BS)
-                expect_cow += int(sharers > 1)
-    assert ncow <= expect_cow and (expect_cow == 0 or ncow > 0)
+                writers[L // BS] = writers.get(L // BS, 0) + 1
+        for k, w in writers.items():
+            holders = sum(1 for L in grp if min(L, P) > k * BS)
+            expect_cow += w if holders > w else w - 1
+    assert ncow == expect_cow
     # every block still in a table is referenced once per table that holds it
     counts = {}
     for t in tab_s[tab_s >= 0]:
