@@ -69,6 +69,9 @@ typedef enum { KV_F32 = 0, KV_BF16 = 1 } kv_dtype;
 #define KV_DEVERR_SLOT_RANGE 0x2    /* slot_mapping entry >= num_blocks * block_size */
 #define KV_DEVERR_TIMEOUT 0x4       /* an mbarrier wait exceeded its time limit */
 #define KV_DEVERR_UNMAPPED 0x8      /* contiguous path: position beyond the mapped range */
+#define KV_DEVERR_VALUE_RANGE 0x10  /* prefill: a V value of a key below the sequence length
+                                       with |v| >= 65536 or infinite; the PV product, run on
+                                       fp16 operands, used +-65504 in its place */
 
 const char *kv_status_string(kv_status s);
 
@@ -517,8 +520,9 @@ kv_status paged_prefill_attention(kv_pool_t p, const void *q, const int32_t *cu_
                                   void *stream);
 
 /* Synchronises `stream`, returns the device error word in *code (0 = none)
- * and clears it.  Returns KV_ERR_DEVICE_BOUNDS or KV_ERR_TIMEOUT when bits are
- * set, KV_OK otherwise. */
+ * and clears it.  Returns KV_ERR_TIMEOUT if the timeout bit is set, else
+ * KV_ERR_UNSUPPORTED if only KV_DEVERR_VALUE_RANGE is set, else
+ * KV_ERR_DEVICE_BOUNDS if any bit is set, KV_OK otherwise. */
 kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream);
 
 /* ======================================================================

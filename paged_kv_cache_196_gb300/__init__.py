@@ -550,7 +550,7 @@ def kv_get_device_error(p: int, stream=None) -> int:
     """Returns the device error bits (and clears them); never raises on set bits."""
     code = _i32()
     st = lib().kv_get_device_error(p, ctypes.byref(code), _stream(stream))
-    if st not in (0, -5, -6):
+    if st not in (0, -3, -5, -6):
         raise KVError(st, "kv_get_device_error")
     return code.value
 

@@ -57,6 +57,7 @@ inline kv_status cuda_status(cudaError_t e) {
 inline kv_status device_error_status(int code) {
     if (code == 0) return KV_OK;
     if (code & KV_DEVERR_TIMEOUT) return KV_ERR_TIMEOUT;
+    if (code == KV_DEVERR_VALUE_RANGE) return KV_ERR_UNSUPPORTED;
     return KV_ERR_DEVICE_BOUNDS;
 }
 

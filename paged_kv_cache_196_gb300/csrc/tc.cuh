@@ -126,6 +126,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_ma
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with fp16 A/B, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn_major,
+                                                     bool b_mn_major) {
+    return (1u << 4)                     // D format: f32; A and B format fields 0: f16
+           | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 KV_DEVICE void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                       uint32_t accumulate) {
@@ -165,6 +173,26 @@ KV_DEVICE void fence_proxy_async_smem() {
 KV_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Packs two floats as fp16 (round to nearest even): lo -> bits 0..15.
+KV_DEVICE uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two bf16 values (a 32-bit word, low half = lower index) as two fp16 values
+// in the same positions.  Exact for magnitudes in [2^-14, 65280]; smaller
+// ones become fp16 subnormals (absolute error below 2^-25); larger finite
+// ones saturate to +-65504 (callers check the range); NaN stays NaN.
+// *mx takes the larger of itself and both magnitudes (NaN is not counted).
+KV_DEVICE uint32_t bf16x2_to_f16x2(uint32_t w, float *mx) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    *mx = fmaxf(*mx, fmaxf(fabsf(lo), fabsf(hi)));
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 

@@ -132,6 +132,39 @@ def test_prefill_leaves_rows_outside_chunks_untouched():
     c.close()
 
 
+def test_prefill_flags_v_values_beyond_fp16():
+    """The PV product runs on fp16 operands: an attended V value of 70000
+    (representable in bf16, not in fp16) saturates to 65504 and sets
+    KV_DEVERR_VALUE_RANGE; rows that do not attend its key stay exact, and no
+    row turns non-finite (a causally masked weight of zero meets a finite
+    value)."""
+    c = PrefillCase([40], [100], hq=4, hkv=2, seed=73, poison=False)
+    key, h, dim = 50, 0, 3                     # chunk position 10: rows 10.. attend it
+    blk, off = int(c.tables[0, key // 16]), key % 16
+    big = W.to_bf16_bits(np.array([70000.0], np.float32))[0]
+    c.ref_v[blk, h, off, dim] = big
+    _, vv = pool_views(c.pool, c.nb, c.hkv, c.d, True)
+    vv[blk, h, off, dim] = int(big)            # 0x4789 < 0x8000: the same int16
+    out = torch.full((c.total_q, c.hq, c.d), float("nan"), dtype=torch.float32, device="cuda")
+    pk.paged_prefill_attention(c.pool, dev(c.q), dev(c.cu), c.total_q, int(c.chunk.max()),
+                               dev(c.tables), c.maxb, dev(c.lens), c.B, c.hq, 1 / math.sqrt(c.d),
+                               out, pk.KV_F32, None)
+    torch.cuda.synchronize()
+    assert pk.kv_get_device_error(c.pool) == 0x10
+    out = host(out).astype(np.float64)
+    assert np.all(np.isfinite(out))
+    ref, _ = c.oracle()
+    assert_close_scaled(out[:10], ref[:10], 2e-3, "rows before the large key")
+    # rows that attend it see 65504 there: the oracle on fp32 copies of the
+    # pools (bf16 widens exactly) with that one value replaced
+    v32 = W.bf16_bits_to_f32(c.ref_v)
+    v32[blk, h, off, dim] = 65504.0
+    ref_sat, _ = oracle.paged_prefill(W.bf16_bits_to_f32(c.ref_k), v32, c.tables, c.lens, c.cu,
+                                      W.bf16_bits_to_f32(c.q), 1 / math.sqrt(c.d))
+    assert_close_scaled(out[10:], ref_sat[10:], 2e-3, "rows attending the saturated value")
+    c.close()
+
+
 @pytest.mark.slow
 def test_yi34b_prefill_full_size_sampled():
     cfg = W.CONFIGS["yi34b_prefill"]
@@ -142,6 +175,14 @@ def test_yi34b_prefill_full_size_sampled():
     g = W.rng(5)
     rows = list(g.integers(0, c.total_q, 40)) + [0, 2047, 2048, c.total_q - 1]
     items = [(int(r), int(h)) for r, h in zip(rows, g.integers(0, c.hq, len(rows)))]
+    T = cfg["chunk_len"]
+    # one CTA's whole slab (two 128-row query tiles) for every query head: the
+    # last 256 rows of the third sequence, ending at its final query
+    items += [(2 * T + T - 256 + r, h) for r in range(256) for h in range(c.hq)]
+    # every row of the first sequence's first query tile, for every head: its
+    # last key tile is the one the causal boundary cuts (cached length 8192)
+    items += [(r, h) for r in range(128) for h in range(c.hq)]
+    items = sorted(set(items))
     ref, ref_lse = c.oracle(items)
     got = np.array([out[r, h] for r, h in items])
     assert_close_scaled(got, ref, 2e-3, "yi-34b prefill sampled")
