@@ -14,6 +14,13 @@ lengths uniform in [512, 4096], 32 query / 8 kv heads, head_dim 128, bf16,
 Metric: KV bytes read by decode attention per second (valid tokens only:
 sum_b L_b * 2 * Hkv * D * 2 bytes) -- "value" -- plus decode tokens/s.
 
+On one GPU the default run also measures, in the same process and with
+short runs, the Yi-6B-shaped long-context decode (paged on the balanced
+schedule and on the grid plan, and the contiguous path, with the
+paged-vs-contiguous slowdown), the shared-prefix step and the Yi-34B-shaped
+prefill with its chunk append; they go under "other_workloads"
+(--no-extras skips them).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
        [--splits S] [--plan auto|grid|balanced] [--prefix-splits P] [--impl reference]
 Under torchrun each rank runs an independent replica (weak scaling).
@@ -521,6 +528,10 @@ def run_ours(args, rank, world, local_rank):
     if contig:
         line["config"]["vmm"] = {"page_bytes": page, "map_seconds": round(map_s, 4),
                                  "head_stride_tokens": head_stride}
+    if contig:
+        pk.kv_contig_destroy(ctx)
+    else:
+        pk.kv_pool_destroy(pool)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, nb, max_blocks)
     if dist:
@@ -709,6 +720,7 @@ def run_prefill(args, rank, world, local_rank):
     append_bytes = 2 * 2 * T * hkv * d * 2 + 8 * T  # read k/v_new, write the pool, slots
     if pk.kv_get_device_error(pool):
         raise RuntimeError("device error word set after the timed region")
+    pk.kv_pool_destroy(pool)
     peak, kind = read_tensor_peak()
     achieved = flops / (attend_ms * 1e-3) / 1e12
     line = {
@@ -901,6 +913,7 @@ def run_shared_prefix(args, rank, world, local_rank):
         raise RuntimeError("device error word set after the timed region")
     peak, peak_kind = read_peaks()
     achieved = unique_bytes / (dec_ms * 1e-3) / 1e9
+    pk.kv_pool_destroy(pool)
     return {
         "metric": METRIC, "value": round(logical_bytes * K / (total_ms * 1e-3) / 1e9, 1),
         "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -1029,6 +1042,67 @@ def run_vmm(args, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------------------------
+# The other workloads, measured in the same process as the headline
+# --------------------------------------------------------------------------
+def _summary(line):
+    r = line.get("roofline", {})
+    out = {"value": line["value"], "unit": line["unit"], "ms_per_step": line["ms_per_step"],
+           "steps": line["steps"],
+           "roofline": {k: r.get(k) for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                              "avg_launch_ms")},
+           "clocks": line.get("clocks")}
+    if "e2e" in line:
+        out["e2e"] = {"value": line["e2e"]["value"], "unit": line["e2e"]["unit"]}
+    plan = line["config"].get("plan")
+    if plan:
+        out["plan"] = plan
+    return out
+
+
+def run_extras(args, local_rank):
+    """Short runs of the Yi-6B decode (paged, balanced schedule and grid plan;
+    contiguous), the shared-prefix step and the Yi-34B prefill (with its chunk
+    append), one after another in this process, for the headline line."""
+    sub = argparse.Namespace(**vars(args))
+    sub.steps = max(20, min(args.steps, 300))
+    sub.warmup = max(3, min(args.warmup, 10))
+    sub.no_cpu_baseline = True
+    sub.splits = 0
+    res = {}
+    runs = [("yi6b_long_decode", "auto"), ("yi6b_long_decode_grid", "grid"),
+            ("yi6b_long_decode_contig", "auto"), ("shared_prefix_step", "auto"),
+            ("yi34b_prefill", "auto")]
+    for key, plan in runs:
+        sub.workload = key.replace("_grid", "")
+        sub.plan = plan
+        t0 = time.time()
+        if sub.workload == "yi34b_prefill":
+            line = run_prefill(sub, 0, 1, local_rank)
+        elif sub.workload == "shared_prefix_step":
+            line = run_shared_prefix(sub, 0, 1, local_rank)
+        else:
+            line = run_ours(sub, 0, 1, local_rank)
+        res[key] = _summary(line)
+        if key == "yi34b_prefill":
+            res["prefill_chunk_append"] = line["append"]
+        if key == "shared_prefix_step":
+            res[key]["decode_ms"] = line["decode_ms"]
+        log(f"[bench] extra workload {key}: {line['value']} {line['unit']} "
+            f"({time.time() - t0:.1f}s)")
+    paged = res["yi6b_long_decode"]["value"]
+    grid = res["yi6b_long_decode_grid"]["value"]
+    contig = res["yi6b_long_decode_contig"]["value"]
+    # slowdown = t_paged / t_contig - 1 over the same KV bytes; positive: paged slower
+    res["yi6b_paged_vs_contiguous"] = {
+        "paged_gbs": paged, "paged_grid_gbs": grid, "contiguous_gbs": contig,
+        "slowdown_paged_balanced": round(contig / paged - 1, 4),
+        "slowdown_paged_same_grid_plan": round(contig / grid - 1, 4),
+        "target": "paged no more than 5% slower (slowdown <= 0.05)"}
+    return res
+
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1054,6 +1128,9 @@ def main():
                          "(0 = kv_cascade_plan)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload: skip the short runs of the other workloads that "
+                         "the headline line reports under other_workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1088,6 +1165,8 @@ def main():
         line = run_vmm(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
+    if world == 1 and args.workload == "llama3_8b_decode" and not args.no_extras:
+        line["other_workloads"] = run_extras(args, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
