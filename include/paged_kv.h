@@ -73,6 +73,9 @@ typedef enum { KV_F32 = 0, KV_BF16 = 1 } kv_dtype;
                                        with |v| >= 65536 or infinite; the PV product, run on
                                        fp16 operands, used +-65504 in its place */
 
+/* Default time limit of a pipeline wait inside a kernel (nanoseconds). */
+#define KV_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+
 const char *kv_status_string(kv_status s);
 
 /* Text of the last CUDA runtime error a call of this library met on the
@@ -619,6 +622,31 @@ kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream);
  * in their stream still runs, and wait for it before touching memory.  Off by
  * default.  Host only. */
 kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable);
+
+/* ======================================================================
+ * Test hooks: failure paths made reachable without faulting a GPU.  Not for
+ * production use.
+ * ==================================================================== */
+
+/* Every pipeline wait inside the kernels (for data a producer has to
+ * deliver, or a stage a consumer has to release) gives up after
+ * KV_WAIT_LIMIT_DEFAULT_NS, records KV_DEVERR_TIMEOUT and lets its kernel run
+ * to the end.  This sets that limit for kernels launched afterwards on the
+ * current device: 0 makes every wait that is not satisfied at its first poll
+ * give up; KV_WAIT_LIMIT_DEFAULT_NS restores the default.  A warp's wait for
+ * its own copies or tensor-core operations before its CTA ends keeps the
+ * default in all cases, so nothing is in flight when the memory they write is
+ * released.  Results of a call that timed out are undefined; the next
+ * kv_get_device_error returns KV_ERR_TIMEOUT and clears the state a merge may
+ * have left. */
+kv_status kv_debug_set_wait_limit_ns(uint64_t ns);
+
+/* Contiguous path: of the physical page creations kv_contig_ensure makes from
+ * now on (pages taken from the background pool do not count), the one after
+ * `after` more successful ones fails as if the device had no memory left, once.
+ * kv_contig_ensure then unmaps what that call had mapped and returns
+ * KV_ERR_OOM.  A negative `after` cancels a pending failure. */
+kv_status kv_debug_fail_page_create(int after);
 
 #ifdef __cplusplus
 }

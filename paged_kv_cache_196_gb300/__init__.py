@@ -30,11 +30,13 @@ __all__ = [
     "paged_decode_attention_cascade", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_page_pool", "kv_contig_page_stats", "kv_contig_append", "contig_decode_attention",
-    "kv_contig_get_device_error",
+    "kv_contig_get_device_error", "kv_debug_set_wait_limit_ns", "kv_debug_fail_page_create",
+    "KV_WAIT_LIMIT_DEFAULT_NS",
 ]
 
 KV_F32 = 0
 KV_BF16 = 1
+KV_WAIT_LIMIT_DEFAULT_NS = 2000000000
 
 STATUS = {0: "KV_OK", -1: "KV_ERR_ARG", -2: "KV_ERR_OOM", -3: "KV_ERR_UNSUPPORTED",
           -4: "KV_ERR_CUDA", -5: "KV_ERR_DEVICE_BOUNDS", -6: "KV_ERR_TIMEOUT", -7: "KV_ERR_STATE"}
@@ -127,6 +129,8 @@ _SIGS = {
                                 _sz, _vp],
     "kv_contig_get_device_error": [_vp, _P(_i32), _vp],
     "kv_contig_set_launch_overlap": [_vp, _i32],
+    "kv_debug_set_wait_limit_ns": [ctypes.c_uint64],
+    "kv_debug_fail_page_create": [_i32],
 }
 _RESTYPE = {"kv_status_string": ctypes.c_char_p, "kv_last_cuda_error": ctypes.c_char_p}
 
@@ -637,3 +641,16 @@ def kv_contig_get_device_error(c: int, stream=None) -> int:
     if st not in (0, -5, -6):
         raise KVError(st, "kv_contig_get_device_error")
     return code.value
+
+
+# ---------------------------------------------------------------- test hooks
+def kv_debug_set_wait_limit_ns(ns: int):
+    """Time limit of the kernels' pipeline waits on the current device (tests
+    only; KV_WAIT_LIMIT_DEFAULT_NS restores the default)."""
+    _check(lib().kv_debug_set_wait_limit_ns(int(ns)), "kv_debug_set_wait_limit_ns")
+
+
+def kv_debug_fail_page_create(after: int):
+    """The contiguous path's page creation after `after` more successful ones
+    fails once (tests only; negative cancels)."""
+    _check(lib().kv_debug_fail_page_create(int(after)), "kv_debug_fail_page_create")

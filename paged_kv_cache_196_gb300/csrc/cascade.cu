@@ -148,7 +148,7 @@ KV_DEVICE int prefix_limit(const CascadeParams &p, int b) {
 // which a TMEM lane quadrant would not allow otherwise).  Each writes its P
 // into its own key half of the row and zeros into the other half, so the one
 // PV product yields two partial O rows, added in the epilogue.
-template <bool DUP>
+template <bool DUP, bool TW>
 __global__ void __launch_bounds__(kCsThreads, 1)
     cascade_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const CascadeParams p) {
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             const int s = t & 1;
             bool stop = false;
             if (lane == 0)
-                stop = *abort_flag || (t >= 2 && !mbar_wait(&empty[s], ((t - 2) >> 1) & 1, p.err));
+                stop = *abort_flag || (t >= 2 && !mbar_wait<TW>(&empty[s], ((t - 2) >> 1) & 1, p.err));
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
             char *dst = ring + s * kCsTileBytes;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], kCsTileBytes);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             if (issued < n) *abort_flag = 1;
             // Never leave copies in flight into this CTA's shared memory.
             for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-                mbar_wait(&full[j & 1], (j >> 1) & 1, p.err);
+                mbar_wait_drain(&full[j & 1], (j >> 1) & 1, p.err);
         }
     } else if (warp == kCsMmaWarp) {
         // ================================================== MMA issuer
@@ -329,27 +329,27 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 tc::mma_commit(&bars->vempty[j & 1]);
                 tc::mma_commit(&bars->odone);
             };
-            bool ok = mbar_wait(&bars->qfull, 0, p.err) && mbar_wait(&bars->kfull[0], 0, p.err);
+            bool ok = mbar_wait<TW>(&bars->qfull, 0, p.err) && mbar_wait<TW>(&bars->kfull[0], 0, p.err);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0);
                 if (n > 1) {
-                    ok = mbar_wait(&bars->kfull[1], 0, p.err);
+                    ok = mbar_wait<TW>(&bars->kfull[1], 0, p.err);
                     tc::fence_after_sync();
                     if (ok) issue_s(1);
                 }
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int s = j & 1;
-                if (!mbar_wait(&bars->pfull[s], (j >> 1) & 1, p.err) ||
-                    !mbar_wait(&bars->vfull[s], (j >> 1) & 1, p.err)) {
+                if (!mbar_wait<TW>(&bars->pfull[s], (j >> 1) & 1, p.err) ||
+                    !mbar_wait<TW>(&bars->vfull[s], (j >> 1) & 1, p.err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
                 issue_pv(j);
                 if (j + 2 < n) {
-                    if (!mbar_wait(&bars->kfull[s], ((j + 2) >> 1) & 1, p.err)) {
+                    if (!mbar_wait<TW>(&bars->kfull[s], ((j + 2) >> 1) & 1, p.err)) {
                         ok = false;
                         break;
                     }
@@ -359,6 +359,10 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             }
             tc::mma_commit(&bars->done);
             if (!ok) *abort_flag = 1;
+            // No MMA may still write tensor memory when it is freed.  In the
+            // ordinary instantiations the softmax warps' wait for `done` has
+            // the full limit and guarantees it already.
+            if constexpr (TW) mbar_wait_drain(&bars->done, 0, p.err);
         }
     } else {
         // ================================================== softmax warps
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             for (int j = 0; j < n; ++j) {
                 const int sb = j & 1;
                 bool bad = bad_next || *abort_flag != 0;
-                if (!bad) bad = !mbar_wait(&bars->sfull[sb], (j >> 1) & 1, p.err);
+                if (!bad) bad = !mbar_wait<TW>(&bars->sfull[sb], (j >> 1) & 1, p.err);
                 tc::fence_after_sync();
                 const uint32_t scol = tmem + lane_base + sb * 128;
                 uint32_t sv[2][32];
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                          (acc2[3].x + acc2[3].y);
                 if (__any_sync(0xffffffffu, rescale)) {
                     // this lane's partial O holds PV(j-1) once that completes
-                    if (__any_sync(0xffffffffu, !mbar_wait(&bars->odone, (j - 1) & 1, p.err))) {
+                    if (__any_sync(0xffffffffu, !mbar_wait<TW>(&bars->odone, (j - 1) & 1, p.err))) {
                         bad_next = true;  // leave together at the next exchange
                     } else {
                         tc::fence_after_sync();
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             // ---- epilogue: the two partial O rows of a query row are added
             // (lane r + 64's through shared memory: the K ring is idle once
             // every MMA has completed)
-            if (ok) ok = mbar_wait(&bars->done, 0, p.err);
+            if (ok) ok = mbar_wait<TW>(&bars->done, 0, p.err);
             tc::fence_after_sync();
             float *xo = reinterpret_cast<float *>(sK);  // [64][128]
             bars->xsum[qr][half] = l_sum;
@@ -534,7 +538,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         for (int j = 0; j < n; ++j) {
             const int sb = j & 1;
             bool bad = *abort_flag != 0;
-            if (!bad) bad = !mbar_wait(&bars->sfull[sb], (j >> 1) & 1, p.err);
+            if (!bad) bad = !mbar_wait<TW>(&bars->sfull[sb], (j >> 1) & 1, p.err);
             if (__any_sync(0xffffffffu, bad)) {
                 ok = false;
                 break;
@@ -605,7 +609,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                          (acc2[3].x + acc2[3].y);
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O holds PV(j-1) once that completes (S(j) was issued before it)
-                    if (__any_sync(0xffffffffu, !mbar_wait(&bars->odone, (j - 1) & 1, p.err))) {
+                    if (__any_sync(0xffffffffu, !mbar_wait<TW>(&bars->odone, (j - 1) & 1, p.err))) {
                         ok = false;
                         *abort_flag = 1;
                         break;
@@ -629,7 +633,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             if (lane == 0) mbar_arrive(&bars->pfull[sb]);  // one arrival per warp
         }
         // ---- epilogue: this row's partial result (normalised o, lse in log2 units)
-        if (ok) ok = mbar_wait(&bars->done, 0, p.err);
+        if (ok) ok = mbar_wait<TW>(&bars->done, 0, p.err);
         if (!ok) *abort_flag = 1;
         tc::fence_after_sync();
         const bool write = ok && member >= 0 && lim > 0;
@@ -669,6 +673,8 @@ static int cascade_splits(int num_groups, int num_kv_heads, int max_prefix_block
     if (ps > tiles) ps = tiles;
     return ps;
 }
+
+cudaError_t set_wait_limit_cascade(unsigned long long ns) { return set_wait_limit_here(ns); }
 
 }  // namespace pkv
 
@@ -786,7 +792,10 @@ kv_status paged_decode_attention_cascade(
         cp.ws_lse = cp.ws_o + (size_t)batch * num_q_heads * cp.max_splits * kCsD;
         cp.err = p->err;
         // groups of at most 64 rows: duplicated rows, keys split over two threads
-        auto fn = (long long)group_size * g <= 64 ? cascade_prefix_kernel<true> : cascade_prefix_kernel<false>;
+        const bool dup = (long long)group_size * g <= 64;
+        auto fn = test_waits_enabled()
+                      ? (dup ? cascade_prefix_kernel<true, true> : cascade_prefix_kernel<false, true>)
+                      : (dup ? cascade_prefix_kernel<true, false> : cascade_prefix_kernel<false, false>);
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsSmemBytes)))
             return st0;

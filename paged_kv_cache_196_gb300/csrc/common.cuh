@@ -11,9 +11,18 @@
 
 namespace pkv {
 
-// A pipeline wait gives up after this many nanoseconds (then the kernel
-// records KV_DEVERR_TIMEOUT and winds down instead of spinning forever).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A pipeline wait gives up after this many nanoseconds by default (then the
+// kernel records KV_DEVERR_TIMEOUT and winds down instead of spinning forever).
+constexpr unsigned long long kWaitLimitNs = KV_WAIT_LIMIT_DEFAULT_NS;
+
+// The limit pipeline waits use: kWaitLimitNs unless a test shortened it
+// (kv_debug_set_wait_limit_ns).  One copy per translation unit and device.
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// Host: sets this translation unit's copy of the limit on the current device.
+static inline cudaError_t set_wait_limit_here(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
 
 KV_DEVICE uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,19 +68,49 @@ KV_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false
-// (after setting KV_DEVERR_TIMEOUT in *err) if that takes longer than
-// kWaitLimitNs.
-KV_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+// (after setting KV_DEVERR_TIMEOUT in *err) if it has not completed by the
+// end of the first round of 64 polls that ends after limit_ns have passed
+// since the first poll failed; with limit_ns = 0 the first failed poll gives
+// up.  The clock is read only between rounds of polls.
+KV_DEVICE bool mbar_wait_for(uint64_t *bar, uint32_t parity, int *err,
+                             unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns == 0) {
+        if (err) atomicOr(err, KV_DEVERR_TIMEOUT);
+        return false;
+    }
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 >= limit_ns) {
             if (err) atomicOr(err, KV_DEVERR_TIMEOUT);
             return false;
         }
     }
+}
+
+// A pipeline wait: data a producer has to deliver, a stage a consumer has to
+// release.  TW = false (the kernels' ordinary instantiations): the limit is
+// the compile-time kWaitLimitNs.  TW = true (the instantiations launched
+// while a test has shortened the limit, kv_debug_set_wait_limit_ns): the
+// limit is read from g_wait_limit_ns.  A run-time limit in every wait costs
+// the register-bound kernels a few per cent, so it stays out of the
+// ordinary instantiations.
+template <bool TW = false>
+KV_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+    if constexpr (TW)
+        return mbar_wait_for(bar, parity, err, g_wait_limit_ns);
+    else
+        return mbar_wait_for(bar, parity, err, kWaitLimitNs);
+}
+
+// A warp's wait for its own copies or tensor-core operations before it exits
+// or its CTA frees what they write (shared or tensor memory): always the full
+// default limit, whatever a test set for pipeline waits, so that nothing is
+// still in flight when the CTA ends.
+KV_DEVICE bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int *err) {
+    return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------ bulk copies

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
             // Do not leave while a copy into this CTA's shared memory may be in flight.
             for (int st = 0; st < kNStage && st < issued; ++st) {
                 const int r_last = (issued - 1 - st) / kNStage;
-                mbar_wait(&full[st], r_last & 1, p.err);
+                mbar_wait_drain(&full[st], r_last & 1, p.err);
             }
         }
         return;
@@ -770,7 +770,7 @@ KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
 
 // NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
 // compiled for MINB resident CTAs per SM.
-template <bool LINEAR, int NST, int MINB>
+template <bool LINEAR, int NST, int MINB, bool TW>
 __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
@@ -855,7 +855,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         for (int i = 0; i < nloc; ++i) {
             const int st = i % NST, r = i / NST;
             bool bad = false;
-            if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
+            if (lane == 0) bad = r > 0 && !mbar_wait<TW>(&empty[st], (r - 1) & 1, p.err);
             if (__shfl_sync(0xffffffffu, bad, 0)) break;
             int y;
             bool valid = true;
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         }
         if (lane == 0)
             for (int st = 0; st < NST && st < issued; ++st)
-                mbar_wait(&full[st], ((issued - 1 - st) / NST) & 1, p.err);
+                mbar_wait_drain(&full[st], ((issued - 1 - st) / NST) & 1, p.err);
         return;
     }
 
@@ -937,7 +937,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
 
     for (int i = warp; i < nloc; i += kNW) {
         const int st = i % NST, r = i / NST;
-        if (!mbar_wait(&full[st], r & 1, p.err)) break;
+        if (!mbar_wait<TW>(&full[st], r & 1, p.err)) break;
         int ntok = (int)min((long long)kBS, L - (long long)(blk0 + i) * kBS);
         if (!stage_valid[st]) ntok = 0;
         const uint32_t kt = stage_base + st * 2 * kTcTile;
@@ -1039,7 +1039,7 @@ KV_DEVICE TcPiece tc_piece(const DecodeKParams &p, int pc, bool report) {
 // slice; it refills the ring as soon as the consumers have read their merge
 // scratch out of it (named barrier 2), so the split merge of one piece
 // overlaps the first copies of the next.  NST ring stages, MINB CTAs per SM.
-template <int NST, int MINB>
+template <int NST, int MINB, bool TW>
 __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_sched_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                            const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
@@ -1103,7 +1103,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                 for (int i = 0; i < w.nloc; ++i) {
                     const int st = gi % NST, r = gi / NST;
                     bool bad = false;
-                    if (lane == 0) bad = r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.err);
+                    if (lane == 0) bad = r > 0 && !mbar_wait<TW>(&empty[st], (r - 1) & 1, p.err);
                     if (__shfl_sync(0xffffffffu, bad, 0)) {
                         stop = true;
                         break;
@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         }
         if (lane == 0)  // no copy may land after the CTA has exited
             for (int st = 0; st < NST && st < gi; ++st)
-                mbar_wait(&full[st], ((gi - 1 - st) / NST) & 1, p.err);
+                mbar_wait_drain(&full[st], ((gi - 1 - st) / NST) & 1, p.err);
         return;
     }
 
@@ -1208,7 +1208,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         if (!s_abort) {
             for (int i = ((warp - gbase) % kNW + kNW) % kNW; i < nloc; i += kNW) {
                 const int gi = gbase + i, st = gi % NST, r = gi / NST;
-                if (!mbar_wait(&full[st], r & 1, p.err)) {
+                if (!mbar_wait<TW>(&full[st], r & 1, p.err)) {
                     s_abort = 1;
                     break;
                 }
@@ -1263,6 +1263,15 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                                s_work[k & 1].split, s_work[k & 1].nsplit, 0, tid, s_mw, &s_flag,
                                more);
     }
+}
+
+// The tensor-core decode kernel for a schedule or a grid plan, ring depth
+// and addressing; TW: the test instantiation (run-time wait limit).
+template <bool TW>
+static auto tc_decode_fn(bool sched, bool deep, bool linear) {
+    return sched ? (deep ? decode_tc_sched_kernel<8, 3, TW> : decode_tc_sched_kernel<4, 5, TW>)
+           : deep ? (linear ? decode_tc_kernel<true, 8, 3, TW> : decode_tc_kernel<false, 8, 3, TW>)
+                  : (linear ? decode_tc_kernel<true, 4, 5, TW> : decode_tc_kernel<false, 4, 5, TW>);
 }
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst, int tables) {
@@ -1484,9 +1493,8 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = a.sched ? (deep ? decode_tc_sched_kernel<8, 3> : decode_tc_sched_kernel<4, 5>)
-                  : deep ? (linear ? decode_tc_kernel<true, 8, 3> : decode_tc_kernel<false, 8, 3>)
-                         : (linear ? decode_tc_kernel<true, 4, 5> : decode_tc_kernel<false, 4, 5>);
+        auto fn = test_waits_enabled() ? tc_decode_fn<true>(a.sched != nullptr, deep, linear)
+                                       : tc_decode_fn<false>(a.sched != nullptr, deep, linear);
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
@@ -1960,6 +1968,10 @@ kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const voi
 }
 
 }  // extern "C"
+
+namespace pkv {
+cudaError_t set_wait_limit_decode(unsigned long long ns) { return set_wait_limit_here(ns); }
+}  // namespace pkv
 
 // ---------------------------------------------------------------------------
 // Decode without caller-provided scratch.

@@ -1,5 +1,6 @@
 // Internal host-side definitions shared by the library's translation units.
 #pragma once
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -45,6 +46,21 @@ void note_cuda_error(cudaError_t e);
 // call then launches nothing), KV_ERR_CUDA when the current device cannot be
 // read.
 kv_status require_device(int device);
+
+// Set the pipeline-wait limit of the kernels of one source file (each has
+// its own copy of the device variable) on the current device.
+cudaError_t set_wait_limit_decode(unsigned long long ns);
+cudaError_t set_wait_limit_prefill(unsigned long long ns);
+cudaError_t set_wait_limit_cascade(unsigned long long ns);
+
+// True once a test has set a pipeline-wait limit other than the default
+// (kv_debug_set_wait_limit_ns): launches then take the kernels' test
+// instantiations, which read the limit at run time.
+bool test_waits_enabled();
+
+// Test hook of the contiguous path: page creations left before one fails
+// (-1: none fails).  Read and decremented by the page-taking code.
+extern std::atomic<int> g_fail_page_create_after;
 
 // Maps a CUDA runtime error to a status.
 inline kv_status cuda_status(cudaError_t e) {

@@ -25,6 +25,10 @@ void note_cuda_error(cudaError_t e) {
              cudaGetErrorString(e));
 }
 
+static std::atomic<bool> g_test_waits{false};
+
+bool test_waits_enabled() { return g_test_waits.load(std::memory_order_relaxed); }
+
 kv_status require_device(int device) {
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) {
@@ -318,6 +322,14 @@ kv_status kv_swap_bytes(kv_pool_t p, int n, size_t *bytes) {
     if (!p || n < 0 || !bytes) return KV_ERR_ARG;
     *bytes = (size_t)n * 2 * p->num_kv_heads * p->block_size * p->head_dim * dtype_bytes(p->dtype);
     return KV_OK;
+}
+
+kv_status kv_debug_set_wait_limit_ns(uint64_t ns) {
+    cudaError_t e = set_wait_limit_decode(ns);
+    if (e == cudaSuccess) e = set_wait_limit_prefill(ns);
+    if (e == cudaSuccess) e = set_wait_limit_cascade(ns);
+    if (e == cudaSuccess) g_test_waits.store(ns != KV_WAIT_LIMIT_DEFAULT_NS);
+    return cuda_status(e);
 }
 
 kv_status kv_get_device_error(kv_pool_t p, int *code, void *stream) {

@@ -119,6 +119,7 @@ struct PfBars {
     int abort;
 };
 
+template <bool TW>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     auto convert = [&](int t, int part) {
         const int s = t % kPfVStages;
         bool stop = false;
-        if (lane == 0) stop = *abort_flag || !mbar_wait(&bars->vland[s], (t / kPfVStages) & 1, p.err);
+        if (lane == 0) stop = *abort_flag || !mbar_wait<TW>(&bars->vland[s], (t / kPfVStages) & 1, p.err);
         if (__shfl_sync(0xffffffffu, stop, 0)) return false;
         // Lane l of part x rewrites 16-byte chunks 32x + l + 256k: chunk i holds
         // dims 8(i % 8).. of key row (i % 1024) / 8 of half i / 1024 (the
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int s = t & 1;
             bool stop = false;
             if (lane == 0)
-                stop = *abort_flag || (t >= 2 && !mbar_wait(&bars->kempty[s], ((t - 2) >> 1) & 1, p.err));
+                stop = *abort_flag || (t >= 2 && !mbar_wait<TW>(&bars->kempty[s], ((t - 2) >> 1) & 1, p.err));
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
             char *dst = sK + s * kPfTileBytes;
             if (lane == 0) mbar_arrive_expect_tx(&bars->kfull[s], kPfTileBytes);
@@ -277,9 +278,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) {
             if (issued < n) *abort_flag = 1;
             // Never leave copies in flight into this CTA's shared memory.
-            mbar_wait(&bars->qfull, 0, p.err);
+            mbar_wait_drain(&bars->qfull, 0, p.err);
             for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-                mbar_wait(&bars->kfull[j & 1], (j >> 1) & 1, p.err);
+                mbar_wait_drain(&bars->kfull[j & 1], (j >> 1) & 1, p.err);
         }
     } else if (warp == kPfVProducerWarp) {
         // ================================================== V producer
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (lane == 0)
                 stop = *abort_flag ||
                        (t >= kPfVStages &&
-                        !mbar_wait(&bars->vempty[s], ((t - kPfVStages) / kPfVStages) & 1, p.err));
+                        !mbar_wait<TW>(&bars->vempty[s], ((t - kPfVStages) / kPfVStages) & 1, p.err));
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
             char *dst = sV + s * kPfTileBytes;
             if (lane == 0) mbar_arrive_expect_tx(&bars->vland[s], kPfTileBytes);
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (issued < n) *abort_flag = 1;
             // Never leave copies in flight into this CTA's shared memory.
             for (int j = (issued > kPfVStages ? issued - kPfVStages : 0); j < issued; ++j)
-                mbar_wait(&bars->vland[j % kPfVStages], (j / kPfVStages) & 1, p.err);
+                mbar_wait_drain(&bars->vland[j % kPfVStages], (j / kPfVStages) & 1, p.err);
         }
     } else if (warp == kPfMmaWarp) {
         // ================================================== MMA issuer
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc::mma_ts(tmem + colO(x), tmem + colS(x) + kk * 8, db, idesc_pv, (j | kk) != 0);
                 }
             };
-            bool ok = mbar_wait(&bars->qfull, 0, p.err) && mbar_wait(&bars->kfull[0], 0, p.err);
+            bool ok = mbar_wait<TW>(&bars->qfull, 0, p.err) && mbar_wait<TW>(&bars->kfull[0], 0, p.err);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
@@ -355,8 +356,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int j = 0; ok && j < n; ++j) {
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
-                    if (!mbar_wait(&bars->pfull[x], j & 1, p.err) ||
-                        (x == 0 && !mbar_wait(&bars->vfull[j % kPfVStages], (j / kPfVStages) & 1,
+                    if (!mbar_wait<TW>(&bars->pfull[x], j & 1, p.err) ||
+                        (x == 0 && !mbar_wait<TW>(&bars->vfull[j % kPfVStages], (j / kPfVStages) & 1,
                                               p.err))) {
                         ok = false;
                         break;
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     issue_pv(x, j);
                     if (x == 1) tc::mma_commit(&bars->vempty[j % kPfVStages]);
                     if (j + 1 < n) {
-                        if (x == 0 && !mbar_wait(&bars->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err)) {
+                        if (x == 0 && !mbar_wait<TW>(&bars->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err)) {
                             ok = false;
                             break;
                         }
@@ -377,6 +378,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             tc::mma_commit(&bars->done);
             if (!ok) *abort_flag = 1;
+            // No MMA may still write tensor memory when it is freed.  In the
+            // ordinary instantiations the softmax warps' wait for `done` has
+            // the full limit and guarantees it already.
+            if constexpr (TW) mbar_wait_drain(&bars->done, 0, p.err);
         }
     } else {
         // ================================================== softmax warps
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = 0; ok && j < n; ++j) {
             // Exits are warp-uniform: the warp arrives on pfull as one.
             bool bad = *abort_flag != 0;
-            if (!bad) bad = !mbar_wait(&bars->sfull[x], j & 1, p.err);
+            if (!bad) bad = !mbar_wait<TW>(&bars->sfull[x], j & 1, p.err);
             if (__any_sync(0xffffffffu, bad)) { ok = false; break; }
             tc::fence_after_sync();
             const long long key0 = (long long)j * kPfBN;
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         report_range();
         // ---- epilogue: O / l for this row
-        if (ok) ok = mbar_wait(&bars->done, 0, p.err);
+        if (ok) ok = mbar_wait<TW>(&bars->done, 0, p.err);
         if (!ok) *abort_flag = 1;
         tc::fence_after_sync();
         const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -534,6 +539,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
 }
 
+cudaError_t set_wait_limit_prefill(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -574,11 +581,12 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     pp.out_bf16 = out_dtype == KV_BF16;
     pp.lse = lse_out;
     pp.err = p->err;
+    auto fn = test_waits_enabled() ? prefill_kernel<true> : prefill_kernel<false>;
     if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
-            prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes)))
+            fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes)))
         return st0;
     const dim3 grid(num_q_heads, (max_q_len + kPfBM - 1) / kPfBM, batch);
-    prefill_kernel<<<grid, kPfThreads, kPfSmemBytes, as_stream(stream)>>>(tm_q, p->tmap_k,
+    fn<<<grid, kPfThreads, kPfSmemBytes, as_stream(stream)>>>(tm_q, p->tmap_k,
                                                                          p->tmap_v, pp);
     return cuda_status(cudaGetLastError());
 }

@@ -157,6 +157,8 @@ static CUmemAllocationProp page_prop(int device) {
     return prop;
 }
 
+std::atomic<int> pkv::g_fail_page_create_after{-1};
+
 // A physical page for a mapping: a spare one if the pool has it, else a new one.
 static bool take_page(kv_contig *c, CUmemGenericAllocationHandle *h) {
     {
@@ -170,6 +172,11 @@ static bool take_page(kv_contig *c, CUmemGenericAllocationHandle *h) {
         }
         c->pp.created += 1;
     }
+    // test hook: the creation after `after` more successful ones fails, once
+    int after = g_fail_page_create_after.load();
+    while (after >= 0 && !g_fail_page_create_after.compare_exchange_weak(after, after - 1)) {
+    }
+    if (after == 0) return false;
     const CUmemAllocationProp prop = page_prop(c->device);
     return driver().create(h, c->page, &prop, 0) == CUDA_SUCCESS;
 }
@@ -583,6 +590,11 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
 kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable) {
     if (!c || (enable != 0 && enable != 1)) return KV_ERR_ARG;
     c->launch_overlap = enable != 0;
+    return KV_OK;
+}
+
+kv_status kv_debug_fail_page_create(int after) {
+    g_fail_page_create_after.store(after < 0 ? -1 : after);
     return KV_OK;
 }
 
