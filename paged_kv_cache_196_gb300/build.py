@@ -38,6 +38,21 @@ def _inputs():
     return deps
 
 
+def _shared_inputs():
+    """Headers every translation unit may include, and this script."""
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    deps.append(os.path.join(INCLUDE, "paged_kv.h"))
+    deps.append(os.path.abspath(__file__))
+    return deps
+
+
+def _stale(src: str, shared_mtime: float) -> bool:
+    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+    if not os.path.exists(obj):
+        return True
+    return os.path.getmtime(obj) < max(shared_mtime, os.path.getmtime(os.path.join(CSRC, src)))
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
     cmd = [nvcc()] + ARCH + FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
@@ -58,8 +73,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if os.path.getmtime(LIB) >= newest:
             return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
+    # recompile only the sources newer than their object (or all of them when
+    # a shared header or this script changed)
+    shared = max(os.path.getmtime(p) for p in _shared_inputs())
+    todo = [s for s in SOURCES if force or verbose or _stale(s, shared)]
+    with cf.ThreadPoolExecutor(max_workers=max(1, len(todo))) as ex:
+        list(ex.map(lambda s: _compile(s, verbose), todo))
+    objs = [os.path.join(OUT_DIR, s + ".o") for s in SOURCES]
     tmp = LIB + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)

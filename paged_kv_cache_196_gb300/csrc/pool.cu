@@ -45,35 +45,56 @@ int sm_count() {
     return n > 0 ? n : 1;
 }
 
-// One thread moves one 16-byte chunk of K and the matching chunk of V.
-// Layout: k_new/v_new [T][Hkv][row_chunks] (16-byte chunks of a head row);
-// pools [NB][Hkv][BS][row_chunks].
-__global__ void __launch_bounds__(256) append_kernel(uint4 *__restrict__ k_pool,
-                                                     uint4 *__restrict__ v_pool,
-                                                     const uint4 *__restrict__ k_new,
-                                                     const uint4 *__restrict__ v_new,
-                                                     const int64_t *__restrict__ slots,
-                                                     long long total_chunks, int hkv,
-                                                     int row_chunks, int block_size,
-                                                     long long num_slots, int *err) {
-    const int per_token = hkv * row_chunks;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total_chunks;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long t = i / per_token;
-        const int rem = (int)(i - t * per_token);
-        const int h = rem / row_chunks, c = rem - h * row_chunks;
-        const int64_t slot = __ldg(slots + t);
-        if (slot < 0) continue;
-        if (slot >= num_slots) {
-            if (rem == 0) atomicOr(err, KV_DEVERR_SLOT_RANGE);
-            continue;
+// Append.  Work item i is 16-byte chunk c of kv head h of token t:
+// i = (t * hkv + h) * row_chunks + c, with k_new / v_new laid out
+// [T][Hkv][row_chunks] and the pools [NB][Hkv][16][row_chunks].  Each thread
+// takes kAppendUnroll items a grid apart and issues all their loads before
+// its stores (more bytes in flight per thread).  Idx is 32-bit when the item
+// count allows it (the host decides): the token index costs a 32-bit division
+// instead of a 64-bit one.  row_chunks is a power of two and the block size
+// is 16, so the rest is shifts and masks.
+constexpr int kAppendUnroll = 2;
+constexpr int kAppendThreads = 256;
+
+template <typename Idx>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(uint4 *__restrict__ k_pool,
+                                                                uint4 *__restrict__ v_pool,
+                                                                const uint4 *__restrict__ k_new,
+                                                                const uint4 *__restrict__ v_new,
+                                                                const int64_t *__restrict__ slots,
+                                                                Idx total, int hkv, int rc_log2,
+                                                                long long num_slots, int *err) {
+    const Idx per_token = (Idx)hkv << rc_log2;
+    const Idx stride = (Idx)gridDim.x * kAppendThreads;
+    const int rc_mask = (1 << rc_log2) - 1;
+    for (Idx base = (Idx)blockIdx.x * kAppendThreads + threadIdx.x; base < total;
+         base += stride * kAppendUnroll) {
+        uint4 kv[kAppendUnroll], vv[kAppendUnroll];
+        long long dst[kAppendUnroll];
+#pragma unroll
+        for (int u = 0; u < kAppendUnroll; ++u) {
+            const Idx i = base + (Idx)u * stride;
+            dst[u] = -1;
+            if (i < total) {
+                const Idx t = i / per_token;
+                const int rem = (int)(i - t * per_token);
+                const int64_t slot = __ldg(slots + t);
+                if (slot >= num_slots) {
+                    if (rem == 0) atomicOr(err, KV_DEVERR_SLOT_RANGE);
+                } else if (slot >= 0) {
+                    const long long row = ((slot >> 4) * hkv + (rem >> rc_log2)) * 16 + (slot & 15);
+                    dst[u] = (row << rc_log2) + (rem & rc_mask);
+                    kv[u] = __ldg(k_new + i);
+                    vv[u] = __ldg(v_new + i);
+                }
+            }
         }
-        const long long blk = slot / block_size, off = slot - blk * block_size;
-        const long long dst = ((blk * hkv + h) * block_size + off) * row_chunks + c;
-        const uint4 kv = __ldg(k_new + i);
-        const uint4 vv = __ldg(v_new + i);
-        k_pool[dst] = kv;
-        v_pool[dst] = vv;
+#pragma unroll
+        for (int u = 0; u < kAppendUnroll; ++u)
+            if (dst[u] >= 0) {
+                k_pool[dst[u]] = kv[u];
+                v_pool[dst[u]] = vv[u];
+            }
     }
 }
 
@@ -275,12 +296,26 @@ kv_status kv_append(kv_pool_t p, const void *k_new, const void *v_new,
     if (!k_new || !v_new || !slot_mapping) return KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
         return KV_ERR_ARG;  // rows are moved as 16-byte chunks
-    const int row_chunks = p->head_dim * dtype_bytes(p->dtype) / 16;
+    const int row_chunks = p->head_dim * dtype_bytes(p->dtype) / 16;  // 8, 16 or 32
+    const int rc_log2 = row_chunks == 8 ? 3 : row_chunks == 16 ? 4 : 5;
     const long long total = (long long)num_tokens * p->num_kv_heads * row_chunks;
-    append_kernel<<<grid_for(total, 256), 256, 0, as_stream(stream)>>>(
-        (uint4 *)p->k, (uint4 *)p->v, (const uint4 *)k_new, (const uint4 *)v_new, slot_mapping,
-        total, p->num_kv_heads, row_chunks, p->block_size,
-        (long long)p->num_blocks * p->block_size, p->err);
+    // eight CTAs per SM at most (full occupancy); fewer for small appends
+    long long blocks = (total + (long long)kAppendThreads * kAppendUnroll - 1) /
+                       ((long long)kAppendThreads * kAppendUnroll);
+    const long long cap = 8LL * sm_count();
+    if (blocks > cap) blocks = cap;
+    // a whole number of CTAs per SM
+    if (blocks > sm_count()) blocks = (blocks + sm_count() - 1) / sm_count() * sm_count();
+    const long long span = blocks * kAppendThreads * kAppendUnroll;  // one loop step of the grid
+    const long long num_slots = (long long)p->num_blocks * p->block_size;
+    if (total + span < (1LL << 31))
+        append_kernel<uint32_t><<<(int)blocks, kAppendThreads, 0, as_stream(stream)>>>(
+            (uint4 *)p->k, (uint4 *)p->v, (const uint4 *)k_new, (const uint4 *)v_new,
+            slot_mapping, (uint32_t)total, p->num_kv_heads, rc_log2, num_slots, p->err);
+    else
+        append_kernel<unsigned long long><<<(int)blocks, kAppendThreads, 0, as_stream(stream)>>>(
+            (uint4 *)p->k, (uint4 *)p->v, (const uint4 *)k_new, (const uint4 *)v_new,
+            slot_mapping, (unsigned long long)total, p->num_kv_heads, rc_log2, num_slots, p->err);
     return cuda_status(cudaGetLastError());
 }
 
