@@ -361,27 +361,50 @@ def run_ours(args, rank, world, local_rank):
     value = job_throughput(kv_bytes, K, world, total_ms) / 1e9
     tokens_per_s = job_throughput(B, K, world, total_ms)
 
-    # ---- end to end through the public API with host buffers: each step copies
-    # its inputs (q, the new k/v, the slots or positions, the lengths, the
-    # grid order or schedule) from a pinned host buffer in a single transfer,
-    # runs the step on views of the device copy, and reads its output back.
-    # Two input and two output buffers: step i's inputs travel on a copy
-    # stream while step i - 1 computes, its output travels back on another
-    # while step i + 1 computes (the steps themselves stay in order on the
-    # compute stream).
+    # ---- end to end through the public API with host buffers: each step plans
+    # its grid order (or balanced schedule) on the host from the host copy of
+    # the lengths, copies its inputs (q, the new k/v, the slots or positions,
+    # the lengths, the order or schedule) from a pinned host buffer in a
+    # single transfer, runs the step on views of the device copy, and reads
+    # its output back.  Two pinned input buffers, two device input buffers and
+    # two output buffers: step i's inputs travel on a copy stream while step
+    # i - 1 computes, its output travels back on another while step i + 1
+    # computes (the steps themselves stay in order on the compute stream).
+    # Every step is the same decode step (same lengths, same slots), so the
+    # slot mapping is planned once, before the loop.
     Ke = min(K, 2000)
     h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu(),
                torch.from_numpy(last.astype(np.int32) if contig else slots), torch.from_numpy(lens)]
-    if not contig:  # recomputed on the host for every batch
+    if not contig:
         h_parts.append(torch.from_numpy(h_sched if balanced else h_order))
     offs, total = [], 0
     for t in h_parts:
         offs.append(total)
         total += (t.numel() * t.element_size() + 255) // 256 * 256
-    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for t, o in zip(h_parts, offs):
-        n = t.numel() * t.element_size()
-        h_in[o:o + n].view(t.dtype).copy_(t.reshape(-1))
+    h_ins = [torch.empty(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    for h_in in h_ins:
+        for t, o in zip(h_parts, offs):
+            n = t.numel() * t.element_size()
+            h_in[o:o + n].view(t.dtype).copy_(t.reshape(-1))
+    # numpy views of each pinned buffer's order / schedule slot, planned into per step
+    plan_views = []
+    if not contig:
+        pt, po = h_parts[5], offs[5]
+        for h_in in h_ins:
+            plan_views.append(h_in[po:po + pt.numel() * 4].view(torch.int32).numpy())
+
+    sched_scratch = (np.zeros(pk.kv_decode_schedule_capacity(B, hkv, max_blocks), np.int32)
+                     if balanced else None)
+
+    def plan(dst):
+        if balanced:  # planned at the capacity bound, the used part copied in
+            used = pk.kv_decode_schedule(lens.astype(np.int32), hkv, max_blocks,
+                                         num_ctas=args.sched_ctas, ring_stages=args.sched_ring,
+                                         flags=pk.KV_SCHED_WHOLE_PIECES if args.sched_whole else 0,
+                                         out=sched_scratch)
+            dst[:len(used)] = used
+        else:
+            pk.kv_decode_order(lens.astype(np.int32), dst)
     d_ins = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
     bufs = []
     for d_in in d_ins:
@@ -422,9 +445,12 @@ def run_ours(args, rank, world, local_rank):
     e0.record(s_comp)
     for i in range(Ke):
         bi = i % 2
+        if plan_views:
+            ev_in[bi].synchronize()  # step i - 2's copy out of this pinned buffer is done
+            plan(plan_views[bi])
         s_in.wait_event(ev_comp[bi])  # step i - 2 has read this input buffer
         with torch.cuda.stream(s_in):
-            d_ins[bi].copy_(h_in, non_blocking=True)
+            d_ins[bi].copy_(h_ins[bi], non_blocking=True)
         ev_in[bi].record(s_in)
         s_comp.wait_event(ev_in[bi])
         s_comp.wait_event(ev_out[bi])  # step i - 2's output has been read back

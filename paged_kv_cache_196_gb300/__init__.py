@@ -454,20 +454,26 @@ KV_SCHED_WHOLE_PIECES = 1
 
 
 def kv_decode_schedule(host_seq_lens, num_kv_heads: int, max_blocks: int, num_sms: int = 0,
-                       num_ctas: int = 0, ring_stages: int = 0, flags: int = 0):
+                       num_ctas: int = 0, ring_stages: int = 0, flags: int = 0, out=None):
     """Balanced decode schedule for these host int32 lengths: an int32 numpy
     array (header, first piece of each CTA, pieces) to copy to the device for
     paged_decode_attention_scheduled.  num_sms = 0: the current device's;
-    num_ctas / ring_stages = 0: the library's rule."""
+    num_ctas / ring_stages = 0: the library's rule.  With `out` (a contiguous
+    int32 host array) the schedule is written there and a view of its used
+    part is returned."""
     import numpy as _np
     lens = _np.ascontiguousarray(host_seq_lens, dtype=_np.int32)
-    cap = kv_decode_schedule_capacity(len(lens), num_kv_heads, max_blocks, num_sms)
-    out = _np.zeros(cap, _np.int32)
+    if out is None:
+        cap = kv_decode_schedule_capacity(len(lens), num_kv_heads, max_blocks, num_sms)
+        buf = _np.zeros(cap, _np.int32)
+    else:
+        buf = out
     used = _sz()
     _check(lib().kv_decode_schedule(_ptr(lens), len(lens), num_kv_heads, max_blocks, num_sms,
-                                    num_ctas, ring_stages, flags, _ptr(out), cap, ctypes.byref(used)),
+                                    num_ctas, ring_stages, flags, _ptr(buf), len(buf),
+                                    ctypes.byref(used)),
            "kv_decode_schedule")
-    return out[:used.value].copy()
+    return buf[:used.value].copy() if out is None else buf[:used.value]
 
 
 def kv_decode_schedule_workspace_size(host_schedule, num_q_heads: int, head_dim: int) -> int:
