@@ -9,7 +9,8 @@ numpy arrays in and out of it.  ``brute.py`` holds a second, pure-Python
 statement used to pin the C code on tiny inputs.
 
 Element arrays: fp32 data is ``np.float32``; bfloat16 data is ``np.uint16``
-holding the bf16 bit pattern.  The dtype code is taken from the array.
+holding the bf16 bit pattern; IEEE half precision is ``np.float16``.  The
+dtype code is taken from the array.
 """
 import ctypes
 import os
@@ -53,6 +54,8 @@ def lib():
         L.oracle_attend_logical.restype = None
         L.oracle_attend_logical.argtypes = [vp, vp, vp, i64, i32, i32, i32, dbl, vp, vp]
         L.oracle_num_threads.restype = i32
+        L.oracle_half_to_double.restype = None
+        L.oracle_half_to_double.argtypes = [vp, i64, vp]
         _lib = L
     return _lib
 
@@ -62,7 +65,9 @@ def _code(a: np.ndarray) -> int:
         return 0
     if a.dtype == np.uint16:
         return 1
-    raise TypeError(f"oracle takes float32 or uint16(bf16 bits) arrays, got {a.dtype}")
+    if a.dtype == np.float16:
+        return 2
+    raise TypeError(f"oracle takes float32, uint16 (bf16 bits) or float16 arrays, got {a.dtype}")
 
 
 def _p(a: np.ndarray):
@@ -201,3 +206,11 @@ def attend_logical(q, K, V, h, scale):
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to fp64, for comparisons."""
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def half_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """The oracle's own exact widening of binary16 bit patterns (uint16) to fp64."""
+    bits = _c(bits, np.uint16)
+    out = np.empty(bits.shape, np.float64)
+    lib().oracle_half_to_double(_p(bits), bits.size, _p(out))
+    return out

@@ -43,7 +43,8 @@
  *   - an empty context gives o = 0 and lse = -infinity.
  *
  * Element types: dtype 0 = IEEE fp32, dtype 1 = bfloat16 (upper half of an
- * fp32 bit pattern).  Both convert exactly to fp64.
+ * fp32 bit pattern), dtype 2 = IEEE binary16 (half precision).  All three
+ * convert exactly to fp64.
  */
 #include <math.h>
 #include <stdint.h>
@@ -54,12 +55,32 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
 
-static int elem_size(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
+static int elem_size(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits.  Exponent field 0: subnormal, value = fraction * 2^-24; 31: infinity
+ * (fraction 0) or NaN; otherwise (1024 + fraction) * 2^(exponent - 25). */
+static double half_to_double(uint16_t h) {
+    const int sign = h >> 15, expo = (h >> 10) & 0x1f, frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);
+    return sign ? -v : v;
+}
 
 /* Exact widening of one stored element to fp64. */
 static double load_elem(const void *base, int64_t idx, int dtype) {
+    if (dtype == OR_F16) {
+        uint16_t h;
+        memcpy(&h, (const char *)base + 2 * idx, 2);
+        return half_to_double(h);
+    }
     if (dtype == OR_BF16) {
         uint16_t h;
         memcpy(&h, (const char *)base + 2 * idx, 2);
@@ -356,3 +377,8 @@ void oracle_attend_logical(const double *q, const double *K, const double *V,
 }
 
 int oracle_elem_size(int dtype) { return elem_size(dtype); }
+
+/* The exact fp64 value of each of n binary16 bit patterns (for the pins). */
+void oracle_half_to_double(const uint16_t *h, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = half_to_double(h[i]);
+}

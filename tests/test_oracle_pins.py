@@ -64,28 +64,48 @@ def _slots_for(table, n):
     return np.array([table[j // BS] * BS + j % BS for j in range(n)], np.int64)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+SENTINEL = {"f32": W.NAN_F32, "bf16": W.NAN_BF16, "f16": W.NAN_F16}
+
+
+def _widen(a, dtype):
+    """Exact fp64 values of stored elements, by numpy (not the oracle)."""
+    return (W.bf16_bits_to_f32(a) if dtype == "bf16" else a).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_append_then_gather_round_trip(dtype):
     g = W.rng(5)
     nb, hkv, d, n = 12, 3, 64, 41
     table = W.permutation(g, nb)[: oracle.blocks_needed(n, BS)]
-    pk = W.empty_pool(nb, hkv, d, dtype, W.NAN_BF16 if dtype == "bf16" else W.NAN_F32)
+    pk = W.empty_pool(nb, hkv, d, dtype, SENTINEL[dtype])
     pv = pk.copy()
     k = W.normal(g, (n, hkv, d), dtype)
     v = W.normal(g, (n, hkv, d), dtype)
     slots = _slots_for(table, n)
     oracle.append(pk, pv, k, v, slots)
-    kf = W.bf16_bits_to_f32(k) if dtype == "bf16" else k
-    vf = W.bf16_bits_to_f32(v) if dtype == "bf16" else v
-    np.testing.assert_array_equal(oracle.gather_logical(pk, table, n), kf.astype(np.float64))
-    np.testing.assert_array_equal(oracle.gather_logical(pv, table, n), vf.astype(np.float64))
+    np.testing.assert_array_equal(oracle.gather_logical(pk, table, n), _widen(k, dtype))
+    np.testing.assert_array_equal(oracle.gather_logical(pv, table, n), _widen(v, dtype))
     # Every slot not named by the mapping keeps its sentinel bits.
     written = np.zeros(nb * BS, bool)
     written[slots] = True
     flat = pk.reshape(nb, hkv, BS, d).transpose(0, 2, 1, 3).reshape(nb * BS, -1)
-    sentinel = W.NAN_BF16 if dtype == "bf16" else W.NAN_F32
-    raw = flat.view(np.uint16 if dtype == "bf16" else np.uint32)
-    assert np.all(raw[~written] == sentinel)
+    raw = flat.view(np.uint32 if dtype == "f32" else np.uint16)
+    assert np.all(raw[~written] == SENTINEL[dtype])
+
+
+def test_half_precision_widening_for_every_bit_pattern():
+    """IEEE 754 binary16 -> fp64 (the oracle's own decode) against numpy's
+    float16 for all 65536 patterns: normals, subnormals, zeros, infinities,
+    NaNs."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+    # a few values by their definition
+    assert oracle.half_bits_to_f64(np.array([0x3C00, 0x0001, 0x7BFF, 0xC000], np.uint16)).tolist() == \
+        [1.0, 2.0 ** -24, 65504.0, -2.0]
 
 
 def test_append_skips_negative_slots():
@@ -161,11 +181,11 @@ def test_physical_placement_does_not_change_the_result():
     np.testing.assert_array_equal(lse1, lse2)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_matches_exact_brute_force(dtype):
     lens, tables, pk, pv, q = _tiny_case(seed=3, lens=(35, 17, 1, 16), nb=24, dtype=dtype)
     out, lse = oracle.paged_decode(pk, pv, tables, lens, q, 0.125)
-    f = W.bf16_bits_to_f32 if dtype == "bf16" else (lambda a: a)
+    f = lambda a: _widen(a, dtype)  # noqa: E731
     bo, bl = brute.paged_decode(f(pk), f(pv), tables, lens, f(q), 0.125, BS)
     np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-13)
     np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-13)

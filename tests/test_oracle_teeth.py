@@ -33,6 +33,10 @@ MUTANTS = {
     "no_max_subtraction": ("double w = exp(s[j] - m);", "double w = exp(s[j]);"),
     "slot_split_swapped": ("int64_t block = slot / block_size, offset = slot % block_size;",
                            "int64_t block = slot % block_size, offset = slot / block_size;"),
+    "half_exponent_bias": ("v = ldexp((double)(1024 + frac), expo - 25);",
+                           "v = ldexp((double)(1024 + frac), expo - 24);"),
+    "half_subnormal_as_normal": ("        v = ldexp((double)frac, -24);",
+                                 "        v = ldexp((double)(1024 + frac), -24);"),
 }
 
 

@@ -11,7 +11,8 @@ The shapes stand in for the workloads the vAttention and PagedAttention
 evaluations use (Llama-3-8B / Yi-6B / Yi-34B head layouts, contexts up to
 192K tokens); no model weights or traces are involved.
 
-bfloat16 data is carried as ``np.uint16`` bit patterns; fp32 as ``np.float32``.
+bfloat16 data is carried as ``np.uint16`` bit patterns; fp32 as ``np.float32``;
+IEEE half precision as ``np.float16``.
 """
 import numpy as np
 
@@ -66,9 +67,14 @@ def bf16_bits_to_f32(u: np.ndarray) -> np.ndarray:
 
 
 def normal(g: np.random.Generator, shape, dtype: str) -> np.ndarray:
-    """N(0, 1) samples drawn in fp32; bf16 data is rounded once from them."""
+    """N(0, 1) samples drawn in fp32; bf16 and f16 data are rounded once from
+    them (round to nearest, ties to even)."""
     x = g.standard_normal(size=shape, dtype=np.float32)
-    return to_bf16_bits(x) if dtype == "bf16" else x
+    if dtype == "bf16":
+        return to_bf16_bits(x)
+    if dtype == "f16":
+        return x.astype(np.float16)
+    return x
 
 
 def lengths(g: np.random.Generator, cfg: dict) -> np.ndarray:
@@ -95,6 +101,8 @@ def empty_pool(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: str,
     shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim)
     if dtype == "bf16":
         return np.full(shape, 0 if fill is None else fill, np.uint16)
+    if dtype == "f16":
+        return np.full(shape, 0 if fill is None else fill, np.uint16).view(np.float16)
     a = np.zeros(shape, np.float32)
     if fill is not None:
         a.view(np.uint32)[...] = fill
@@ -102,6 +110,7 @@ def empty_pool(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: str,
 
 
 NAN_BF16 = 0x7FC1      # quiet-NaN bit patterns used as "never written" sentinels
+NAN_F16 = 0x7E01
 NAN_F32 = 0x7FC00001
 
 
