@@ -30,8 +30,9 @@
  *     for it checks that this device is current; a call made while another
  *     device is current returns KV_ERR_ARG and launches nothing.  The
  *     destroy calls switch to the object's device to free it and switch back.
- *   - Element types: KV_F32 (IEEE fp32) or KV_BF16 (bfloat16).  q, k_new and
- *     v_new use the pool's type; out may be KV_F32 or the pool's type.
+ *   - Element types: KV_F32 (IEEE fp32), KV_BF16 (bfloat16) or KV_F16 (IEEE
+ *     half precision).  q, k_new and v_new use the pool's type; out may be
+ *     KV_F32 or the pool's type.  The cascade decode takes bf16 pools only.
  *   - head_dim must be 64 or 128, block_size must be 16, num_q_heads must be
  *     a multiple of num_kv_heads with num_q_heads / num_kv_heads <= 8.
  *
@@ -62,7 +63,8 @@ typedef enum {
     KV_ERR_STATE = -7           /* call not valid in the object's current state */
 } kv_status;
 
-typedef enum { KV_F32 = 0, KV_BF16 = 1 } kv_dtype;
+/* Element types: IEEE fp32, bfloat16, IEEE half precision (binary16). */
+typedef enum { KV_F32 = 0, KV_BF16 = 1, KV_F16 = 2 } kv_dtype;
 
 /* Bits of the device error word. */
 #define KV_DEVERR_BLOCK_RANGE 0x1   /* block-table entry outside [0, num_blocks) */

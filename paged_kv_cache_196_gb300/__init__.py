@@ -15,7 +15,7 @@ import os
 from . import build as _build
 
 __all__ = [
-    "KVError", "lib", "KV_F32", "KV_BF16", "kv_status_string", "kv_last_cuda_error", "kv_blocks_for_tokens",
+    "KVError", "lib", "KV_F32", "KV_BF16", "KV_F16", "kv_status_string", "kv_last_cuda_error", "kv_blocks_for_tokens",
     "kv_allocator_create", "kv_allocator_destroy", "kv_allocator_set_order",
     "kv_allocator_alloc", "kv_allocator_share", "kv_allocator_free", "kv_allocator_refcount",
     "kv_allocator_num_free", "kv_prepare_append", "kv_prepare_append_batch",
@@ -36,6 +36,7 @@ __all__ = [
 
 KV_F32 = 0
 KV_BF16 = 1
+KV_F16 = 2
 KV_WAIT_LIMIT_DEFAULT_NS = 2000000000
 
 STATUS = {0: "KV_OK", -1: "KV_ERR_ARG", -2: "KV_ERR_OOM", -3: "KV_ERR_UNSUPPORTED",

@@ -154,4 +154,33 @@ KV_DEVICE uint16_t float_to_bf16_rn(float f) {
 
 KV_DEVICE float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
+// ---------------------------------------------------------------- fp16
+// Two IEEE half-precision values (a 32-bit word, low half = lower index) as fp32
+// (exact).
+KV_DEVICE float2 f16x2_to_float2(uint32_t w) {
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+    return make_float2(lo, hi);
+}
+
+KV_DEVICE uint16_t float_to_f16_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+// One output element, stored as the call's output type (KV_F32, KV_BF16 or
+// KV_F16; 16-bit outputs rounded to nearest even).
+KV_DEVICE void store_out(void *out, size_t idx, float v, int out_type) {
+    if (out_type == KV_F32)
+        reinterpret_cast<float *>(out)[idx] = v;
+    else if (out_type == KV_BF16)
+        reinterpret_cast<uint16_t *>(out)[idx] = float_to_bf16_rn(v);
+    else
+        reinterpret_cast<uint16_t *>(out)[idx] = float_to_f16_rn(v);
+}
+
 }  // namespace pkv

@@ -108,7 +108,7 @@ struct DecodeKParams {
     // for it before touching memory, and lets the next launch begin at once
     int chain;
     void *out;
-    int out_bf16;
+    int out_type;  // kv_dtype of out
     float *lse;
     float *ws_o;
     float *ws_lse;
@@ -116,30 +116,40 @@ struct DecodeKParams {
     int *err;
 };
 
-template <int D, bool BF16>
+// Element types of the pool (the kv_dtype values): ET = KV_F32, KV_BF16 or KV_F16.
+template <int D, int ET>
 struct TileShape {
-    static constexpr int kElem = BF16 ? 2 : 4;
+    static constexpr int kElem = ET == KV_F32 ? 4 : 2;
     static constexpr int kBytes = kBS * D * kElem;  // one (block, kv head) tile
     static constexpr int kDPL = D / 16;             // dimensions per lane
     static constexpr int kPairs = kDPL / 2;
 };
 
+// Two 16-bit elements of type ET as fp32 (exact).
+template <int ET>
+KV_DEVICE float2 half2_to_float2(uint32_t w) {
+    if constexpr (ET == KV_BF16)
+        return bf16x2_to_float2(w);
+    else
+        return f16x2_to_float2(w);
+}
+
 // Loads this lane's kDPL dimensions of row t of a tile as fp32 pairs.
-template <int D, bool BF16>
-KV_DEVICE void load_row(const char *tile, int t, int c, float2 (&x)[TileShape<D, BF16>::kPairs]) {
-    using S = TileShape<D, BF16>;
+template <int D, int ET>
+KV_DEVICE void load_row(const char *tile, int t, int c, float2 (&x)[TileShape<D, ET>::kPairs]) {
+    using S = TileShape<D, ET>;
     const char *row = tile + (size_t)t * D * S::kElem + (size_t)c * S::kDPL * S::kElem;
-    if constexpr (BF16) {
+    if constexpr (ET != KV_F32) {
         if constexpr (S::kDPL == 8) {
             const uint4 w = *reinterpret_cast<const uint4 *>(row);
-            x[0] = bf16x2_to_float2(w.x);
-            x[1] = bf16x2_to_float2(w.y);
-            x[2] = bf16x2_to_float2(w.z);
-            x[3] = bf16x2_to_float2(w.w);
+            x[0] = half2_to_float2<ET>(w.x);
+            x[1] = half2_to_float2<ET>(w.y);
+            x[2] = half2_to_float2<ET>(w.z);
+            x[3] = half2_to_float2<ET>(w.w);
         } else {
             const uint2 w = *reinterpret_cast<const uint2 *>(row);
-            x[0] = bf16x2_to_float2(w.x);
-            x[1] = bf16x2_to_float2(w.y);
+            x[0] = half2_to_float2<ET>(w.x);
+            x[1] = half2_to_float2<ET>(w.y);
         }
     } else {
 #pragma unroll
@@ -174,9 +184,9 @@ KV_DEVICE void reduce_scatter16(float *v, int lane) {
 }
 
 // Bytes of the stage ring; the final cross-warp merge reuses it.
-template <int D, int G, bool BF16>
+template <int D, int G, int ET>
 constexpr size_t decode_ring_bytes(int nstage = kNStage) {
-    const size_t ring = (size_t)nstage * 2 * TileShape<D, BF16>::kBytes;
+    const size_t ring = (size_t)nstage * 2 * TileShape<D, ET>::kBytes;
     constexpr size_t merge =
         (size_t)kNW * (G * D + 2 * G) * sizeof(float) + (G * kFuseMaxSplits + 4) * sizeof(float);
     return ((ring > merge ? ring : merge) + 127) / 128 * 128;
@@ -246,10 +256,7 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
         const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
         const size_t row = (size_t)b * p.num_q_heads + h * p.g + j;
         if (ntot == 1) {
-            if (p.out_bf16)
-                reinterpret_cast<uint16_t *>(p.out)[row * D + d] = float_to_bf16_rn(o);
-            else
-                reinterpret_cast<float *>(p.out)[row * D + d] = o;
+            store_out(p.out, row * D + d, o, p.out_type);
             if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
         } else {
             p.ws_o[(row * p.max_splits + p.part_base + split) * D + d] = o;
@@ -303,12 +310,12 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
             acc.z += ws * v.z;
             acc.w += ws * v.w;
         }
-        if (p.out_bf16) {
-            uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + row * D + 4 * d4;
-            o[0] = float_to_bf16_rn(acc.x);
-            o[1] = float_to_bf16_rn(acc.y);
-            o[2] = float_to_bf16_rn(acc.z);
-            o[3] = float_to_bf16_rn(acc.w);
+        if (p.out_type != KV_F32) {
+            const size_t o0 = row * D + 4 * d4;
+            store_out(p.out, o0, acc.x, p.out_type);
+            store_out(p.out, o0 + 1, acc.y, p.out_type);
+            store_out(p.out, o0 + 2, acc.z, p.out_type);
+            store_out(p.out, o0 + 3, acc.w, p.out_type);
         } else {
             reinterpret_cast<float4 *>(p.out)[(row * D) / 4 + d4] = acc;
         }
@@ -319,9 +326,9 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
 // HS = 1: the two half-warps take different tokens (2 per pass) and every
 // lane carries all G heads.  HS = 2: both halves take the same token and each
 // carries G/2 heads (half the q and accumulator registers, for large G).
-template <int D, int G, int HS, bool BF16, bool LINEAR>
+template <int D, int G, int HS, int ET, bool LINEAR>
 __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kernel(const DecodeKParams p) {
-    using S = TileShape<D, BF16>;
+    using S = TileShape<D, ET>;
     constexpr int kTile = S::kBytes;
     constexpr int kPairs = S::kPairs;
     constexpr int GH = G / HS;                 // heads per lane
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
     // ---- shared memory
     extern __shared__ __align__(128) char smem[];
     char *stages = smem;                                                   // kNStage x (K, V)
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + decode_ring_bytes<D, G, BF16>());
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + decode_ring_bytes<D, G, ET>());
     uint64_t *empty = full + kNStage;
     int *stage_valid = reinterpret_cast<int *>(empty + kNStage);
     float2 *pscr = reinterpret_cast<float2 *>(stage_valid + kNStage);      // [kNW][16][G]
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
         if (jj < p.g) {
             const size_t base = ((size_t)b * p.num_q_heads + h * p.g + jj) * D + c * S::kDPL;
             float2 x[kPairs];
-            load_row<D, BF16>(reinterpret_cast<const char *>(p.q) + base * S::kElem, 0, 0, x);
+            load_row<D, ET>(reinterpret_cast<const char *>(p.q) + base * S::kElem, 0, 0, x);
 #pragma unroll
             for (int m = 0; m < kPairs; ++m)
                 qv[j][m] = make_float2(x[m].x * p.scale_log2, x[m].y * p.scale_log2);
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
         for (int pass = 0; pass < kPasses; ++pass) {
             const int t = HS == 1 ? 2 * pass + hf : pass;
             float2 kx[kPairs];
-            load_row<D, BF16>(kt, t, c, kx);
+            load_row<D, ET>(kt, t, c, kx);
             float part[GH];
 #pragma unroll
             for (int j = 0; j < GH; ++j) {
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
             for (int pass = 0; pass < kPasses; ++pass) {
                 const int t = HS == 1 ? 2 * pass + hf : pass;
                 float2 vx[kPairs];
-                load_row<D, BF16>(vt, t, c, vx);
+                load_row<D, ET>(vt, t, c, vx);
                 const float2 *prow = pw + t * G + hoff;
 #pragma unroll
                 for (int j = 0; j < GH; ++j) {
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeMinBlocks) decode_kerne
                 const int t = HS == 1 ? 2 * pass + hf : pass;
                 if (t < ntok) {
                     float2 vx[kPairs];
-                    load_row<D, BF16>(vt, t, c, vx);
+                    load_row<D, ET>(vt, t, c, vx);
                     const float2 *prow = pw + t * G + hoff;
 #pragma unroll
                     for (int j = 0; j < GH; ++j) {
@@ -648,6 +655,20 @@ KV_DEVICE void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, ui
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// d += A(16x16 fp16, row) * B(16x8 fp16, col), fp32 accumulate
+KV_DEVICE void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                       uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+KV_DEVICE uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 KV_DEVICE uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -686,7 +707,10 @@ KV_DEVICE void q_fragment(const uint2 *qs, int kk, int lane, uint32_t &q0, uint3
 // into bf16 hi + lo parts.  kt / vt: shared addresses of the block's swizzled
 // K and V tiles; ntok: valid tokens in the block (the rest are masked, their V
 // lanes zeroed).  State (m_run, l_run, o) is this lane's share.
-template <typename QF>
+// F16: the pool, q and the weights are IEEE half precision (one PV MMA with
+// fp16 weights, 11 significant bits); otherwise bf16, the weights split into
+// bf16 hi + lo parts (two PV MMAs).
+template <bool F16, typename QF>
 KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
                                float scale_log2, int lane, float (&m_run)[2], float (&l_run)[2],
                                float (&o)[8][4]) {
@@ -704,7 +728,10 @@ KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
         mma::ldsm_x4(addr, a0, a1, a2, a3);
         uint32_t q0, q1;
         q_fragment(qf, kk, lane, q0, q1);
-        mma::mma_bf16(c, a0, a1, a2, a3, q0, q1);
+        if constexpr (F16)
+            mma::mma_f16(c, a0, a1, a2, a3, q0, q1);
+        else
+            mma::mma_bf16(c, a0, a1, a2, a3, q0, q1);
     }
     // c0,c1: token g, heads 2t,2t+1; c2,c3: token g+8
     const bool v0 = g < ntok, v1 = g + 8 < ntok;
@@ -736,12 +763,20 @@ KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
             o[mt][3] *= al1;
         }
     }
-    // ---- P^T fragments (bf16 hi + lo), via transpose of the S layout
-    const uint32_t h01 = mma::pack_bf16(p0, p1), h23 = mma::pack_bf16(p2, p3);
-    const uint32_t l01 = mma::pack_bf16(p0 - mma::bf16_lo_f(h01), p1 - mma::bf16_hi_f(h01));
-    const uint32_t l23 = mma::pack_bf16(p2 - mma::bf16_lo_f(h23), p3 - mma::bf16_hi_f(h23));
-    const uint32_t bh0 = mma::movm_t(h01), bh1 = mma::movm_t(h23);
-    const uint32_t bl0 = mma::movm_t(l01), bl1 = mma::movm_t(l23);
+    // ---- P^T fragments (fp16, or bf16 hi + lo), via transpose of the S layout
+    uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
+    if constexpr (F16) {
+        bh0 = mma::movm_t(mma::pack_f16(p0, p1));
+        bh1 = mma::movm_t(mma::pack_f16(p2, p3));
+    } else {
+        const uint32_t h01 = mma::pack_bf16(p0, p1), h23 = mma::pack_bf16(p2, p3);
+        const uint32_t l01 = mma::pack_bf16(p0 - mma::bf16_lo_f(h01), p1 - mma::bf16_hi_f(h01));
+        const uint32_t l23 = mma::pack_bf16(p2 - mma::bf16_lo_f(h23), p3 - mma::bf16_hi_f(h23));
+        bh0 = mma::movm_t(h01);
+        bh1 = mma::movm_t(h23);
+        bl0 = mma::movm_t(l01);
+        bl1 = mma::movm_t(l23);
+    }
     // token masks for the V fragments (pairs 2t,2t+1 and 2t+8,2t+9)
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (ntok < kBS) {
@@ -762,15 +797,19 @@ KV_DEVICE void tc_attend_block(const QF &qf, uint32_t kt, uint32_t vt, int ntok,
         a1 &= mlo;
         a2 &= mhi;
         a3 &= mhi;
-        mma::mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-        mma::mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+        if constexpr (F16) {
+            mma::mma_f16(o[mt], a0, a1, a2, a3, bh0, bh1);
+        } else {
+            mma::mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma::mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+        }
     }
 }
 
 
 // NST ring stages (a multiple of kNW: stage st belongs to warp st % kNW),
 // compiled for MINB resident CTAs per SM.
-template <bool LINEAR, int NST, int MINB, bool TW>
+template <bool LINEAR, int NST, int MINB, bool TW, bool F16>
 __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
@@ -822,7 +861,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     char *stages = smem;  // NST x (K tile, V tile), swizzled
-    constexpr size_t kRing = decode_ring_bytes<D, G, true>(NST);
+    constexpr size_t kRing = decode_ring_bytes<D, G, KV_BF16>(NST);
     static_assert(NST % kNW == 0, "each stage must belong to one consumer warp");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
     uint64_t *empty = full + NST;
@@ -951,7 +990,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             __syncwarp();
         }
 
-        tc_attend_block(s_q, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
+        tc_attend_block<F16>(s_q, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
         __syncwarp();
         mbar_arrive(&empty[st]);
     }
@@ -1039,7 +1078,7 @@ KV_DEVICE TcPiece tc_piece(const DecodeKParams &p, int pc, bool report) {
 // slice; it refills the ring as soon as the consumers have read their merge
 // scratch out of it (named barrier 2), so the split merge of one piece
 // overlaps the first copies of the next.  NST ring stages, MINB CTAs per SM.
-template <int NST, int MINB, bool TW>
+template <int NST, int MINB, bool TW, bool F16>
 __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_sched_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                            const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
@@ -1057,7 +1096,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     char *stages = smem;  // NST x (K tile, V tile), swizzled
-    constexpr size_t kRing = decode_ring_bytes<D, G, true>(NST);
+    constexpr size_t kRing = decode_ring_bytes<D, G, KV_BF16>(NST);
     static_assert(NST % kNW == 0, "each stage must belong to one consumer warp");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
     uint64_t *empty = full + NST;
@@ -1225,7 +1264,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
                     __syncwarp();
                 }
 
-                tc_attend_block(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
+                tc_attend_block<F16>(qf, kt, vt, ntok, p.scale_log2, lane, m_run, l_run, o);
                 __syncwarp();
                 mbar_arrive(&empty[st]);
             }
@@ -1266,16 +1305,17 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
 }
 
 // The tensor-core decode kernel for a schedule or a grid plan, ring depth
-// and addressing; TW: the test instantiation (run-time wait limit).
-template <bool TW>
+// and addressing; TW: the test instantiation (run-time wait limit); F16:
+// half-precision pool.
+template <bool TW, bool F16>
 static auto tc_decode_fn(bool sched, bool deep, bool linear) {
-    return sched ? (deep ? decode_tc_sched_kernel<8, 3, TW> : decode_tc_sched_kernel<4, 5, TW>)
-           : deep ? (linear ? decode_tc_kernel<true, 8, 3, TW> : decode_tc_kernel<false, 8, 3, TW>)
-                  : (linear ? decode_tc_kernel<true, 4, 5, TW> : decode_tc_kernel<false, 4, 5, TW>);
+    return sched ? (deep ? decode_tc_sched_kernel<8, 3, TW, F16> : decode_tc_sched_kernel<4, 5, TW, F16>)
+           : deep ? (linear ? decode_tc_kernel<true, 8, 3, TW, F16> : decode_tc_kernel<false, 8, 3, TW, F16>)
+                  : (linear ? decode_tc_kernel<true, 4, 5, TW, F16> : decode_tc_kernel<false, 4, 5, TW, F16>);
 }
 
 static size_t decode_tc_smem_bytes(bool linear, int part_blocks, int nst, int tables) {
-    return 1024 + decode_ring_bytes<128, 8, true>(nst) + 2 * nst * sizeof(uint64_t) +
+    return 1024 + decode_ring_bytes<128, 8, KV_BF16>(nst) + 2 * nst * sizeof(uint64_t) +
            nst * sizeof(int) + 32 * sizeof(uint4) +
            (size_t)(linear ? 0 : tables * part_blocks) * sizeof(int32_t);
 }
@@ -1291,7 +1331,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
                                                     int max_len_tokens, int batch,
                                                     int num_q_heads, int head_dim,
                                                     int part_blocks, int max_splits, void *out,
-                                                    int out_bf16, float *lse, int min_splits,
+                                                    int out_type, float *lse, int min_splits,
                                                     const int32_t *start_tokens, int part_base) {
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -1328,10 +1368,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float *__restrict__ ws
             for (int s = 0; s < ntot; ++s)
                 num += exp2f(ls[slot(s)] - M) * ws_o[((size_t)row * max_splits + slot(s)) * head_dim + d];
         const float o = num * inv;
-        if (out_bf16)
-            reinterpret_cast<uint16_t *>(out)[(size_t)row * head_dim + d] = float_to_bf16_rn(o);
-        else
-            reinterpret_cast<float *>(out)[(size_t)row * head_dim + d] = o;
+        store_out(out, (size_t)row * head_dim + d, o, out_type);
     }
     if (lse && lane == 0) lse[row] = den > 0.f ? (M + log2f(den)) * 0.6931471805599453f : -INFINITY;
 }
@@ -1364,19 +1401,19 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_
     return (size_t)batch * num_q_heads * max_splits * (head_dim + 1) * sizeof(float);
 }
 
-template <int D, int G, bool BF16, bool LINEAR>
+template <int D, int G, int ET, bool LINEAR>
 static size_t decode_smem_bytes(int part_blocks) {
-    return decode_ring_bytes<D, G, BF16>() + 2 * kNStage * sizeof(uint64_t) + kNStage * sizeof(int) +
+    return decode_ring_bytes<D, G, ET>() + 2 * kNStage * sizeof(uint64_t) + kNStage * sizeof(int) +
            (size_t)kNW * kBS * G * sizeof(float2) + (size_t)kNW * G * sizeof(float) +
            (size_t)(LINEAR ? 0 : part_blocks) * sizeof(int32_t);
 }
 
-template <int D, int G, bool BF16, bool LINEAR>
+template <int D, int G, int ET, bool LINEAR>
 static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
-    const size_t smem = decode_smem_bytes<D, G, BF16, LINEAR>(kp.part_blocks);
+    const size_t smem = decode_smem_bytes<D, G, ET, LINEAR>(kp.part_blocks);
     // Large head groups split their heads across the two half-warps (register pressure).
     constexpr int HS = (G >= 8 && D == 128) ? 2 : 1;
-    auto fn = decode_kernel<D, G, HS, BF16, LINEAR>;
+    auto fn = decode_kernel<D, G, HS, ET, LINEAR>;
     if (kv_status st0 = cuda_status(
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
         return st0;
@@ -1384,15 +1421,26 @@ static kv_status launch_t(const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
     return cuda_status(cudaGetLastError());
 }
 
-template <int D, bool BF16, bool LINEAR>
+template <int D, int ET, bool LINEAR>
 static kv_status launch_g(int G, const DecodeKParams &kp, dim3 grid, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_t<D, 1, BF16, LINEAR>(kp, grid, s);
-        case 2: return launch_t<D, 2, BF16, LINEAR>(kp, grid, s);
-        case 4: return launch_t<D, 4, BF16, LINEAR>(kp, grid, s);
-        case 8: return launch_t<D, 8, BF16, LINEAR>(kp, grid, s);
+        case 1: return launch_t<D, 1, ET, LINEAR>(kp, grid, s);
+        case 2: return launch_t<D, 2, ET, LINEAR>(kp, grid, s);
+        case 4: return launch_t<D, 4, ET, LINEAR>(kp, grid, s);
+        case 8: return launch_t<D, 8, ET, LINEAR>(kp, grid, s);
     }
     return KV_ERR_UNSUPPORTED;
+}
+
+// The CUDA-core decode for this element type and addressing.
+template <int D>
+static kv_status launch_cc(kv_dtype dt, bool linear, int G, const DecodeKParams &kp, dim3 grid,
+                           cudaStream_t s) {
+    if (dt == KV_BF16)
+        return linear ? launch_g<D, KV_BF16, true>(G, kp, grid, s) : launch_g<D, KV_BF16, false>(G, kp, grid, s);
+    if (dt == KV_F16)
+        return linear ? launch_g<D, KV_F16, true>(G, kp, grid, s) : launch_g<D, KV_F16, false>(G, kp, grid, s);
+    return linear ? launch_g<D, KV_F32, true>(G, kp, grid, s) : launch_g<D, KV_F32, false>(G, kp, grid, s);
 }
 
 kv_status launch_decode(const DecodeArgs &a, bool linear) {
@@ -1455,7 +1503,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         kp.sched_npieces = a.sched_pieces;
     }
     kp.out = a.out;
-    kp.out_bf16 = a.out_dtype == KV_BF16;
+    kp.out_type = a.out_dtype;
     kp.lse = a.lse;
     kp.ws_o = static_cast<float *>(a.workspace);
     kp.ws_lse = need > 0 ? kp.ws_o + (size_t)a.batch * a.num_q_heads * slots * a.head_dim : nullptr;
@@ -1466,10 +1514,10 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
                                                                                        : nullptr;
     const dim3 grid = a.sched ? dim3(a.sched_ctas, 1, 1) : dim3(ms, a.num_kv_heads, a.batch);
     kv_status st;
-    const bool bf = a.dtype == KV_BF16;
-    // Large head groups on bf16 / d128 go to the tensor-core variant when the
-    // tiled-TMA maps of the K/V storage are available.
-    const bool use_tc = bf && a.head_dim == 128 && g >= kTcMinGroup &&
+    // Large head groups on 16-bit storage (bf16 or fp16) with d128 go to the
+    // tensor-core variant when the tiled-TMA maps of the K/V storage are
+    // available.
+    const bool use_tc = a.dtype != KV_F32 && a.head_dim == 128 && g >= kTcMinGroup &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
     if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
     // a schedule: paged tensor-core path, every merge inside the kernel
@@ -1493,8 +1541,12 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
         CUtensorMap dummy{};
         const CUtensorMap &mk = linear ? dummy : *a.pool_map_k;
         const CUtensorMap &mv = linear ? dummy : *a.pool_map_v;
-        auto fn = test_waits_enabled() ? tc_decode_fn<true>(a.sched != nullptr, deep, linear)
-                                       : tc_decode_fn<false>(a.sched != nullptr, deep, linear);
+        const bool sched = a.sched != nullptr, f16 = a.dtype == KV_F16;
+        auto fn = test_waits_enabled()
+                      ? (f16 ? tc_decode_fn<true, true>(sched, deep, linear)
+                             : tc_decode_fn<true, false>(sched, deep, linear))
+                      : (f16 ? tc_decode_fn<false, true>(sched, deep, linear)
+                             : tc_decode_fn<false, false>(sched, deep, linear));
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return st0;
@@ -1516,15 +1568,9 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
             st = cuda_status(cudaGetLastError());
         }
     } else if (a.head_dim == 128) {
-        st = bf ? (linear ? launch_g<128, true, true>(G, kp, grid, a.stream)
-                          : launch_g<128, true, false>(G, kp, grid, a.stream))
-                : (linear ? launch_g<128, false, true>(G, kp, grid, a.stream)
-                          : launch_g<128, false, false>(G, kp, grid, a.stream));
+        st = launch_cc<128>(a.dtype, linear, G, kp, grid, a.stream);
     } else {
-        st = bf ? (linear ? launch_g<64, true, true>(G, kp, grid, a.stream)
-                          : launch_g<64, true, false>(G, kp, grid, a.stream))
-                : (linear ? launch_g<64, false, true>(G, kp, grid, a.stream)
-                          : launch_g<64, false, false>(G, kp, grid, a.stream));
+        st = launch_cc<64>(a.dtype, linear, G, kp, grid, a.stream);
     }
     if (st != KV_OK || slots <= 1 || a.sched) return st;  // schedules merge inside the kernel
     const int min_splits = kp.counters ? kFuseMaxSplits + 1 : 2;
@@ -1533,7 +1579,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     merge_kernel<<<(rows + 3) / 4, 128, 0, a.stream>>>(
         kp.ws_o, kp.ws_lse, a.seq_lens, linear ? a.mapped_tokens : nullptr, a.req_ids,
         a.max_requests, a.max_blocks * kBS, a.batch, a.num_q_heads, a.head_dim, pb, slots, a.out,
-        kp.out_bf16, a.lse, min_splits, a.start_tokens, a.part_base);
+        kp.out_type, a.lse, min_splits, a.start_tokens, a.part_base);
     return cuda_status(cudaGetLastError());
 }
 
@@ -1843,7 +1889,7 @@ kv_status paged_decode_attention(kv_pool_t p, const void *q, const int32_t *bloc
     a.counters = p->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
-    if (p->dtype == KV_BF16 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
+    if (p->dtype != KV_F32 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
         a.pool_map_k = &p->tmap_k;
         a.pool_map_v = &p->tmap_v;
     }
@@ -1888,7 +1934,7 @@ kv_status paged_append_and_decode(kv_pool_t p, const void *q, const void *k_new,
     a.counters = p->counters;
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
-    if (p->dtype == KV_BF16 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
+    if (p->dtype != KV_F32 && p->head_dim == 128 && pool_tensor_maps(p) == KV_OK) {
         a.pool_map_k = &p->tmap_k;
         a.pool_map_v = &p->tmap_v;
     }
@@ -1927,7 +1973,7 @@ kv_status paged_decode_attention_scheduled(kv_pool_t p, const void *q, const voi
     if (k_new && (!v_new || !slot_mapping)) return KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
         return KV_ERR_ARG;
-    if (p->dtype != KV_BF16 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+    if (p->dtype == KV_F32 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
     if (kv_status st = pool_tensor_maps(p)) return st;
     DecodeArgs a{};
     a.q = q;

@@ -33,7 +33,7 @@ struct kv_pool {
 
 namespace pkv {
 
-inline int dtype_bytes(kv_dtype t) { return t == KV_BF16 ? 2 : 4; }
+inline int dtype_bytes(kv_dtype t) { return t == KV_F32 ? 4 : 2; }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 

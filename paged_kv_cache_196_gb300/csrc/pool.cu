@@ -184,7 +184,7 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
                          kv_dtype dtype, kv_pool_t *out) {
     if (!out || num_blocks <= 0 || num_kv_heads <= 0) return KV_ERR_ARG;
     if (block_size != 16 || (head_dim != 64 && head_dim != 128) ||
-        (dtype != KV_F32 && dtype != KV_BF16))
+        (dtype != KV_F32 && dtype != KV_BF16 && dtype != KV_F16))
         return KV_ERR_UNSUPPORTED;
     kv_pool *p = new (std::nothrow) kv_pool();
     if (!p) return KV_ERR_OOM;

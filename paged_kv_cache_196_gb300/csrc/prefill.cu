@@ -104,7 +104,7 @@ struct PrefillParams {
     int g;
     float scale_log2;
     void *out;
-    int out_bf16;
+    int out_type;  // kv_dtype of out: KV_F32 or the pool's type
     float *lse;
     int *err;
 };
@@ -119,7 +119,7 @@ struct PfBars {
     int abort;
 };
 
-template <bool TW>
+template <bool TW, bool F16>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -203,7 +203,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // swizzle permutes chunks within a 128-byte row, never across rows).
         uint4 *vt = reinterpret_cast<uint4 *>(sV + s * kPfTileBytes);
         const long long valid = L - (long long)t * kPfBN;  // rows below this hold keys < L
-        if (valid >= kPfBN) {
+        if constexpr (F16) {
+            // an fp16 pool: V is already in the MMA's type; only the rows of
+            // keys at or past L are zeroed
+            if (valid < kPfBN)
+                for (int i = 32 * part + lane; i < 2048; i += 256)
+                    if (((i & 1023) >> 3) >= valid) vt[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else if (valid >= kPfBN) {
 #pragma unroll 8
             for (int i = 32 * part + lane; i < 2048; i += 256) {
                 uint4 u = vt[i];
@@ -320,7 +326,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     } else if (warp == kPfMmaWarp) {
         // ================================================== MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t idesc_qk = F16 ? tc::idesc_f16_f32(128, 128, false, false)
+                                              : tc::idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, false, true);
             const uint32_t q_addr = smem_addr(sQ), k_addr = smem_addr(sK), v_addr = smem_addr(sV);
             auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
@@ -507,17 +514,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc::tmem_ld32(tmem + lane_base + colO(x) + 32 * i, v);
             tc::tmem_wait_ld();
             if (row_valid && ok) {
-                if (p.out_bf16) {
+                if (p.out_type != KV_F32) {  // the pool's 16-bit type
                     uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) + orow + 32 * i);
+                    auto pack = [&](int k2) {
+                        const float lo = __uint_as_float(v[k2]) * inv, hi = __uint_as_float(v[k2 + 1]) * inv;
+                        return F16 ? tc::pack_f16x2(lo, hi) : tc::pack_bf16x2(lo, hi);
+                    };
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 u;
-                        u.x = tc::pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-                        u.y = tc::pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-                        u.z = tc::pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-                        u.w = tc::pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-                        dst[k] = u;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(pack(8 * k), pack(8 * k + 2), pack(8 * k + 4), pack(8 * k + 6));
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + orow + 32 * i);
 #pragma unroll
@@ -553,9 +558,9 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     if (!p || batch < 0 || total_q < 0 || max_q_len < 0 || max_blocks < 0 || num_q_heads <= 0)
         return KV_ERR_ARG;
     if (kv_status st = require_device(p->device)) return st;
-    if (p->dtype != KV_BF16 || p->head_dim != kPfD) return KV_ERR_UNSUPPORTED;
+    if (p->dtype == KV_F32 || p->head_dim != kPfD) return KV_ERR_UNSUPPORTED;
     if (num_q_heads % p->num_kv_heads) return KV_ERR_ARG;
-    if (out_dtype != KV_F32 && out_dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
+    if (out_dtype != KV_F32 && out_dtype != p->dtype) return KV_ERR_UNSUPPORTED;
     if (batch == 0 || max_q_len == 0 || total_q == 0) return KV_OK;
     if (!q || !cu_q || !block_tables || !seq_lens || !out) return KV_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(q) & 15) return KV_ERR_ARG;
@@ -578,10 +583,12 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     pp.g = num_q_heads / p->num_kv_heads;
     pp.scale_log2 = scale * 1.4426950408889634f;
     pp.out = out;
-    pp.out_bf16 = out_dtype == KV_BF16;
+    pp.out_type = out_dtype;
     pp.lse = lse_out;
     pp.err = p->err;
-    auto fn = test_waits_enabled() ? prefill_kernel<true> : prefill_kernel<false>;
+    const bool f16 = p->dtype == KV_F16;
+    auto fn = test_waits_enabled() ? (f16 ? prefill_kernel<true, true> : prefill_kernel<true, false>)
+                                   : (f16 ? prefill_kernel<false, true> : prefill_kernel<false, false>);
     if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
             fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes)))
         return st0;

@@ -1,7 +1,8 @@
 // Tiled-TMA tensor maps (CUtensorMap) for the pools, per-request contiguous
-// regions and prefill queries.  Every map describes bf16 rows of 128 values
-// read as boxes of 16 rows x 64 values with 128-byte swizzle (the layout both
-// the tcgen05 descriptors and the ldmatrix address math expect).
+// regions and prefill queries.  Every map describes rows of 128 16-bit values
+// (bf16 or fp16: the copies move bits, so one data type serves both) read as
+// boxes of 16 rows x 64 values with 128-byte swizzle (the layout both the
+// tcgen05 descriptors and the ldmatrix address math expect).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -57,7 +58,7 @@ bool encode_q_map(CUtensorMap *m, const void *q, int rows, int hq) {
 
 kv_status pool_tensor_maps(kv_pool *p) {
     if (p->tmaps_ready) return KV_OK;
-    if (p->dtype != KV_BF16 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
+    if (p->dtype == KV_F32 || p->head_dim != 128) return KV_ERR_UNSUPPORTED;
     const long long rows = (long long)p->num_blocks * p->num_kv_heads * 16;
     if (rows > INT32_MAX) return KV_ERR_UNSUPPORTED;
     if (!encode_rows_map(&p->tmap_k, p->k, rows) || !encode_rows_map(&p->tmap_v, p->v, rows))

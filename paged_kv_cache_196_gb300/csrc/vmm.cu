@@ -252,7 +252,7 @@ extern "C" {
 kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, int head_dim,
                            kv_dtype dtype, kv_contig_t *out) {
     if (!out || max_requests <= 0 || max_tokens <= 0 || num_kv_heads <= 0) return KV_ERR_ARG;
-    if ((head_dim != 64 && head_dim != 128) || (dtype != KV_F32 && dtype != KV_BF16))
+    if ((head_dim != 64 && head_dim != 128) || (dtype != KV_F32 && dtype != KV_BF16 && dtype != KV_F16))
         return KV_ERR_UNSUPPORTED;
     DriverVmm &d = driver();
     if (!d.ok) return KV_ERR_CUDA;
@@ -305,7 +305,7 @@ kv_status kv_contig_create(int max_requests, int max_tokens, int num_kv_heads, i
         kv_contig_destroy(c);
         return KV_ERR_OOM;
     }
-    if (dtype == KV_BF16 && head_dim == 128 && (long long)num_kv_heads * c->head_stride <= INT32_MAX) {
+    if (dtype != KV_F32 && head_dim == 128 && (long long)num_kv_heads * c->head_stride <= INT32_MAX) {
         if (cudaMalloc(&c->d_maps, sizeof(CUtensorMap) * 2 * max_requests) != cudaSuccess) {
             cudaGetLastError();
             kv_contig_destroy(c);

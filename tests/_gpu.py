@@ -33,9 +33,9 @@ class _Raw:
                                          "data": (ptr, False), "version": 3, "strides": None}
 
 
-def view(ptr: int, shape, bf16: bool) -> torch.Tensor:
+def view(ptr: int, shape, bf16: bool, typestr=None) -> torch.Tensor:
     """A torch tensor aliasing library-owned device memory (no copy)."""
-    return torch.as_tensor(_Raw(ptr, shape, "<i2" if bf16 else "<f4"), device="cuda")
+    return torch.as_tensor(_Raw(ptr, shape, typestr or ("<i2" if bf16 else "<f4")), device="cuda")
 
 
 _cudart = None
