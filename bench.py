@@ -179,14 +179,22 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # Workload set-up (shared by both arms: host arrays only)
 # --------------------------------------------------------------------------
-def decode_workload(name):
+def kv_type(args):
+    """The storage type of the K/V cache (and of q, the new rows and the
+    output): the library's code and the workloads' name for it."""
+    import paged_kv_cache_196_gb300 as pk
+    f16 = getattr(args, "kv_dtype", "bf16") == "f16"
+    return (pk.KV_F16 if f16 else pk.KV_BF16), ("f16" if f16 else "bf16")
+
+
+def decode_workload(name, dtype=None):
     base = name.replace("_contig", "")
     cfg = W.CONFIGS[base]
     lens = W.decode_lengths(base)
     need = int(sum((int(L) + 15) // 16 for L in lens))  # blocks the contexts occupy
     nb = int(math.ceil(cfg["pool_factor"] * need))
     t0 = time.time()
-    inp = W.decode_inputs(base, nb)
+    inp = W.decode_inputs(base, nb, dtype=dtype)
     log(f"[bench] generated {name} inputs in {time.time() - t0:.1f}s "
         f"({nb} blocks, {int(lens.sum())} tokens)")
     max_blocks = (cfg["len_hi"] + 15) // 16
@@ -207,7 +215,8 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as tdist
 
     contig = args.workload.endswith("_contig")
-    cfg, inp, nb, max_blocks = decode_workload(args.workload)
+    KVT, kvt = kv_type(args)
+    cfg, inp, nb, max_blocks = decode_workload(args.workload, kvt)
     lens = inp["lens"]
     B, hq, hkv, d = len(lens), cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     e = 2
@@ -226,7 +235,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- device state: the cache (paged pool or per-request virtual ranges)
     if not contig:
-        pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+        pool = pk.kv_pool_create(nb, 16, hkv, d, KVT)
         if args.launch_overlap:
             pk.kv_pool_set_launch_overlap(pool, True)
         kp, vp = pk.kv_pool_ptrs(pool)
@@ -235,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
         d_tables = torch.from_numpy(tables).cuda()
         slots = tables[np.arange(B), last // 16].astype(np.int64) * 16 + last % 16
     else:
-        ctx = pk.kv_contig_create(B, cfg["len_hi"], hkv, d, pk.KV_BF16)
+        ctx = pk.kv_contig_create(B, cfg["len_hi"], hkv, d, KVT)
         if args.launch_overlap:
             pk.kv_contig_set_launch_overlap(ctx, True)
         t0 = time.time()
@@ -260,8 +269,8 @@ def run_ours(args, rank, world, local_rank):
     d_lens = torch.from_numpy(lens).cuda()
     q = torch.from_numpy(inp["q"].view(np.int16)).cuda()
     g = W.rng(cfg["seed"] + 1000 + rank)
-    k_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
-    v_new = torch.from_numpy(W.normal(g, (B, hkv, d), "bf16").view(np.int16)).cuda()
+    k_new = torch.from_numpy(W.normal(g, (B, hkv, d), kvt).view(np.int16)).cuda()
+    v_new = torch.from_numpy(W.normal(g, (B, hkv, d), kvt).view(np.int16)).cuda()
     out = torch.empty((B, hq, d), dtype=torch.int16, device="cuda")
     # the split plan: from the host-known lengths unless forced on the command line
     splits = args.splits if args.splits > 0 else pk.kv_decode_plan(lens, hkv, max_blocks)
@@ -298,16 +307,16 @@ def run_ours(args, rank, world, local_rank):
 
     def attend():
         if contig:
-            pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, pk.KV_BF16,
+            pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, KVT,
                                        None, splits, ws, ws_bytes)
         elif balanced:
             pk.paged_decode_attention_scheduled(pool, q, d_tables, max_blocks, d_lens, B, hq, scale,
-                                                h_sched, d_sched, out, pk.KV_BF16, None, ws,
+                                                h_sched, d_sched, out, KVT, None, ws,
                                                 ws_bytes, k_new=k_new, v_new=v_new,
                                                 slot_mapping=d_slots)
         else:
             pk.paged_append_and_decode(pool, q, k_new, v_new, d_slots, d_tables, max_blocks, d_lens,
-                                       B, hq, scale, out, pk.KV_BF16, None, splits, ws, ws_bytes,
+                                       B, hq, scale, out, KVT, None, splits, ws, ws_bytes,
                                        seq_order=d_order)
 
     # merge_kernel runs only for plans of more than 32 splits
@@ -489,7 +498,7 @@ def run_ours(args, rank, world, local_rank):
     kname = "decode_tc_kernel" if (hq // hkv >= 3 and d == 128) else "decode_kernel"
     if balanced:
         kname = "decode_tc_sched_kernel"
-    traffic = recorded_traffic(kname, args.workload, src)
+    traffic = recorded_traffic(kname, args.workload + ("_f16" if kvt == "f16" else ""), src)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -501,11 +510,12 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": kvt,
         "data": "synthetic",
         "config": {
             "workload": DESCR[args.workload],
             "name": args.workload,
+            "kv_dtype": kvt,
             "batch": B,
             "tokens": int(lens.sum()),
             "kv_bytes_per_step": kv_bytes,
@@ -670,6 +680,7 @@ def run_prefill(args, rank, world, local_rank):
     import paged_kv_cache_196_gb300 as pk
 
     torch.cuda.set_device(local_rank)
+    KVT, kvt = kv_type(args)
     cfg = W.CONFIGS["yi34b_prefill"]
     B, hq, hkv, d = cfg["batch"], cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     c_len, t_len = cfg["cached_len"], cfg["chunk_len"]
@@ -677,7 +688,7 @@ def run_prefill(args, rank, world, local_rank):
     max_blocks = (L + 15) // 16
     nb = int(math.ceil(cfg["pool_factor"] * B * max_blocks))
     t0 = time.time()
-    inp = W.prefill_inputs("yi34b_prefill", nb)
+    inp = W.prefill_inputs("yi34b_prefill", nb, dtype=kvt)
     log(f"[bench] generated yi34b_prefill inputs in {time.time() - t0:.1f}s")
     lens = np.full(B, L, np.int32)
     alloc = pk.kv_allocator_create(nb)
@@ -691,7 +702,7 @@ def run_prefill(args, rank, world, local_rank):
         slots.append(s[c_len:])
     pk.kv_allocator_destroy(alloc)
     slots = np.concatenate(slots)
-    pool = pk.kv_pool_create(nb, 16, hkv, d, pk.KV_BF16)
+    pool = pk.kv_pool_create(nb, 16, hkv, d, KVT)
     kp, vp = pk.kv_pool_ptrs(pool)
     _fill(kp, torch.from_numpy(inp["pool_k"].view(np.int16)))
     _fill(vp, torch.from_numpy(inp["pool_v"].view(np.int16)))
@@ -713,7 +724,7 @@ def run_prefill(args, rank, world, local_rank):
 
     def attend():
         pk.paged_prefill_attention(pool, q, cu, T, t_len, d_tables, max_blocks, d_lens, B, hq,
-                                   scale, out, pk.KV_BF16, None)
+                                   scale, out, KVT, None)
 
     for _ in range(args.warmup):
         append()
@@ -753,12 +764,12 @@ def run_prefill(args, rank, world, local_rank):
     # of sources and destinations together, more than L2: each launch reads
     # its inputs from HBM and its destination lines are written back.
     R = 4
-    apool = pk.kv_pool_create(R * T // 16, 16, hkv, d, pk.KV_BF16)
+    apool = pk.kv_pool_create(R * T // 16, 16, hkv, d, KVT)
     g_app = W.rng(cfg["seed"] + 2000)
     sets = []
     for r in range(R):
-        ks = torch.from_numpy(W.normal(g_app, (T, hkv, d), "bf16").view(np.int16)).cuda()
-        vs = torch.from_numpy(W.normal(g_app, (T, hkv, d), "bf16").view(np.int16)).cuda()
+        ks = torch.from_numpy(W.normal(g_app, (T, hkv, d), kvt).view(np.int16)).cuda()
+        vs = torch.from_numpy(W.normal(g_app, (T, hkv, d), kvt).view(np.int16)).cuda()
         # chunk r's tokens fill the blocks of region r of the pool, shuffled
         perm = W.permutation(g_app, T // 16).astype(np.int64)
         j = np.arange(T, dtype=np.int64)
@@ -794,12 +805,13 @@ def run_prefill(args, rank, world, local_rank):
     del sets, srcs, dsts
     peak, kind = read_tensor_peak()
     achieved = flops / (attend_ms * 1e-3) / 1e12
+    sfx = "_f16" if kvt == "f16" else ""
     line = {
         "metric": PREFILL_METRIC, "value": round(flops * K / (total_ms * 1e-3) / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": DESCR["yi34b_prefill"], "name": "yi34b_prefill",
+        "vs_baseline": None, "dtype": kvt, "data": "synthetic",
+        "config": {"workload": DESCR["yi34b_prefill"], "name": "yi34b_prefill", "kv_dtype": kvt,
                    "flop_per_step": flops, "append_tokens_per_step": T,
                    "l2": "KV 168 MB + Q 117 MB per step, larger than L2; no flush"},
         "prefill_tokens_per_s": round(T * K / (total_ms * 1e-3), 1),
@@ -815,13 +827,15 @@ def run_prefill(args, rank, world, local_rank):
                    "same_bytes_device_copy_ms": round(copy_ms, 5),
                    "frac_of_same_bytes_copy": round(copy_ms / append_b2b_ms, 4),
                    "kernel": "kv_append (append_kernel)",
-                   "traffic": recorded_traffic("append_kernel", "yi34b_prefill_chunk", source_hash(
+                   "traffic": recorded_traffic("append_kernel", "yi34b_prefill_chunk" + sfx, source_hash(
                        "paged_kv_cache_196_gb300/csrc/pool.cu"))},
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention (prefill_kernel)",
                      "achieved": round(achieved, 2), "peak": peak,
-                     "peak_kind": f"{kind} dense bf16 (cuBLAS burst)", "unit": "TFLOP/s",
+                     "peak_kind": f"{kind} dense bf16 (cuBLAS burst)" + (
+                         "; fp16 has the same nominal dense rate (ratio 1)" if sfx else ""),
+                     "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic("prefill_kernel", "yi34b_prefill", source_hash(
+                     "traffic": recorded_traffic("prefill_kernel", "yi34b_prefill" + sfx, source_hash(
                          "paged_kv_cache_196_gb300/csrc/prefill.cu",
                          "paged_kv_cache_196_gb300/csrc/tc.cuh",
                          "paged_kv_cache_196_gb300/csrc/common.cuh")),
@@ -1144,8 +1158,9 @@ def _summary(line):
 
 def run_extras(args, local_rank):
     """Short runs of the Yi-6B decode (paged, balanced schedule and grid plan;
-    contiguous), the shared-prefix step and the Yi-34B prefill (with its chunk
-    append), one after another in this process, for the headline line."""
+    contiguous), the shared-prefix step, the Yi-34B prefill (with its chunk
+    append), and the Llama-3-8B decode and Yi-34B prefill on fp16 storage,
+    one after another in this process, for the headline line."""
     sub = argparse.Namespace(**vars(args))
     sub.steps = max(20, min(args.steps, 300))
     sub.warmup = max(3, min(args.warmup, 10))
@@ -1154,9 +1169,10 @@ def run_extras(args, local_rank):
     res = {}
     runs = [("yi6b_long_decode", "auto"), ("yi6b_long_decode_grid", "grid"),
             ("yi6b_long_decode_contig", "auto"), ("shared_prefix_step", "auto"),
-            ("yi34b_prefill", "auto")]
+            ("yi34b_prefill", "auto"), ("llama3_8b_decode_f16", "auto"), ("yi34b_prefill_f16", "auto")]
     for key, plan in runs:
-        sub.workload = key.replace("_grid", "")
+        sub.workload = key.replace("_grid", "").replace("_f16", "")
+        sub.kv_dtype = "f16" if key.endswith("_f16") else "bf16"
         sub.plan = plan
         t0 = time.time()
         if sub.workload == "yi34b_prefill":
@@ -1210,6 +1226,9 @@ def main():
                          "(0 = kv_cascade_plan)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "f16"],
+                    help="storage type of the K/V cache, q and the output (decode and prefill "
+                         "workloads); the workloads' inputs are the same draws rounded to it")
     ap.add_argument("--no-extras", action="store_true",
                     help="default workload: skip the short runs of the other workloads that "
                          "the headline line reports under other_workloads")

@@ -416,9 +416,9 @@ kv_status kv_decode_schedule_workspace_size(const int32_t *host_schedule, int nu
  *   schedule       its device copy, 16-byte aligned, all used words;
  *   k_new, v_new, slot_mapping  as paged_append_and_decode, or k_new = NULL
  *                  for no append.
- * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16,
- * head_dim 128, 3..8 query heads per kv head and batch * num_kv_heads <=
- * 65536, else KV_ERR_UNSUPPORTED.  Device lengths that do not match the
+ * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16 or
+ * KV_F16, head_dim 128, 3..8 query heads per kv head and batch *
+ * num_kv_heads <= 65536, else KV_ERR_UNSUPPORTED.  Device lengths that do not match the
  * schedule's (a piece past a sequence's end, or a sequence's last piece
  * stopping short of it) are recorded as KV_ERR_DEVICE_BOUNDS; nothing outside
  * the sequence's table row and the pool is read. */

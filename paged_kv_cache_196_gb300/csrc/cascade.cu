@@ -68,21 +68,6 @@ KV_DEVICE float cs_ex2(float x) {
     return y;
 }
 
-// Named barrier that also returns the OR of a flag over the participating
-// threads, so that they all take the same decision.
-KV_DEVICE bool cs_bar_or(int id, int threads, bool flag) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)flag), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
 KV_DEVICE float cs_max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -421,7 +406,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 }
                 bars->xmax[j & 1][qr][half] = mhalf;
                 // both halves decide together whether to go on (the barrier has no timeout)
-                if (cs_bar_or(pair_bar, 64, bad)) {
+                if (named_bar_or(pair_bar, 64, bad)) {
                     ok = false;
                     *abort_flag = 1;
                     break;
@@ -506,7 +491,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                     for (int k = 0; k < 16; ++k) xo[qr * kCsD + 16 * i + k] = __uint_as_float(v[k]);
                 }
             }
-            const bool okay = !cs_bar_or(pair_bar, 64, !ok);
+            const bool okay = !named_bar_or(pair_bar, 64, !ok);
             if (!okay) *abort_flag = 1;
             if (half == 0) {
                 const float lrow = bars->xsum[qr][0] + bars->xsum[qr][1];

@@ -137,6 +137,21 @@ KV_DEVICE void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also returns the OR of a flag over the participating
+// threads, so that they all take the same decision.
+KV_DEVICE bool named_bar_or(int id, int threads, bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- bf16
 // A 32-bit word holding two bfloat16 values (low half = lower index).
 // Widening bf16 -> fp32 is exact: the bf16 bits are the top half of fp32.

@@ -74,11 +74,13 @@ def test_decode_wait_timeout_is_reported_and_the_next_call_is_correct():
         c.close()
 
 
-def test_scheduled_decode_wait_timeout_then_correct():
-    """The balanced-schedule kernel: consumers and the producer meet on a
-    named barrier at every piece boundary whether or not a wait ran out."""
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 4)])
+def test_scheduled_decode_wait_timeout_then_correct(hq, hkv):
+    """The balanced-schedule kernel (4 and 8 query heads per kv head):
+    consumers and the producer meet on a named barrier at every piece
+    boundary whether or not a wait ran out."""
     require_cuda()
-    c = random_case(_lens(16, 502), hq=32, hkv=8, d=128, dtype="bf16", seed=503)
+    c = random_case(_lens(16, 502), hq=hq, hkv=hkv, d=128, dtype="bf16", seed=503 + hkv)
     try:
         maxb = c.tables.shape[1]
         h_sched = pk.kv_decode_schedule(c.lens, c.hkv, maxb)

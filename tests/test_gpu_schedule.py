@@ -23,11 +23,11 @@ from test_gpu_decode import TOL, _full_decode_case, _sample_items, random_case
 pytestmark = pytest.mark.gpu
 
 
-def _sched_run(case, num_sms, lens_dev=None, expect_err=0, flags=0):
+def _sched_run(case, num_sms, lens_dev=None, expect_err=0, flags=0, ring_stages=0):
     """Scheduled decode of a test_gpu_decode Case (no append)."""
     hq, hkv, d = case.hq, case.hkv, case.d
     maxb = case.tables.shape[1]
-    s = pk.kv_decode_schedule(case.lens, hkv, maxb, num_sms, flags=flags)
+    s = pk.kv_decode_schedule(case.lens, hkv, maxb, num_sms, ring_stages=ring_stages, flags=flags)
     wsb = pk.kv_decode_schedule_workspace_size(s, hq, d)
     ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
     out = torch.empty((case.B, hq, d), dtype=torch.float32, device="cuda")
@@ -42,14 +42,15 @@ def _sched_run(case, num_sms, lens_dev=None, expect_err=0, flags=0):
     return host(out).astype(np.float64), host(lse).astype(np.float64), s
 
 
-@pytest.mark.parametrize("num_sms", [0, 3, 16])
-def test_scheduled_decode_matches_oracle(num_sms):
+@pytest.mark.parametrize("num_sms,hq,hkv", [(0, 32, 8), (3, 32, 8), (16, 32, 8), (3, 24, 8),
+                                             (3, 32, 4), (16, 32, 4)])
+def test_scheduled_decode_matches_oracle(num_sms, hq, hkv):
     """Ragged lengths (one-token, exact-block and block+1 sequences, an empty
     one).  num_sms = 3 packs many pieces into each of few CTAs; 0 plans for
-    the device."""
+    the device.  3, 4 and 8 query heads per kv head."""
     require_cuda()
     lens = [1, 16, 17, 33, 300, 511, 1024, 1025, 2000, 47, 0, 4096, 5]
-    c = random_case(lens, 32, 8, 128, "bf16", seed=700 + num_sms)
+    c = random_case(lens, hq, hkv, 128, "bf16", seed=700 + num_sms + hq + hkv)
     out, lse, s = _sched_run(c, num_sms)
     if num_sms == 3:
         assert s[0] <= 15 and s[1] > 2 * s[0]  # several pieces per CTA
@@ -82,6 +83,20 @@ def test_whole_piece_schedule_matches_oracle(num_sms):
     live = np.isfinite(ref_lse)
     np.testing.assert_allclose(lse[live], ref_lse[live], atol=1e-3)
     assert np.all(out[10] == 0) and np.all(np.isneginf(lse[10]))
+    c.close()
+
+
+def test_wide_schedule_with_long_pieces_matches_oracle():
+    """Four ring stages forced on pieces of several hundred blocks (the wide
+    kernel with table slices of about a thousand entries)."""
+    require_cuda()
+    lens = [9000, 7001, 8192, 5000, 33]
+    c = random_case(lens, 32, 8, 128, "bf16", seed=712)
+    out, lse, s = _sched_run(c, 3, ring_stages=4)
+    assert s[4] == 0 and s[3] >= 300
+    ref, ref_lse = c.oracle()
+    assert_close_scaled(out, ref, TOL["bf16"], "wide schedule, long pieces")
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-3)
     c.close()
 
 

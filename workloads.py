@@ -114,20 +114,23 @@ NAN_F16 = 0x7E01
 NAN_F32 = 0x7FC00001
 
 
-def decode_inputs(name: str, num_blocks: int, seed_offset: int = 0) -> dict:
+def decode_inputs(name: str, num_blocks: int, seed_offset: int = 0, dtype=None) -> dict:
     """Random draws for a paged-decode workload, in a fixed order.
 
     Returns lens [B], perm [num_blocks], pool_k / pool_v [NB][Hkv][16][D], q [B][Hq][D].
     The caller sizes the pool (``num_blocks``) and builds the block tables.
+    ``dtype`` overrides the workload's storage type (the same draws, rounded
+    to that type).
     """
     cfg = CONFIGS[name]
+    dt = dtype or cfg["dtype"]
     g = rng(cfg["seed"] + seed_offset)
     lens = lengths(g, cfg)
     perm = permutation(g, num_blocks)
     shape = (num_blocks, cfg["num_kv_heads"], BLOCK_SIZE, cfg["head_dim"])
-    pool_k = normal(g, shape, cfg["dtype"])
-    pool_v = normal(g, shape, cfg["dtype"])
-    q = normal(g, (len(lens), cfg["num_q_heads"], cfg["head_dim"]), cfg["dtype"])
+    pool_k = normal(g, shape, dt)
+    pool_v = normal(g, shape, dt)
+    q = normal(g, (len(lens), cfg["num_q_heads"], cfg["head_dim"]), dt)
     return dict(lens=lens, perm=perm, pool_k=pool_k, pool_v=pool_v, q=q)
 
 
@@ -170,15 +173,16 @@ def shared_prefix_inputs(name: str = "shared_prefix_step", seed_offset: int = 0,
 
 
 def prefill_inputs(name: str, num_blocks: int, batch=None, cached_len=None, chunk_len=None,
-                   seed_offset: int = 0) -> dict:
+                   seed_offset: int = 0, dtype=None) -> dict:
     """Random draws for the chunked-prefill workload.
 
     Returns cached_lens [B], chunk_lens [B], perm [num_blocks], pool_k / pool_v
     (cached tokens' content; every slot drawn), k_new / v_new [sum T][Hkv][D]
-    and q [sum T][Hq][D].
+    and q [sum T][Hq][D].  ``dtype`` overrides the storage type.
     """
     cfg = dict(CONFIGS[name])
-    for k, v in (("batch", batch), ("cached_len", cached_len), ("chunk_len", chunk_len)):
+    for k, v in (("batch", batch), ("cached_len", cached_len), ("chunk_len", chunk_len),
+                 ("dtype", dtype)):
         if v is not None:
             cfg[k] = v
     g = rng(cfg["seed"] + seed_offset)
