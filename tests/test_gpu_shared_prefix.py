@@ -16,7 +16,7 @@ import torch
 import oracle
 import paged_kv_cache_196_gb300 as pk
 import workloads as W
-from _gpu import assert_close_scaled, dev, host, require_cuda
+from _gpu import assert_close_scaled, dev, host, pool_views, require_cuda
 
 pytestmark = pytest.mark.gpu
 BS = 16
@@ -229,3 +229,55 @@ def test_cascade_groups_of_128_rows():
     assert_close_scaled(out_s, ref, 2e-3, "plain decode, 8 heads per kv head")
     assert_close_scaled(out_c, ref, 2e-3, "cascade decode, 128-row groups")
     np.testing.assert_allclose(lse_c, ref_lse, atol=1e-3)
+
+
+@pytest.mark.parametrize("hq,hkv,B", [(16, 4, 4), (64, 8, 9)])
+def test_cascade_prefix_attends_large_v_values_exactly(hq, hkv, B):
+    """The prefix kernel multiplies bf16 V by the weights in two bf16 parts
+    (hi + lo), so a shared V value of 70000 (beyond fp16's range) is attended
+    as it is, with no value-range flag: every member attends that key (it
+    lies in the shared part), and the saturated dim and the others agree
+    with the oracle at their own scales.  16 rows per group
+    (duplicated-row kernel) and 72 (plain kernel)."""
+    require_cuda()
+    g = W.rng(990 + B)
+    d, P, max_blocks = 128, 64, 8
+    lens = np.array([P + int(x) for x in g.integers(1, 60, size=B)], np.int32)
+    nb = 4 + B * (max_blocks - 4)
+    tables = np.full((B, max_blocks), -1, np.int32)
+    for b in range(B):  # blocks 0-3 shared by all, then each member's own
+        n = -(-int(lens[b]) // BS)
+        tables[b, :4] = np.arange(4)
+        tables[b, 4:n] = 4 + b * (max_blocks - 4) + np.arange(n - 4)
+    pool_k = W.normal(g, (nb, hkv, BS, d), "bf16")
+    pool_v = W.normal(g, (nb, hkv, BS, d), "bf16")
+    q = W.normal(g, (B, hq, d), "bf16")
+    blk, h, off, dim = 1, 0, 5, 3
+    pool_v[blk, h, off, dim] = W.to_bf16_bits(np.array([70000.0], np.float32))[0]
+    pool = pk.kv_pool_create(nb, BS, hkv, d, pk.KV_BF16)
+    try:
+        kv, vv = pool_views(pool, nb, hkv, d, True)
+        kv.copy_(dev(pool_k))
+        vv.copy_(dev(pool_v))
+        group_seqs = np.arange(B, dtype=np.int32).reshape(1, B)
+        shared = np.full(B, P, np.int32)
+        ps = pk.kv_cascade_plan(1, hkv, P // BS, 0)
+        wsc = pk.kv_cascade_workspace_size(B, hq, hkv, d, max_blocks, 0, ps)
+        wc = torch.empty(max(wsc // 4, 1), dtype=torch.float32, device="cuda")
+        out = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
+        pk.paged_decode_attention_cascade(pool, dev(q), dev(tables), max_blocks, dev(lens), B, hq,
+                                          1 / math.sqrt(d), dev(group_seqs), 1, B, dev(shared),
+                                          P // BS, ps, out, pk.KV_F32, None, 0, wc, wsc)
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error(pool) == 0
+        out = host(out).astype(np.float64)
+        ref, _ = oracle.paged_decode(pool_k, pool_v, tables, lens, q, 1 / math.sqrt(d))
+        g_ = hq // hkv
+        rows = slice(h * g_, (h + 1) * g_)   # the query heads of kv head 0
+        other = [x for x in range(d) if x != dim]
+        assert np.max(np.abs(ref[:, rows, dim])) > 500  # the large value dominates that dim
+        assert_close_scaled(out[:, rows, dim], ref[:, rows, dim], 2e-3, "the large dim")
+        assert_close_scaled(out[:, :, other], ref[:, :, other], 2e-3, "the other dims")
+        assert_close_scaled(out[:, g_:, :], ref[:, g_:, :], 2e-3, "the other kv heads")
+    finally:
+        pk.kv_pool_destroy(pool)
