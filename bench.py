@@ -946,9 +946,10 @@ def run_shared_prefix(args, rank, world, local_rank):
     wsc = torch.empty(max(wsc_bytes // 4, 1), dtype=torch.float32, device="cuda")
     d_groups = torch.from_numpy(group_seqs).cuda()
     d_shared = torch.from_numpy(shared).cuda()
-    # the suffix grid takes the sequences with the longest own part first
+    # the suffix grid's order: longest own part first, the one-block suffixes
+    # after the first third (kv_cascade_order)
     s_order = np.zeros(B, np.int32)
-    pk.kv_decode_order(suffix_lens, s_order)
+    pk.kv_cascade_order(suffix_lens, s_order)
     d_sorder = torch.from_numpy(s_order).cuda()
 
     def decode_plain():

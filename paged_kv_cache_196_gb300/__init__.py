@@ -26,7 +26,7 @@ __all__ = [
     "kv_swap_in", "kv_swap_bytes",
     "kv_decode_workspace_size", "kv_decode_split_plan", "kv_decode_plan", "paged_decode_attention",
     "paged_append_and_decode", "kv_decode_order",
-    "paged_decode_attention_noalloc", "kv_cascade_plan", "kv_cascade_workspace_size",
+    "paged_decode_attention_noalloc", "kv_cascade_plan", "kv_cascade_order", "kv_cascade_workspace_size",
     "paged_decode_attention_cascade", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_page_pool", "kv_contig_page_stats", "kv_contig_append", "contig_decode_attention",
@@ -107,6 +107,7 @@ _SIGS = {
     "paged_decode_attention_noalloc": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _vp, _i32, _vp],
     "kv_cascade_plan": [_i32, _i32, _i32, _i32, _P(_i32)],
+    "kv_cascade_order": [_vp, _i32, _vp],
     "kv_cascade_workspace_size": [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _P(_sz)],
     "paged_decode_attention_cascade": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                        _i32, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _vp, _vp,
@@ -514,6 +515,12 @@ def paged_decode_attention_noalloc(p: int, q, block_tables, max_blocks: int, seq
                                                 _ptr(out), out_dtype, _ptr(lse_out), num_splits,
                                                 _stream(stream)),
            "paged_decode_attention_noalloc")
+
+
+def kv_cascade_order(host_suffix_lens, order_out):
+    """host_suffix_lens, order_out: int32 numpy arrays of the batch size (host)."""
+    _check(lib().kv_cascade_order(_ptr(host_suffix_lens), len(host_suffix_lens), _ptr(order_out)),
+           "kv_cascade_order")
 
 
 def kv_cascade_plan(num_groups: int, num_kv_heads: int, max_prefix_blocks: int,

@@ -409,3 +409,25 @@ def test_decode_schedule_arguments():
     # lengths past the table width are clamped to it (the device flags them)
     s = _parse_schedule(pk.kv_decode_schedule(np.array([10**6], np.int32), 1, 64, num_sms=4))
     assert sum(q["n"] for q in s["pieces"]) == 64
+
+
+def test_cascade_order_places_one_block_suffixes_after_the_first_third():
+    """kv_cascade_order: sequences with more than 16 own tokens longest first
+    (ties in batch order), those with at most 16 as one run, longest first,
+    after the first third (rounded) of the others; a permutation of the batch."""
+    g = W.rng(4043)
+    lens = np.concatenate([g.integers(17, 1025, 40), g.integers(1, 17, 25), [16, 17, 0, 17]])
+    lens = g.permutation(lens).astype(np.int32)
+    order = np.zeros(len(lens), np.int32)
+    pk.kv_cascade_order(lens, order)
+    assert sorted(order) == list(range(len(lens)))
+    longs = [b for b in sorted(range(len(lens)), key=lambda b: (-int(lens[b]), b)) if lens[b] > 16]
+    shorts = [b for b in sorted(range(len(lens)), key=lambda b: (-int(lens[b]), b)) if lens[b] <= 16]
+    head = (len(longs) + 1) // 3
+    assert list(order) == longs[:head] + shorts + longs[head:]
+    # all long or all short: plain longest first
+    for sel in (lens[lens > 16], lens[lens <= 16]):
+        o = np.zeros(len(sel), np.int32)
+        pk.kv_cascade_order(sel.astype(np.int32), o)
+        assert list(o) == sorted(range(len(sel)), key=lambda b: (-int(sel[b]), b))
+    pk.kv_cascade_order(np.zeros(0, np.int32), np.zeros(0, np.int32))  # empty batch

@@ -27,7 +27,8 @@ def _append_tokens(pool, k, v, slots):
         pk.kv_append(pool, dev(k), dev(v), dev(np.asarray(slots, np.int64)), len(slots))
 
 
-def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: int = 0):
+def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: int = 0,
+                   order: str = "none"):
     """Builds the cache (shared or private prefixes), runs the step; returns
     (out, lse, tables, refcount checks, cow pair count, cascade out, cascade lse).
     The cascade decode (shared layout only) reads each group's shared blocks
@@ -114,15 +115,18 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: 
         wc = torch.empty(max(wsc // 4, 1), dtype=torch.float32, device="cuda")
         oc = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
         lc = torch.empty((B, hq), dtype=torch.float32, device="cuda")
-        order = None
-        if prefix_splits == 3:  # also the suffix grid in longest-first order
-            order = np.zeros(B, np.int32)
-            pk.kv_decode_order((new_lens - shared).astype(np.int32), order)
-            order = dev(order)
+        # the suffix grid's order: the batch's, longest own part first
+        # (kv_decode_order) or the cascade's order (kv_cascade_order)
+        s_order = None
+        if order != "none":
+            s_order = np.zeros(B, np.int32)
+            (pk.kv_decode_order if order == "decode" else pk.kv_cascade_order)(
+                (new_lens - shared).astype(np.int32), s_order)
+            s_order = dev(s_order)
         pk.paged_decode_attention_cascade(pool, dev(inp["q"]), dev(tables), max_blocks,
                                           dev(new_lens), B, hq, 1 / math.sqrt(d), dev(group_seqs),
                                           groups, G, dev(shared), P // BS, ps, oc, pk.KV_F32, lc, 0,
-                                          wc, wsc, seq_order=order)
+                                          wc, wsc, seq_order=s_order)
         torch.cuda.synchronize()
         assert pk.kv_get_device_error(pool) == 0
         out_c, lse_c = host(oc).astype(np.float64), host(lc).astype(np.float64)
@@ -155,9 +159,10 @@ def oracle_step(inp):
     return oracle.paged_decode(pk_, pv_, tables, new_lens, inp["q"], 1 / math.sqrt(d))
 
 
-def _check(inp, max_blocks, prefix_splits=0):
+def _check(inp, max_blocks, prefix_splits=0, order="none"):
     out_s, lse_s, tab_s, refs, ncow, out_c, lse_c = build_and_step(inp, True, max_blocks, seed=91,
-                                                                   prefix_splits=prefix_splits)
+                                                                   prefix_splits=prefix_splits,
+                                                                   order=order)
     out_p, lse_p, _, _, ncow_p, _, _ = build_and_step(inp, False, max_blocks, seed=92)
     # shared blocks == private copies, bit for bit
     np.testing.assert_array_equal(out_s, out_p)
@@ -200,20 +205,24 @@ def test_shared_prefix_step_two_groups():
     _check(inp, max_blocks=(2048 + 1 + 15) // 16)
 
 
-@pytest.mark.parametrize("prefix_splits", [1, 3, 8])
-def test_cascade_prefix_splits_and_ragged_group(prefix_splits):
+@pytest.mark.parametrize("prefix_splits,order", [(1, "none"), (3, "decode"), (8, "cascade")])
+def test_cascade_prefix_splits_and_ragged_group(prefix_splits, order):
     """Cascade with several key-range partitions of the prefix (8 = one per
-    128-key tile) and a last group with empty member slots (37 = 2 x 16 + 5)."""
+    128-key tile) and a last group with empty member slots (37 = 2 x 16 + 5);
+    the suffix grid in batch order, longest first (kv_decode_order) and in the
+    cascade's order (kv_cascade_order)."""
     require_cuda()
     inp = W.shared_prefix_inputs(batch=37, seed_offset=1)
-    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits)
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits, order=order)
 
 
 @pytest.mark.slow
 def test_shared_prefix_step_full_size():
+    """The benchmark's shared-prefix step at full size, with its suffix order
+    (kv_cascade_order)."""
     require_cuda()
     inp = W.shared_prefix_inputs()
-    _check(inp, max_blocks=(2048 + 1 + 15) // 16)
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16, order="cascade")
 
 
 def test_cascade_groups_of_128_rows():
