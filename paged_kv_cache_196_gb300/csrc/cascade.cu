@@ -812,6 +812,13 @@ kv_status paged_decode_attention_cascade(
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsSmemBytes)))
             return st0;
+        // The whole shared memory as carveout: an SM holding a prefix CTA
+        // (about 164 KiB) then keeps room for a suffix decode CTA beside it
+        // (without, the SM was sized for the prefix CTA alone and the suffix
+        // ran on the 24 other SMs only until the prefix grid ended).
+        if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
+                fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared)))
+            return st0;
         const dim3 grid(ps, p->num_kv_heads, num_groups);
         fn<<<grid, kCsThreads, kCsSmemBytes, s>>>(p->tmap_k, p->tmap_v, cp);
         if (kv_status st1 = cuda_status(cudaGetLastError())) return st1;
