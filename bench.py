@@ -947,7 +947,7 @@ def run_shared_prefix(args, rank, world, local_rank):
     d_groups = torch.from_numpy(group_seqs).cuda()
     d_shared = torch.from_numpy(shared).cuda()
     # the suffix grid's order: longest own part first, the one-block suffixes
-    # after the first third (kv_cascade_order)
+    # after the first 40% (kv_cascade_order)
     s_order = np.zeros(B, np.int32)
     pk.kv_cascade_order(suffix_lens, s_order)
     d_sorder = torch.from_numpy(s_order).cuda()

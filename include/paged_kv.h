@@ -493,10 +493,10 @@ kv_status kv_cascade_plan(int num_groups, int num_kv_heads, int max_prefix_block
  * host_suffix_lens[batch]; order_out: host int32[batch]).  Sequences with more
  * than one block (16 tokens) of their own come longest first (ties in batch
  * order); those with at most one block, whose CTAs are mostly start-up and
- * merge latency, come as one run (longest first) after the first third
+ * merge latency, come as one run (longest first) after the first 40%
  * (rounded) of the others, so that they overlap the long ones' streaming
  * instead of forming the grid's tail.  The pages fix no order; the rule is
- * this library's, measured on GB300 (the shared-prefix step's decode 0.079 ms
+ * this library's, measured on GB300 (the shared-prefix step's decode 0.077 ms
  * against 0.085 ms longest first).  Host only. */
 kv_status kv_cascade_order(const int32_t *host_suffix_lens, int batch, int32_t *order_out);
 kv_status kv_cascade_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,

@@ -684,10 +684,11 @@ kv_status kv_cascade_plan(int num_groups, int num_kv_heads, int max_prefix_block
 // bandwidth.  Run at the end of a longest-first grid, 880 such CTAs (the
 // shared-prefix step: 110 of 256 sequences x 8 kv heads) formed a tail in
 // which HBM idled; at the start they held the SMs the longest sequences need
-// first.  Placed as one run after the first third of the others, they overlap
+// first.  Placed as one run after the first 40% of the others, they overlap
 // the long CTAs' streaming: the step's decode went from 0.0844-0.0848 ms to
-// 0.0789-0.0793 ms on GB300 (after the first 10% / 20% / 45% / 60%: 0.0846,
-// 0.0825, 0.0795, 0.0847 ms).
+// 0.0771-0.0772 ms on GB300 (after the first 20% / 25% / 33% / 36% / 38% /
+// 42% / 44% / 50%: 0.0809, 0.0804, 0.0785, 0.0776, 0.0777-0.0779, 0.0773,
+// 0.0782, 0.0798 ms).
 kv_status kv_cascade_order(const int32_t *host_suffix_lens, int batch, int32_t *order_out) {
     if (batch < 0 || (batch > 0 && (!host_suffix_lens || !order_out))) return KV_ERR_ARG;
     std::vector<int32_t> idx(batch), longs, shorts;
@@ -695,7 +696,7 @@ kv_status kv_cascade_order(const int32_t *host_suffix_lens, int batch, int32_t *
     std::stable_sort(idx.begin(), idx.end(),
                      [&](int32_t x, int32_t y) { return host_suffix_lens[x] > host_suffix_lens[y]; });
     for (int32_t b : idx) (host_suffix_lens[b] > kCsBlockTokens ? longs : shorts).push_back(b);
-    const size_t head = (longs.size() + 1) / 3;  // the first third, rounded
+    const size_t head = (2 * longs.size() + 2) / 5;  // the first 40%, rounded
     size_t o = 0;
     for (size_t i = 0; i < head; ++i) order_out[o++] = longs[i];
     for (int32_t b : shorts) order_out[o++] = b;

@@ -411,10 +411,10 @@ def test_decode_schedule_arguments():
     assert sum(q["n"] for q in s["pieces"]) == 64
 
 
-def test_cascade_order_places_one_block_suffixes_after_the_first_third():
+def test_cascade_order_places_one_block_suffixes_after_the_first_40_percent():
     """kv_cascade_order: sequences with more than 16 own tokens longest first
     (ties in batch order), those with at most 16 as one run, longest first,
-    after the first third (rounded) of the others; a permutation of the batch."""
+    after the first 40% (rounded) of the others; a permutation of the batch."""
     g = W.rng(4043)
     lens = np.concatenate([g.integers(17, 1025, 40), g.integers(1, 17, 25), [16, 17, 0, 17]])
     lens = g.permutation(lens).astype(np.int32)
@@ -423,7 +423,7 @@ def test_cascade_order_places_one_block_suffixes_after_the_first_third():
     assert sorted(order) == list(range(len(lens)))
     longs = [b for b in sorted(range(len(lens)), key=lambda b: (-int(lens[b]), b)) if lens[b] > 16]
     shorts = [b for b in sorted(range(len(lens)), key=lambda b: (-int(lens[b]), b)) if lens[b] <= 16]
-    head = (len(longs) + 1) // 3
+    head = (2 * len(longs) + 2) // 5
     assert list(order) == longs[:head] + shorts + longs[head:]
     # all long or all short: plain longest first
     for sel in (lens[lens > 16], lens[lens <= 16]):
