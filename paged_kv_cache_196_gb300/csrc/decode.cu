@@ -238,6 +238,13 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
                                 int tid, float *w, int *flag, bool release) {
     const int ntot = pre + nsplit;
     constexpr float kLn2 = 0.6931471805599453f;
+    // Cascade, one partition after the prefix: this CTA is the only one left
+    // to contribute once the prefix grid is complete, so it merges its result
+    // with the prefix's partial results itself (no workspace write of its
+    // own, no arrival counter).  Only with fused merges: then no merge kernel
+    // runs afterwards over these rows.
+    const bool direct = pre > 0 && nsplit == 1 && p.counters && ntot <= kFuseMaxSplits;
+    if (direct) asm volatile("griddepcontrol.wait;" ::: "memory");  // the prefix's results are complete
     for (int idx = tid; idx < p.g * D; idx += kNW * 32) {
         const int j = idx / D, d = idx - j * D;
         float M = -INFINITY;
@@ -258,13 +265,31 @@ KV_DEVICE void finish_partition(const DecodeKParams &p, const float *sm_o, const
         if (ntot == 1) {
             store_out(p.out, row * D + d, o, p.out_type);
             if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+        } else if (direct) {
+            // o = (2^(lse2 - Mx) o + sum_s 2^(lse_s - Mx) o_s) / (the same weights' sum)
+            const float *ls = p.ws_lse + row * p.max_splits;
+            const float *os = p.ws_o + row * p.max_splits * D + d;
+            float Mx = lse2;
+            for (int s2 = 0; s2 < pre; ++s2) Mx = fmaxf(Mx, __ldcg(ls + s2));
+            float acc = 0.f, wsum = 0.f;
+            if (Mx != -INFINITY) {
+                wsum = exp2f(lse2 - Mx);
+                acc = wsum * o;
+                for (int s2 = 0; s2 < pre; ++s2) {
+                    const float e = exp2f(__ldcg(ls + s2) - Mx);
+                    acc += e * __ldcg(os + (size_t)s2 * D);
+                    wsum += e;
+                }
+            }
+            store_out(p.out, row * D + d, wsum > 0.f ? acc / wsum : 0.f, p.out_type);
+            if (p.lse && d == 0) p.lse[row] = wsum > 0.f ? (Mx + log2f(wsum)) * kLn2 : -INFINITY;
         } else {
             p.ws_o[(row * p.max_splits + p.part_base + split) * D + d] = o;
             if (d == 0) p.ws_lse[row * p.max_splits + p.part_base + split] = lse2;
         }
     }
     if (release) named_bar_sync(2, kDecodeThreads);
-    if (ntot == 1 || !p.counters || ntot > kFuseMaxSplits) return;
+    if (ntot == 1 || direct || !p.counters || ntot > kFuseMaxSplits) return;
 
     // ---- fused merge by the last-arriving CTA of this (sequence, kv head)
     __threadfence();  // partial results visible device-wide before the arrival

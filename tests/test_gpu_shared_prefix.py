@@ -28,7 +28,7 @@ def _append_tokens(pool, k, v, slots):
 
 
 def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: int = 0,
-                   order: str = "none"):
+                   order: str = "none", suffix_splits: int = 0):
     """Builds the cache (shared or private prefixes), runs the step; returns
     (out, lse, tables, refcount checks, cow pair count, cascade out, cascade lse).
     The cascade decode (shared layout only) reads each group's shared blocks
@@ -111,7 +111,7 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: 
                 k += 1
             shared[b] = k * BS
         ps = pk.kv_cascade_plan(groups, hkv, P // BS, prefix_splits)
-        wsc = pk.kv_cascade_workspace_size(B, hq, hkv, d, max_blocks, 0, ps)
+        wsc = pk.kv_cascade_workspace_size(B, hq, hkv, d, max_blocks, suffix_splits, ps)
         wc = torch.empty(max(wsc // 4, 1), dtype=torch.float32, device="cuda")
         oc = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
         lc = torch.empty((B, hq), dtype=torch.float32, device="cuda")
@@ -125,8 +125,8 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: 
             s_order = dev(s_order)
         pk.paged_decode_attention_cascade(pool, dev(inp["q"]), dev(tables), max_blocks,
                                           dev(new_lens), B, hq, 1 / math.sqrt(d), dev(group_seqs),
-                                          groups, G, dev(shared), P // BS, ps, oc, pk.KV_F32, lc, 0,
-                                          wc, wsc, seq_order=s_order)
+                                          groups, G, dev(shared), P // BS, ps, oc, pk.KV_F32, lc,
+                                          suffix_splits, wc, wsc, seq_order=s_order)
         torch.cuda.synchronize()
         assert pk.kv_get_device_error(pool) == 0
         out_c, lse_c = host(oc).astype(np.float64), host(lc).astype(np.float64)
@@ -159,10 +159,11 @@ def oracle_step(inp):
     return oracle.paged_decode(pk_, pv_, tables, new_lens, inp["q"], 1 / math.sqrt(d))
 
 
-def _check(inp, max_blocks, prefix_splits=0, order="none"):
+def _check(inp, max_blocks, prefix_splits=0, order="none", suffix_splits=0):
     out_s, lse_s, tab_s, refs, ncow, out_c, lse_c = build_and_step(inp, True, max_blocks, seed=91,
                                                                    prefix_splits=prefix_splits,
-                                                                   order=order)
+                                                                   order=order,
+                                                                   suffix_splits=suffix_splits)
     out_p, lse_p, _, _, ncow_p, _, _ = build_and_step(inp, False, max_blocks, seed=92)
     # shared blocks == private copies, bit for bit
     np.testing.assert_array_equal(out_s, out_p)
@@ -205,15 +206,21 @@ def test_shared_prefix_step_two_groups():
     _check(inp, max_blocks=(2048 + 1 + 15) // 16)
 
 
-@pytest.mark.parametrize("prefix_splits,order", [(1, "none"), (3, "decode"), (8, "cascade")])
-def test_cascade_prefix_splits_and_ragged_group(prefix_splits, order):
+@pytest.mark.parametrize("prefix_splits,order,suffix_splits",
+                         [(1, "none", 0), (3, "decode", 0), (8, "cascade", 0), (1, "cascade", 8),
+                          (3, "none", 5)])
+def test_cascade_prefix_splits_and_ragged_group(prefix_splits, order, suffix_splits):
     """Cascade with several key-range partitions of the prefix (8 = one per
     128-key tile) and a last group with empty member slots (37 = 2 x 16 + 5);
     the suffix grid in batch order, longest first (kv_decode_order) and in the
-    cascade's order (kv_cascade_order)."""
+    cascade's order (kv_cascade_order).  With one suffix partition a CTA
+    merges its result with the prefix's directly; with suffix_splits 8 or 5
+    (partitions of 20 or 28 blocks: 129 / splits, rounded up to a multiple of 4) long suffixes
+    have several, merged by the last-arriving CTA through the counters."""
     require_cuda()
     inp = W.shared_prefix_inputs(batch=37, seed_offset=1)
-    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits, order=order)
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits, order=order,
+           suffix_splits=suffix_splits)
 
 
 @pytest.mark.slow
