@@ -247,18 +247,22 @@ def test_cascade_groups_of_128_rows():
     np.testing.assert_allclose(lse_c, ref_lse, atol=1e-3)
 
 
-@pytest.mark.parametrize("hq,hkv,B", [(16, 4, 4), (64, 8, 9)])
+@pytest.mark.parametrize("hq,hkv,B", [(16, 4, 4), (64, 8, 9), (24, 6, 5)])
 def test_cascade_prefix_attends_large_v_values_exactly(hq, hkv, B):
     """The prefix kernel multiplies bf16 V by the weights in two bf16 parts
     (hi + lo), so a shared V value of 70000 (beyond fp16's range) is attended
     as it is, with no value-range flag: every member attends that key (it
     lies in the shared part), and the saturated dim and the others agree
     with the oracle at their own scales.  16 rows per group
-    (duplicated-row kernel) and 72 (plain kernel)."""
+    (duplicated-row kernel) and 72 (plain kernel); 4, 8 and 6 kv heads.
+    Members own 0 to 4 blocks after the shared part: the first none (its
+    result is the prefix's alone), the second one."""
     require_cuda()
     g = W.rng(990 + B)
     d, P, max_blocks = 128, 64, 8
     lens = np.array([P + int(x) for x in g.integers(1, 60, size=B)], np.int32)
+    lens[0] = P  # no own block
+    lens[1] = P + 1 + int(g.integers(0, 16))  # one own block
     nb = 4 + B * (max_blocks - 4)
     tables = np.full((B, max_blocks), -1, np.int32)
     for b in range(B):  # blocks 0-3 shared by all, then each member's own
