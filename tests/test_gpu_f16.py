@@ -263,3 +263,103 @@ def test_f16_contiguous_equals_paged(hq):
         if pool is not None:
             pk.kv_pool_destroy(pool)
         pk.kv_contig_destroy(ctx)
+
+
+def test_f16_llama3_8b_step_full_size():
+    """The benchmark's fp16 Llama-3-8B-shaped step at full size
+    (`bench.py --kv-dtype f16`): paged_append_and_decode with the planner's
+    split count, the grid longest first and launch overlap on.  The pool after
+    the step bit for bit against the oracle's append; sampled (sequence, query
+    head) items against the oracle."""
+    require_cuda()
+    name = "llama3_8b_decode"
+    cfg = W.CONFIGS[name]
+    lens = W.decode_lengths(name)
+    nb = int(math.ceil(cfg["pool_factor"] * sum(oracle.blocks_needed(int(L), 16) for L in lens)))
+    inp = W.decode_inputs(name, nb, dtype="f16")
+    maxb = oracle.blocks_needed(cfg["len_hi"], 16)
+    tables = oracle.build_block_tables(lens, 16, inp["perm"], maxb)
+    B, hq, hkv, d = len(lens), cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    g = W.rng(cfg["seed"] + 1000)
+    k_new = W.normal(g, (B, hkv, d), "f16")
+    v_new = W.normal(g, (B, hkv, d), "f16")
+    last = lens.astype(np.int64) - 1
+    slots = tables[np.arange(B), last // 16].astype(np.int64) * 16 + last % 16
+    order = np.zeros(B, np.int32)
+    pk.kv_decode_order(lens, order)
+    splits = pk.kv_decode_plan(lens, hkv, maxb)
+    scale = 1 / math.sqrt(d)
+    pool, kv, vv = _pool_with(inp["pool_k"], inp["pool_v"])
+    try:
+        pk.kv_pool_set_launch_overlap(pool, True)
+        wsb = pk.kv_decode_workspace_size(B, hq, hkv, d, maxb, splits)
+        ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+        out = torch.empty((B, hq, d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+        pk.paged_append_and_decode(pool, dev(inp["q"]), dev(k_new), dev(v_new), dev(slots),
+                                   dev(tables), maxb, dev(lens), B, hq, scale, out, pk.KV_F32, lse,
+                                   splits, ws, wsb, seq_order=dev(order))
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error(pool) == 0
+        exp_k, exp_v = inp["pool_k"].copy(), inp["pool_v"].copy()
+        oracle.append(exp_k, exp_v, k_new, v_new, slots)
+        np.testing.assert_array_equal(_h(kv).view(np.uint16), exp_k.view(np.uint16))
+        np.testing.assert_array_equal(_h(vv).view(np.uint16), exp_v.view(np.uint16))
+        gi = W.rng(7)
+        items = sorted({(int(b), int(h)) for b, h in zip(gi.integers(0, B, 128), gi.integers(0, hq, 128))})
+        ref, ref_lse = oracle.paged_decode(exp_k, exp_v, tables, lens, inp["q"], scale, items=items)
+        o = _h(out)
+        assert_close_scaled(np.array([o[b, h] for b, h in items]), ref, TOL, "f16 llama3-8b step")
+        np.testing.assert_allclose([_h(lse)[b, h] for b, h in items], ref_lse, atol=1e-3)
+        assert np.all(np.isfinite(o))
+    finally:
+        pk.kv_pool_destroy(pool)
+
+
+@pytest.mark.slow
+def test_f16_yi34b_prefill_full_size_sampled():
+    """The benchmark's fp16 Yi-34B-shaped prefill at full size (4 x (8192
+    cached + 2048 new) tokens, 56 query / 8 kv heads): one complete 256-row
+    slab for every query head, every row of the first query tile, and random
+    items, against the oracle."""
+    require_cuda()
+    cfg = W.CONFIGS["yi34b_prefill"]
+    B, hq, hkv, d = cfg["batch"], cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    c_len, t_len = cfg["cached_len"], cfg["chunk_len"]
+    L = c_len + t_len
+    maxb = oracle.blocks_needed(L, 16)
+    nb = B * maxb
+    inp = W.prefill_inputs("yi34b_prefill", nb, dtype="f16")
+    lens = np.full(B, L, np.int32)
+    tables = oracle.build_block_tables(lens, 16, inp["perm"], maxb)
+    slots = []
+    for b in range(B):
+        pos = np.arange(c_len, L)
+        slots.append(tables[b, pos // 16].astype(np.int64) * 16 + pos % 16)
+    slots = np.concatenate(slots)
+    T = B * t_len
+    cu = np.arange(0, T + 1, t_len, dtype=np.int32)
+    scale = 1 / math.sqrt(d)
+    pool, _, _ = _pool_with(inp["pool_k"], inp["pool_v"])
+    try:
+        pk.kv_append(pool, dev(inp["k_new"]), dev(inp["v_new"]), dev(slots), T)
+        out = torch.empty((T, hq, d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((T, hq), dtype=torch.float32, device="cuda")
+        pk.paged_prefill_attention(pool, dev(inp["q"]), dev(cu), T, t_len, dev(tables), maxb,
+                                   dev(lens), B, hq, scale, out, pk.KV_F32, lse)
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error(pool) == 0
+        ref_k, ref_v = inp["pool_k"].copy(), inp["pool_v"].copy()
+        oracle.append(ref_k, ref_v, inp["k_new"], inp["v_new"], slots)
+        gi = W.rng(8)
+        items = {(int(r), int(h)) for r, h in zip(gi.integers(0, T, 48), gi.integers(0, hq, 48))}
+        items |= {(2 * t_len + t_len - 256 + r, h) for r in range(256) for h in range(hq)}
+        items |= {(r, h) for r in range(128) for h in range(hq)}
+        items = sorted(items)
+        ref, ref_lse = oracle.paged_prefill(ref_k, ref_v, tables, lens, cu, inp["q"], scale,
+                                            items=items)
+        o, l = _h(out), _h(lse)
+        assert_close_scaled(np.array([o[r, h] for r, h in items]), ref, TOL, "f16 yi34b prefill")
+        np.testing.assert_allclose([l[r, h] for r, h in items], ref_lse, atol=1e-3)
+    finally:
+        pk.kv_pool_destroy(pool)
