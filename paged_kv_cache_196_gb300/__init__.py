@@ -170,10 +170,17 @@ def _ptr(x):
     raise TypeError(f"cannot take the address of {type(x)}")
 
 
+_torch = None
+
+
 def _stream(s):
+    """A stream argument as the raw handle: None = torch's current stream."""
+    global _torch
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        if _torch is None:
+            import torch
+            _torch = torch
+        return _torch.cuda.current_stream().cuda_stream
     if isinstance(s, int):
         return s
     return s.cuda_stream
