@@ -224,11 +224,17 @@ kv_status kv_pool_allocator(kv_pool_t p, kv_allocator_t *out);
 
 /* enable = 1: the tensor-core decode launches on this pool (paged decode,
  * the fused decode step, the scheduled decode) may begin while the previous
- * kernel in their stream is still running (a programmatic dependent launch);
- * each waits for that kernel to complete before it reads or writes any
- * memory, so results are unchanged and only the launch latency between
- * back-to-back steps is hidden.  enable = 0 (the default): ordinary launches.
- * Host only; takes effect from the next call. */
+ * kernel in their stream is still running (a programmatic dependent launch).
+ * The grid-indexed paged decode first reads its inputs that a decode step
+ * never writes -- the block tables, seq_lens, seq_order and q -- and then
+ * waits for that kernel to complete before it touches the pool, the
+ * workspace, the outputs or the new rows; the scheduled decode waits before
+ * it reads anything.  So the kernel launched right before such a decode must
+ * not write those four inputs (a decode step does not; a copy in the stream
+ * between the two launches ends the overlap anyway).  Results are unchanged
+ * and the launch latency between back-to-back steps is hidden.  enable = 0
+ * (the default): ordinary launches.  Host only; takes effect from the next
+ * call. */
 kv_status kv_pool_set_launch_overlap(kv_pool_t p, int enable);
 
 /* Block manager calls on the pool's own allocator ("Makale Bulteni --

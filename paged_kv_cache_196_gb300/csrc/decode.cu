@@ -839,7 +839,16 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_k_map,
                      const __grid_constant__ CUtensorMap pool_v_map, const DecodeKParams p) {
     constexpr int G = 8, D = 128;
-    chain_entry(p);
+    // With launch overlap the paged decode reads the inputs a decode step
+    // never writes (block tables, lengths, order, q) before it waits for the
+    // previous kernel, and everything else after: the table slice and q are
+    // on chip when that kernel ends.  The contiguous path waits first (its
+    // request maps and mapped lengths change between calls).
+    if constexpr (LINEAR) {
+        chain_entry(p);
+    } else if (p.chain) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     const int split = blockIdx.x, h = blockIdx.y;
     const int b = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
     if (b < 0 || b >= (int)gridDim.z) {  // not a permutation of the batch
@@ -914,6 +923,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_k) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(map_v) : "memory");
         }
+        if (!LINEAR && p.chain) asm volatile("griddepcontrol.wait;" ::: "memory");  // before the pool reads
         const uint64_t policy = l2_evict_first_policy();
         int issued = 0;
         for (int i = 0; i < nloc; ++i) {
@@ -962,20 +972,6 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     // K row, lane 16 + x chunk x of the V row.
     const bool fuse = p.new_k != nullptr && split == nsplit - 1;
     const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk;
-    if (fuse && warp == (patch ? (nloc - 1) % kNW : 0)) {
-        const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
-        const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
-        newrow[lane] = v;  // kept in shared memory until the last block arrives
-        const long long slot = p.new_slots[b];
-        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
-            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
-            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
-                         row * (D * 2 / 16) + (lane & 15);
-            *dst = v;
-        } else if (slot >= 0 && lane == 0) {
-            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
-        }
-    }
     // Q^T fragments for the 8 k-steps (head g, dims 16kk + 2t (+1) and +8
     // (+9)), staged once in shared memory by warp 0 and read per block: held
     // in registers they cost the 4-stage instantiation spills at its
@@ -989,6 +985,21 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         for (int kk = 0; kk < 8; ++kk)
             s_q[kk * 32 + lane] = make_uint2(live ? __ldg(qrow + 8 * kk + t) : 0u,
                                              live ? __ldg(qrow + 8 * kk + 4 + t) : 0u);
+    }
+    if (!LINEAR && p.chain) asm volatile("griddepcontrol.wait;" ::: "memory");  // before the pool access
+    if (fuse && warp == (patch ? (nloc - 1) % kNW : 0)) {
+        const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
+        const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
+        newrow[lane] = v;  // kept in shared memory until the last block arrives
+        const long long slot = p.new_slots[b];
+        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
+            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
+            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
+                         row * (D * 2 / 16) + (lane & 15);
+            *dst = v;
+        } else if (slot >= 0 && lane == 0) {
+            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+        }
     }
     named_bar_sync(1, kNW * 32);
     // running state for heads 2t, 2t+1 (replicated over g)
