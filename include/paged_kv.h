@@ -521,10 +521,14 @@ kv_status paged_decode_attention_cascade(
  * of which are the new chunk (already appended with kv_append).  Query row
  * r = cu_q[b] + i sits at position (seq_lens[b] - T_b) + i and attends keys
  * 0..(seq_lens[b] - T_b) + i.  QK^T and PV run on the tcgen05 tensor cores
- * (bf16 operands, fp32 accumulation in tensor memory; the softmax weights are
- * rounded to bf16 for the PV product).  Requires pool dtype KV_BF16 and
- * head_dim 128.
- *   q         device [total_q][num_q_heads][head_dim], bf16;
+ * with fp32 accumulation in tensor memory.  QK^T multiplies q by K in the
+ * pool's type.  PV multiplies the softmax weights, rounded to fp16, by V in
+ * fp16; a bf16 pool's V is converted in shared memory, exactly for
+ * magnitudes up to 65280, and larger attended values are handled as
+ * KV_DEVERR_VALUE_RANGE describes.  Requires pool dtype KV_BF16 or KV_F16
+ * and head_dim 128.  The query tiles of a chunk are launched last (heaviest)
+ * first.
+ *   q         device [total_q][num_q_heads][head_dim], the pool's type;
  *   cu_q      device int32[batch + 1], cu_q[0] = 0, non-decreasing, cu_q[batch]
  *             <= total_q;
  *   total_q   host: rows of q and out;
@@ -534,7 +538,12 @@ kv_status paged_decode_attention_cascade(
  *   lse_out   device fp32[total_q][num_q_heads] or NULL.
  * A sequence with seq_lens[b] < T_b, seq_lens[b] > max_blocks*16 or a chunk
  * past total_q is skipped and sets KV_DEVERR_BLOCK_RANGE; so does an
- * out-of-range block id (its keys read as zeros). */
+ * out-of-range block id (its keys read as zeros).  Returns KV_ERR_ARG for a
+ * NULL pointer, a negative size, num_q_heads not a multiple of the pool's kv
+ * heads or q not 16-byte aligned, and KV_ERR_UNSUPPORTED for another pool
+ * type or head_dim, an out_dtype other than KV_F32 or the pool's type,
+ * batch > 65535, max_q_len > 65535 * 256, or a pool of more than 2^31 - 1
+ * (block, kv head, token) rows. */
 kv_status paged_prefill_attention(kv_pool_t p, const void *q, const int32_t *cu_q, int total_q,
                                   int max_q_len, const int32_t *block_tables, int max_blocks,
                                   const int32_t *seq_lens, int batch, int num_q_heads,

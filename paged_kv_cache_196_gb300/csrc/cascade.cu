@@ -289,31 +289,26 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, false, true);
-            const uint32_t q_addr = smem_addr(sQ), k_addr = smem_addr(sK), v_addr = smem_addr(sV);
+            // Each 128-deep product is one block of PTX (two 32-bit adds per
+            // MMA): descriptor low words formed once, offset in 16-byte units;
+            // one high word (stride 1 KiB, 128-byte swizzle) for Q, K and V.
+            const uint32_t d_hi = tc::smem_desc_sw128_hi(1024);
+            const uint32_t q_lo = tc::smem_desc_sw128_lo(smem_addr(sQ), 16);
+            const uint32_t k_lo = tc::smem_desc_sw128_lo(smem_addr(sK), 16);
+            const uint32_t v_lo = tc::smem_desc_sw128_lo(smem_addr(sV), kCsHalfBytes);
             auto issue_s = [&](int j) {  // S(j) = Q K_j^T into S buffer j & 1
-                const uint32_t kb = k_addr + (j & 1) * kCsTileBytes;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t da = tc::smem_desc_sw128(q_addr + hh * kCsHalfBytes + kk * 32, 16, 1024);
-                        const uint64_t db = tc::smem_desc_sw128(kb + hh * kCsHalfBytes + kk * 32, 16, 1024);
-                        tc::mma_ss(tmem + (j & 1) * 128, da, db, idesc_qk, (hh | kk) != 0);
-                    }
+                tc::mma_ss_k128(tmem + (j & 1) * 128, q_lo, k_lo + (((j & 1) * kCsTileBytes) >> 4), d_hi,
+                                idesc_qk, 0, 1);
                 tc::mma_commit(&bars->sfull[j & 1]);
                 tc::mma_commit(&bars->kempty[j & 1]);
             };
-            auto issue_pv = [&](int j) {  // O += P(j) V_j
-                const uint32_t vb = v_addr + (j & 1) * kCsTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // B = V tile, keys 16kk..16kk+15 x 128 dims (MN-major): the two
-                    // 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
-                    const uint64_t db = tc::smem_desc_sw128(vb + kk * 2048, kCsHalfBytes, 1024);
-                    const uint32_t pcol = tmem + (j & 1) * 128 + kk * 8;
-                    tc::mma_ts(tmem + kColO, pcol, db, idesc_pv, (j | kk) != 0);  // P_hi
-                    tc::mma_ts(tmem + kColO, pcol + 64, db, idesc_pv, 1);            // P_lo
-                }
+            auto issue_pv = [&](int j) {  // O += P(j) V_j, P = P_hi + P_lo
+                // B = V tile, 16 keys x 128 dims per step (MN-major): the two
+                // 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
+                const uint32_t vb = v_lo + (((j & 1) * kCsTileBytes) >> 4);
+                const uint32_t pcol = tmem + (j & 1) * 128;
+                tc::mma_ts_k128(tmem + kColO, pcol, vb, d_hi, idesc_pv, j != 0, 1);  // P_hi
+                tc::mma_ts_k128(tmem + kColO, pcol + 64, vb, d_hi, idesc_pv, 1, 1);  // P_lo
                 tc::mma_commit(&bars->vempty[j & 1]);
                 tc::mma_commit(&bars->odone);
             };

@@ -123,7 +123,11 @@ template <bool TW, bool F16>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    const int hq = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+    // A sequence's query tiles are launched last-first: a later tile of a
+    // chunk sees more keys, so the grid's last wave holds light CTAs.  The
+    // sequences stay in order, so the CTAs running at one time share one
+    // sequence's K/V in L2.
+    const int hq = blockIdx.x, qt = gridDim.y - 1 - blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q_begin = p.cu_q[b];
     const int T = p.cu_q[b + 1] - q_begin;
@@ -329,29 +333,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             constexpr uint32_t idesc_qk = F16 ? tc::idesc_f16_f32(128, 128, false, false)
                                               : tc::idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, 128, false, true);
-            const uint32_t q_addr = smem_addr(sQ), k_addr = smem_addr(sK), v_addr = smem_addr(sV);
+            // One thread issues every MMA while two softmax warps share its
+            // SM sub-partition, so each 128-deep product is one block of PTX
+            // whose MMAs cost two 32-bit adds each: the descriptors' low words
+            // (start address, leading offset) are formed once and offset in
+            // 16-byte units (shared-memory addresses stay below 2^18, so the
+            // 14-bit address field never carries); the high word (stride
+            // offset 1 KiB, format version, 128-byte swizzle) is the same for
+            // Q, K and V.
+            const uint32_t d_hi = tc::smem_desc_sw128_hi(1024);
+            const uint32_t q_lo = tc::smem_desc_sw128_lo(smem_addr(sQ), 16);
+            const uint32_t k_lo = tc::smem_desc_sw128_lo(smem_addr(sK), 16);
+            const uint32_t v_lo = tc::smem_desc_sw128_lo(smem_addr(sV), kPfHalfBytes);
             auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
-                const uint32_t kb = k_addr + (j & 1) * kPfTileBytes;
-                const uint32_t qb = q_addr + x * kPfTileBytes;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t da = tc::smem_desc_sw128(qb + hh * kPfHalfBytes + kk * 32, 16, 1024);
-                        const uint64_t db = tc::smem_desc_sw128(kb + hh * kPfHalfBytes + kk * 32, 16, 1024);
-                        tc::mma_ss(tmem + colS(x), da, db, idesc_qk, (hh | kk) != 0);
-                    }
+                tc::mma_ss_k128(tmem + colS(x), q_lo + ((x * kPfTileBytes) >> 4),
+                                k_lo + (((j & 1) * kPfTileBytes) >> 4), d_hi, idesc_qk, 0, 1);
                 tc::mma_commit(&bars->sfull[x]);
             };
             auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j
-                const uint32_t vb = v_addr + (j % kPfVStages) * kPfTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // B = V tile, keys 16kk..16kk+15 x all 128 dims (MN-major):
-                    // the two 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
-                    const uint64_t db = tc::smem_desc_sw128(vb + kk * 2048, kPfHalfBytes, 1024);
-                    tc::mma_ts(tmem + colO(x), tmem + colS(x) + kk * 8, db, idesc_pv, (j | kk) != 0);
-                }
+                // B = V tile, 16 keys x all 128 dims per step (MN-major): the two
+                // 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
+                tc::mma_ts_k128(tmem + colO(x), tmem + colS(x), v_lo + (((j % kPfVStages) * kPfTileBytes) >> 4),
+                                d_hi, idesc_pv, j != 0, 1);
             };
             bool ok = mbar_wait<TW>(&bars->qfull, 0, p.err) && mbar_wait<TW>(&bars->kfull[0], 0, p.err);
             if (ok) {
@@ -592,7 +595,9 @@ extern "C" kv_status paged_prefill_attention(kv_pool_t p, const void *q, const i
     if (kv_status st0 = cuda_status(cudaFuncSetAttribute(
             fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes)))
         return st0;
-    const dim3 grid(num_q_heads, (max_q_len + kPfBM - 1) / kPfBM, batch);
+    const int q_tiles = (max_q_len + kPfBM - 1) / kPfBM;
+    if (q_tiles > 65535) return KV_ERR_UNSUPPORTED;
+    const dim3 grid(num_q_heads, q_tiles, batch);
     fn<<<grid, kPfThreads, kPfSmemBytes, as_stream(stream)>>>(tm_q, p->tmap_k,
                                                                          p->tmap_v, pp);
     return cuda_status(cudaGetLastError());
