@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             const uint32_t v_lo = tc::smem_desc_sw128_lo(smem_addr(sV), kCsHalfBytes);
             auto issue_s = [&](int j) {  // S(j) = Q K_j^T into S buffer j & 1
                 tc::mma_ss_k128(tmem + (j & 1) * 128, q_lo, k_lo + (((j & 1) * kCsTileBytes) >> 4), d_hi,
-                                idesc_qk, 0, 1);
+                                idesc_qk, 0);
                 tc::mma_commit(&bars->sfull[j & 1]);
                 tc::mma_commit(&bars->kempty[j & 1]);
             };
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 // 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
                 const uint32_t vb = v_lo + (((j & 1) * kCsTileBytes) >> 4);
                 const uint32_t pcol = tmem + (j & 1) * 128;
-                tc::mma_ts_k128(tmem + kColO, pcol, vb, d_hi, idesc_pv, j != 0, 1);  // P_hi
-                tc::mma_ts_k128(tmem + kColO, pcol + 64, vb, d_hi, idesc_pv, 1, 1);  // P_lo
+                tc::mma_ts_k128(tmem + kColO, pcol, vb, d_hi, idesc_pv, j != 0);  // P_hi
+                tc::mma_ts_k128(tmem + kColO, pcol + 64, vb, d_hi, idesc_pv, 1);  // P_lo
                 tc::mma_commit(&bars->vempty[j & 1]);
                 tc::mma_commit(&bars->odone);
             };

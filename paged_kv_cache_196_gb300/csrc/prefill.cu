@@ -347,14 +347,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint32_t v_lo = tc::smem_desc_sw128_lo(smem_addr(sV), kPfHalfBytes);
             auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
                 tc::mma_ss_k128(tmem + colS(x), q_lo + ((x * kPfTileBytes) >> 4),
-                                k_lo + (((j & 1) * kPfTileBytes) >> 4), d_hi, idesc_qk, 0, 1);
+                                k_lo + (((j & 1) * kPfTileBytes) >> 4), d_hi, idesc_qk, 0);
                 tc::mma_commit(&bars->sfull[x]);
             };
             auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j
                 // B = V tile, 16 keys x all 128 dims per step (MN-major): the two
                 // 64-dim halves are 16 KiB apart, 8-key groups 1 KiB apart.
                 tc::mma_ts_k128(tmem + colO(x), tmem + colS(x), v_lo + (((j % kPfVStages) * kPfTileBytes) >> 4),
-                                d_hi, idesc_pv, j != 0, 1);
+                                d_hi, idesc_pv, j != 0);
             };
             bool ok = mbar_wait<TW>(&bars->qfull, 0, p.err) && mbar_wait<TW>(&bars->kfull[0], 0, p.err);
             if (ok) {

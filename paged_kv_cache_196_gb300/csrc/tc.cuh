@@ -117,14 +117,6 @@ __host__ __device__ constexpr uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32
 __host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo) {
     return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
-KV_DEVICE uint64_t desc64(uint32_t lo, uint32_t hi) {
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
-    return d;
-}
-KV_DEVICE uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return desc64(smem_desc_sw128_lo(saddr, lbo), smem_desc_sw128_hi(sbo));
-}
 
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulate.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_major,
@@ -144,93 +136,61 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn_maj
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-KV_DEVICE void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                      uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]
-KV_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                      uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // The eight K16 steps of one 128-deep contraction in one block of PTX, so
 // that an MMA costs its two descriptor adds: D = A B^T (D += with acc_first)
 // with A and B K-major 128-row tiles in shared memory, each two 64-element
 // swizzle atoms 16 KiB apart.  a_lo / b_lo are the tiles' descriptor low
 // words and hi their shared high word (smem_desc_sw128_lo / _hi); step kk of
-// atom hh starts 16384 hh + 32 kk bytes in.  Only a thread with issue != 0
-// issues (a warp may run this converged).
+// atom hh starts 16384 hh + 32 kk bytes in.
 KV_DEVICE void mma_ss_k128(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
-                           uint32_t idesc, uint32_t acc_first, uint32_t issue) {
+                           uint32_t idesc, uint32_t acc_first) {
     asm volatile(
-        "{\n\t.reg .pred l, p, t;\n\t.reg .b32 x, y;\n\t.reg .b64 a, b;\n\t"
-        "setp.ne.u32 l, %6, 0;\n\tsetp.ne.u32 p, %5, 0;\n\tsetp.eq.u32 t, %6, %6;\n\t"
+        "{\n\t.reg .pred p, t;\n\t.reg .b32 x, y;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.u32 p, %5, 0;\n\tsetp.eq.u32 t, %5, %5;\n\t"
         "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t"
         "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 1024;\n\tadd.u32 y, %2, 1024;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 1026;\n\tadd.u32 y, %2, 1026;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 1028;\n\tadd.u32 y, %2, 1028;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
         "add.u32 x, %1, 1030;\n\tadd.u32 y, %2, 1030;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t}" ::"r"(d_tmem),
-        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc_first), "r"(issue)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc_first)
         : "memory");
 }
 // The same with A in tensor memory: D (+)= A B for 128 K values, A at
 // a_tmem (step kk at column offset 8 kk: 16 fp16 values per lane), B an
 // MN-major shared-memory operand whose step kk starts 2048 kk bytes in.
 KV_DEVICE void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
-                           uint32_t idesc, uint32_t acc_first, uint32_t issue) {
+                           uint32_t idesc, uint32_t acc_first) {
     asm volatile(
-        "{\n\t.reg .pred l, p, t;\n\t.reg .b32 x, y;\n\t.reg .b64 b;\n\t"
-        "setp.ne.u32 l, %6, 0;\n\tsetp.ne.u32 p, %5, 0;\n\tsetp.eq.u32 t, %6, %6;\n\t"
+        "{\n\t.reg .pred p, t;\n\t.reg .b32 x, y;\n\t.reg .b64 b;\n\t"
+        "setp.ne.u32 p, %5, 0;\n\tsetp.eq.u32 t, %5, %5;\n\t"
         "mov.b64 b, {%2, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
         "add.u32 x, %1, 8;\n\tadd.u32 y, %2, 128;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 16;\n\tadd.u32 y, %2, 256;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 24;\n\tadd.u32 y, %2, 384;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 32;\n\tadd.u32 y, %2, 512;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 40;\n\tadd.u32 y, %2, 640;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 48;\n\tadd.u32 y, %2, 768;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t"
         "add.u32 x, %1, 56;\n\tadd.u32 y, %2, 896;\n\tmov.b64 b, {y, %3};\n\t"
-        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc_first), "r"(issue)
-        : "memory");
-}
-// mma_commit by the thread with issue != 0 only.
-KV_DEVICE void mma_commit_if(uint64_t *bar, uint32_t issue) {
-    asm volatile(
-        "{\n\t.reg .pred l;\n\tsetp.ne.u32 l, %1, 0;\n\t"
-        "@l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            smem_addr(bar)),
-        "r"(issue)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %4, t;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc_first)
         : "memory");
 }
 // The mbarrier receives one arrival when every tcgen05 operation issued so
