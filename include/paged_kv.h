@@ -30,6 +30,15 @@
  *     for it checks that this device is current; a call made while another
  *     device is current returns KV_ERR_ARG and launches nothing.  The
  *     destroy calls switch to the object's device to free it and switch back.
+ *   - Host buffers.  The per-step arguments of paged_append_and_decode,
+ *     paged_decode_attention_scheduled, kv_contig_append and
+ *     contig_decode_attention (q, k_new, v_new, slot_mapping, positions,
+ *     seq_lens, seq_order, schedule, out, lse_out) may be pinned host memory
+ *     (cudaHostAlloc, cudaHostRegister) instead of device memory: the GPU
+ *     reads and writes it directly over the host link (NVLink-C2C on GB300),
+ *     with the same results as device buffers.  The host must not change
+ *     such a buffer until the call has completed.  Block tables, request ids,
+ *     the pool, the contexts' memory and workspaces are device memory.
  *   - Element types: KV_F32 (IEEE fp32), KV_BF16 (bfloat16) or KV_F16 (IEEE
  *     half precision).  q, k_new and v_new use the pool's type; out may be
  *     KV_F32 or the pool's type.  The cascade decode takes bf16 pools only.
