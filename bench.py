@@ -295,20 +295,14 @@ def run_ours(args, rank, world, local_rank):
             ws_bytes = pk.kv_decode_schedule_workspace_size(h_sched, hq, d)
             ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device="cuda")
             max_splits = int(h_sched[2])
-    else:
-        d_pos = torch.from_numpy(last.astype(np.int32)).cuda()
 
-    # One step: the new tokens' K/V go into their slots, then decode over
-    # all tokens.  Paged: one call (the append fused into the decode kernel);
-    # contiguous: the append, then the decode.
-    def append():
+    # One step: the new tokens' K/V go into their slots (contiguous path:
+    # position seq_lens - 1 of each request), then decode over all tokens, in
+    # one call (the append fused into the decode kernel).
+    def step():
         if contig:
-            pk.kv_contig_append(ctx, k_new, v_new, req_ids, d_pos, B)
-
-    def attend():
-        if contig:
-            pk.contig_decode_attention(ctx, q, req_ids, d_lens, B, hq, scale, out, KVT,
-                                       None, splits, ws, ws_bytes)
+            pk.contig_append_and_decode(ctx, q, k_new, v_new, req_ids, d_lens, B, hq, scale, out,
+                                        KVT, None, splits, ws, ws_bytes)
         elif balanced:
             pk.paged_decode_attention_scheduled(pool, q, d_tables, max_blocks, d_lens, B, hq, scale,
                                                 h_sched, d_sched, out, KVT, None, ws,
@@ -320,12 +314,11 @@ def run_ours(args, rank, world, local_rank):
                                        seq_order=d_order)
 
     # merge_kernel runs only for plans of more than 32 splits
-    launches_per_step = (2 if contig else 1) + (1 if max_splits > 32 else 0)
+    launches_per_step = 1 + (1 if max_splits > 32 else 0)
 
     # ---- warm-up
     for _ in range(args.warmup):
-        append()
-        attend()
+        step()
     torch.cuda.synchronize()
     err = pk.kv_contig_get_device_error(ctx) if contig else pk.kv_get_device_error(pool)
     if err:
@@ -344,8 +337,7 @@ def run_ours(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
     for i in range(K):
-        append()
-        attend()
+        step()
     t_end.record()
     torch.cuda.synchronize()
     if dist:
@@ -358,9 +350,8 @@ def run_ours(args, rank, world, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(Ka)]
     for i in range(Ka):
-        append()
         ev[i][0].record()
-        attend()
+        step()
         ev[i][1].record()
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -383,8 +374,10 @@ def run_ours(args, rank, world, local_rank):
     # Every step is the same decode step (same lengths, same slots), so the
     # slot mapping is planned once, before the loops.
     Ke = min(K, 2000)
-    h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu(),
-               torch.from_numpy(last.astype(np.int32) if contig else slots), torch.from_numpy(lens)]
+    h_parts = [torch.from_numpy(inp["q"].view(np.int16)), k_new.cpu(), v_new.cpu()]
+    if not contig:
+        h_parts.append(torch.from_numpy(slots))
+    h_parts.append(torch.from_numpy(lens))
     if not contig:
         h_parts.append(torch.from_numpy(h_sched if balanced else h_order))
     offs, total = [], 0
@@ -434,17 +427,17 @@ def run_ours(args, rank, world, local_rank):
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def use(views, o):
-        nonlocal q, k_new, v_new, d_pos, d_slots, d_lens, d_sched, d_order, out
+        nonlocal q, k_new, v_new, d_slots, d_lens, d_sched, d_order, out
         q, k_new, v_new = views[0], views[1], views[2]
-        if contig:
-            d_pos = views[3]
-        else:
+        if contig:  # q, k_new, v_new, lengths
+            d_lens = views[3]
+        else:  # q, k_new, v_new, slots, lengths, schedule or order
             d_slots = views[3]
-        d_lens = views[4]
-        if balanced:
-            d_sched = views[5]
-        elif not contig:
-            d_order = views[5]
+            d_lens = views[4]
+            if balanced:
+                d_sched = views[5]
+            else:
+                d_order = views[5]
         out = o
 
     if dist:
@@ -465,8 +458,7 @@ def run_ours(args, rank, world, local_rank):
         s_comp.wait_event(ev_in[bi])
         s_comp.wait_event(ev_out[bi])  # step i - 2's output has been read back
         use(bufs[bi], outs[bi])
-        append()
-        attend()
+        step()
         ev_comp[bi].record(s_comp)
         s_out.wait_event(ev_comp[bi])
         with torch.cuda.stream(s_out):
@@ -514,8 +506,7 @@ def run_ours(args, rank, world, local_rank):
         if z_plans:
             plan(z_plans[zi])
         use(z_views[zi], z_outs[zi])
-        append()
-        attend()
+        step()
         z_done[zi].record(s_comp)
     e1.record(s_comp)
     torch.cuda.synchronize()
@@ -579,10 +570,9 @@ def run_ours(args, rank, world, local_rank):
         "decode_tokens_per_s": round(tokens_per_s, 1),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("contig_decode_attention" if contig else
+            "kernel": ("contig_append_and_decode" if contig else
                        "paged_decode_attention_scheduled" if balanced else "paged_append_and_decode")
-                      + f" ({kname}" + ("" if contig or kname == "decode_kernel" else
-                                         ", the append fused")
+                      + f" ({kname}" + ("" if kname == "decode_kernel" else ", the append fused")
                       + (" + split merge kernel)" if max_splits > 32 else ")"),
             "achieved": round(achieved, 1),
             "peak": peak,

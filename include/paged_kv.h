@@ -31,12 +31,12 @@
  *     device is current returns KV_ERR_ARG and launches nothing.  The
  *     destroy calls switch to the object's device to free it and switch back.
  *   - Host buffers.  The per-step arguments of paged_append_and_decode,
- *     paged_decode_attention_scheduled, kv_contig_append and
- *     contig_decode_attention (q, k_new, v_new, slot_mapping, positions,
- *     seq_lens, seq_order, schedule, out, lse_out) may be pinned host memory
- *     (cudaHostAlloc, cudaHostRegister) instead of device memory: the GPU
- *     reads and writes it directly over the host link (NVLink-C2C on GB300),
- *     with the same results as device buffers.  The host must not change
+ *     paged_decode_attention_scheduled, kv_contig_append,
+ *     contig_decode_attention and contig_append_and_decode (q, k_new, v_new,
+ *     slot_mapping, positions, seq_lens, seq_order, schedule, out, lse_out)
+ *     may be pinned host memory (cudaHostAlloc, cudaHostRegister) instead of
+ *     device memory: the GPU reads and writes it directly over the host link
+ *     (NVLink-C2C on GB300), with the same results as device buffers.  The host must not change
  *     such a buffer until the call has completed.  Block tables, request ids,
  *     the pool, the contexts' memory and workspaces are device memory.
  *   - Element types: KV_F32 (IEEE fp32), KV_BF16 (bfloat16) or KV_F16 (IEEE
@@ -652,12 +652,32 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
                                   int num_splits, void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/* One decode step on the contiguous path: each sequence's new token (device
+ * k_new / v_new [batch][num_kv_heads][head_dim], the context's type) goes to
+ * position seq_lens[b] - 1 of request req_ids[b] (mapped beforehand with
+ * kv_contig_ensure), then contig_decode_attention attends all seq_lens[b]
+ * tokens ("Makale Bulteni -- vAttention", "Iddia ve Gerceklik: vAttention":
+ * the request's KV grows in place at the end of its contiguous range).  Same
+ * results as kv_contig_append at those positions followed by
+ * contig_decode_attention.  One launch where the tensor-core decode applies
+ * (16-bit storage, head_dim 128, 3..8 query heads per kv head): the last
+ * partition of each (sequence, kv head) writes the row and patches it into
+ * its own copy of the last block; otherwise the two calls.  A sequence with
+ * seq_lens[b] = 0 has no new token; one beyond the mapped range sets
+ * KV_DEVERR_UNMAPPED and appends nothing. */
+kv_status contig_append_and_decode(kv_contig_t c, const void *q, const void *k_new,
+                                   const void *v_new, const int32_t *req_ids,
+                                   const int32_t *seq_lens, int batch, int num_q_heads,
+                                   float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                   int num_splits, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
 kv_status kv_contig_get_device_error(kv_contig_t c, int *code, void *stream);
 
 /* As kv_pool_set_launch_overlap for a contiguous context: kv_contig_append and
- * the tensor-core contig_decode_attention may begin while the previous kernel
- * in their stream still runs, and wait for it before touching memory.  Off by
- * default.  Host only. */
+ * the tensor-core contig_decode_attention / contig_append_and_decode may begin
+ * while the previous kernel in their stream still runs, and wait for it before
+ * touching memory.  Off by default.  Host only. */
 kv_status kv_contig_set_launch_overlap(kv_contig_t c, int enable);
 
 /* ======================================================================

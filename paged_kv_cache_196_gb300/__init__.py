@@ -30,7 +30,7 @@ __all__ = [
     "paged_decode_attention_cascade", "paged_prefill_attention", "kv_get_device_error", "kv_contig_create", "kv_contig_destroy",
     "kv_contig_layout", "kv_contig_reserve", "kv_contig_ensure", "kv_contig_release",
     "kv_contig_ptrs", "kv_contig_stats", "kv_contig_page_pool", "kv_contig_page_stats", "kv_contig_append", "contig_decode_attention",
-    "kv_contig_get_device_error", "kv_debug_set_wait_limit_ns", "kv_debug_fail_page_create",
+    "contig_append_and_decode", "kv_contig_get_device_error", "kv_debug_set_wait_limit_ns", "kv_debug_fail_page_create",
     "KV_WAIT_LIMIT_DEFAULT_NS",
 ]
 
@@ -129,6 +129,8 @@ _SIGS = {
     "kv_contig_append": [_vp, _vp, _vp, _vp, _vp, _i32, _vp],
     "contig_decode_attention": [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i32, _vp, _i32, _vp,
                                 _sz, _vp],
+    "contig_append_and_decode": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i32, _vp,
+                                 _i32, _vp, _sz, _vp],
     "kv_contig_get_device_error": [_vp, _P(_i32), _vp],
     "kv_contig_set_launch_overlap": [_vp, _i32],
     "kv_debug_set_wait_limit_ns": [ctypes.c_uint64],
@@ -648,6 +650,20 @@ def contig_decode_attention(c: int, q, req_ids, seq_lens, batch: int, num_q_head
                                          num_splits, _ptr(workspace), workspace_bytes,
                                          _stream(stream)),
            "contig_decode_attention")
+
+
+def contig_append_and_decode(c: int, q, k_new, v_new, req_ids, seq_lens, batch: int,
+                             num_q_heads: int, scale: float, out, out_dtype: int, lse_out=None,
+                             num_splits: int = 0, workspace=None, workspace_bytes: int = 0,
+                             stream=None):
+    """Each sequence's new token at position seq_lens[b] - 1 of its request,
+    then contig_decode_attention (one fused launch where supported).  See the
+    C header."""
+    _check(lib().contig_append_and_decode(c, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_ids),
+                                          _ptr(seq_lens), batch, num_q_heads, scale, _ptr(out),
+                                          out_dtype, _ptr(lse_out), num_splits, _ptr(workspace),
+                                          workspace_bytes, _stream(stream)),
+           "contig_append_and_decode")
 
 
 def kv_contig_set_launch_overlap(c: int, enable: bool):

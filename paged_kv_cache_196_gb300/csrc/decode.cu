@@ -85,7 +85,8 @@ struct DecodeKParams {
     const int32_t *start_tokens;  // cascade: tokens of each sequence attended elsewhere, or null
     int part_base;                // cascade: workspace slots [0, part_base) hold those results
     // fused append (tensor-core decode only): each sequence's new token
-    // ([batch][num_kv_heads][128] bf16) and its pool slot, or null
+    // ([batch][num_kv_heads][128], 16-bit) and its pool slot (paged path; the
+    // contiguous path writes row seq_lens[b] - 1), or null
     const uint4 *new_k;
     const uint4 *new_v;
     const int64_t *new_slots;
@@ -860,16 +861,20 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
 
     long long L = p.seq_lens[b];
     const CUtensorMap *map_k = &pool_k_map, *map_v = &pool_v_map;
+    int req = -1;             // contiguous path: the sequence's request
+    bool len_ok = true;       // L is the sequence's length, not clamped after an error
     if constexpr (LINEAR) {
-        const int req = p.req_ids[b];
+        req = p.req_ids[b];
         if (req < 0 || req >= p.max_requests || p.k_bases[req] == 0) {
             if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
             L = 0;
+            len_ok = false;
         } else {
             const long long mapped = p.mapped_tokens[req];
             if (L > mapped) {
                 if (tid == 0 && split == 0 && h == 0) atomicOr(p.err, KV_DEVERR_UNMAPPED);
                 L = mapped;
+                len_ok = false;
             }
             map_k = p.req_maps + 2 * req;
             map_v = p.req_maps + 2 * req + 1;
@@ -879,6 +884,7 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         if (tid == 0 && split == 0 && h == 0)
             atomicOr(p.err, LINEAR ? KV_DEVERR_UNMAPPED : KV_DEVERR_BLOCK_RANGE);
         L = (long long)p.max_blocks * kBS;
+        len_ok = false;
     }
     if (L < 0) L = 0;
     const int nblk = (int)((L + kBS - 1) / kBS);
@@ -966,12 +972,13 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
     // ---- consumer warps: lane = (g = lane / 4, t = lane % 4)
     const int g = lane >> 2, t = lane & 3;
     // Fused append: the last split of (b, h) writes the new token's K/V row
-    // (head h) to its pool slot and, since the block holding it may have been
-    // copied before that write lands, patches the row into its own copy of
-    // the sequence's last block.  Lane x < 16 carries 16-byte chunk x of the
-    // K row, lane 16 + x chunk x of the V row.
+    // (head h) to its pool slot (contiguous path: row L - 1 of the request's
+    // head region) and, since the block holding it may have been copied
+    // before that write lands, patches the row into its own copy of the
+    // sequence's last block.  Lane x < 16 carries 16-byte chunk x of the K
+    // row, lane 16 + x chunk x of the V row.
     const bool fuse = p.new_k != nullptr && split == nsplit - 1;
-    const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk;
+    const bool patch = fuse && nloc > 0 && blk0 + nloc == nblk && (!LINEAR || len_ok);
     // Q^T fragments for the 8 k-steps (head g, dims 16kk + 2t (+1) and +8
     // (+9)), staged once in shared memory by warp 0 and read per block: held
     // in registers they cost the 4-stage instantiation spills at its
@@ -991,14 +998,24 @@ __global__ void __launch_bounds__(kDecodeThreads, MINB)
         const size_t src = ((size_t)b * p.num_kv_heads + h) * (D * 2 / 16) + (lane & 15);
         const uint4 v = lane < 16 ? __ldg(p.new_k + src) : __ldg(p.new_v + src);
         newrow[lane] = v;  // kept in shared memory until the last block arrives
-        const long long slot = p.new_slots[b];
-        if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
-            const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
-            uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
-                         row * (D * 2 / 16) + (lane & 15);
-            *dst = v;
-        } else if (slot >= 0 && lane == 0) {
-            atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+        if constexpr (LINEAR) {
+            // row L - 1 is mapped (L never exceeds the mapped tokens); after a
+            // clamped length nothing is written
+            if (len_ok && L > 0) {
+                const unsigned long long base = lane < 16 ? p.k_bases[req] : p.v_bases[req];
+                reinterpret_cast<uint4 *>(base)[((long long)h * p.head_stride + (L - 1)) * (D * 2 / 16) +
+                                                (lane & 15)] = v;
+            }
+        } else {
+            const long long slot = p.new_slots[b];
+            if (slot >= 0 && slot < (long long)p.num_blocks * kBS) {
+                const long long row = ((slot / kBS) * p.num_kv_heads + h) * kBS + slot % kBS;
+                uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lane < 16 ? p.k_pool : p.v_pool)) +
+                             row * (D * 2 / 16) + (lane & 15);
+                *dst = v;
+            } else if (slot >= 0 && lane == 0) {
+                atomicOr(p.err, KV_DEVERR_SLOT_RANGE);
+            }
         }
     }
     named_bar_sync(1, kNW * 32);
@@ -1555,7 +1572,7 @@ kv_status launch_decode(const DecodeArgs &a, bool linear) {
     // available.
     const bool use_tc = a.dtype != KV_F32 && a.head_dim == 128 && g >= kTcMinGroup &&
                         (linear ? a.req_maps != nullptr : a.pool_map_k != nullptr);
-    if (a.new_k && (!use_tc || linear)) return KV_ERR_UNSUPPORTED;  // fused append: paged tensor-core path only
+    if (a.new_k && !use_tc) return KV_ERR_UNSUPPORTED;  // fused append: tensor-core kernels only
     // a schedule: paged tensor-core path, every merge inside the kernel
     if (a.sched && (!use_tc || linear || (slots > 1 && !kp.counters))) return KV_ERR_UNSUPPORTED;
     // an overlapping launch: the grid-indexed tensor-core kernel, merges inside it

@@ -122,7 +122,8 @@ struct DecodeArgs {
     const int32_t *start_tokens;
     int part_base;
     // fused append of one new token per sequence (tensor-core decode only):
-    // device [batch][num_kv_heads][head_dim] K and V rows and int64 slots, or null
+    // device [batch][num_kv_heads][head_dim] K and V rows and, on the paged
+    // path, int64 slots (the contiguous path writes row seq_lens[b] - 1), or null
     const void *new_k;
     const void *new_v;
     const int64_t *new_slots;

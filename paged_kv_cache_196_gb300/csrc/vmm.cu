@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(256) contig_append_kernel(
     const unsigned long long *__restrict__ k_bases, const unsigned long long *__restrict__ v_bases,
     const long long *__restrict__ mapped, const uint4 *__restrict__ k_new,
     const uint4 *__restrict__ v_new, const int32_t *__restrict__ req_ids,
-    const int32_t *__restrict__ positions, long long total_chunks, int hkv, int row_chunks,
-    long long head_stride, int max_requests, int *err, int chain) {
+    const int32_t *__restrict__ positions, const int32_t *__restrict__ lens, long long total_chunks,
+    int hkv, int row_chunks, long long head_stride, int max_requests, int *err, int chain) {
     if (chain) {  // an overlapping launch: let the next one begin, wait for the previous
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -86,7 +86,10 @@ __global__ void __launch_bounds__(256) contig_append_kernel(
         const int rem = (int)(i - t * per_token);
         const int h = rem / row_chunks, c = rem - h * row_chunks;
         const int req = __ldg(req_ids + t);
-        const int pos = __ldg(positions + t);
+        // the token's position, or the last position of a sequence of lens[t]
+        // tokens (an empty sequence has no new token)
+        const int pos = positions ? __ldg(positions + t) : __ldg(lens + t) - 1;
+        if (!positions && pos < 0) continue;
         if (req < 0 || req >= max_requests || pos < 0 || (long long)pos >= mapped[req] ||
             k_bases[req] == 0) {
             if (rem == 0) atomicOr(err, KV_DEVERR_UNMAPPED);
@@ -513,15 +516,11 @@ kv_status kv_contig_stats(kv_contig_t c, int req, int64_t *mapped_tokens,
     return KV_OK;
 }
 
-kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
-                           const int32_t *req_ids, const int32_t *positions, int num_tokens,
-                           void *stream) {
-    if (!c || num_tokens < 0) return KV_ERR_ARG;
-    if (kv_status st = require_device(c->device)) return st;
-    if (num_tokens == 0) return KV_OK;
-    if (!k_new || !v_new || !req_ids || !positions) return KV_ERR_ARG;
-    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
-        return KV_ERR_ARG;
+// Writes num_tokens K/V rows into their requests' head regions: token t at
+// positions[t], or (positions null) at lens[t] - 1.
+static kv_status contig_append_rows(kv_contig_t c, const void *k_new, const void *v_new,
+                                    const int32_t *req_ids, const int32_t *positions,
+                                    const int32_t *lens, int num_tokens, void *stream) {
     const int row_chunks = c->head_dim * dtype_bytes(c->dtype) / 16;
     const long long total = (long long)num_tokens * c->hkv * row_chunks;
     long long blocks = (total + 255) / 256;
@@ -540,22 +539,32 @@ kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
         return cuda_status(cudaLaunchKernelEx(
             &cfg, contig_append_kernel, (const unsigned long long *)c->d_kbase,
             (const unsigned long long *)c->d_vbase, (const long long *)c->d_mapped,
-            (const uint4 *)k_new, (const uint4 *)v_new, req_ids, positions, total, c->hkv, row_chunks,
-            c->head_stride, c->max_requests, c->err, 1));
+            (const uint4 *)k_new, (const uint4 *)v_new, req_ids, positions, lens, total, c->hkv,
+            row_chunks, c->head_stride, c->max_requests, c->err, 1));
     }
     contig_append_kernel<<<(int)blocks, 256, 0, as_stream(stream)>>>(
         c->d_kbase, c->d_vbase, c->d_mapped, (const uint4 *)k_new, (const uint4 *)v_new, req_ids,
-        positions, total, c->hkv, row_chunks, c->head_stride, c->max_requests, c->err, 0);
+        positions, lens, total, c->hkv, row_chunks, c->head_stride, c->max_requests, c->err, 0);
     return cuda_status(cudaGetLastError());
 }
 
-kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *req_ids,
-                                  const int32_t *seq_lens, int batch, int num_q_heads,
-                                  float scale, void *out, kv_dtype out_dtype, float *lse_out,
-                                  int num_splits, void *workspace, size_t workspace_bytes,
-                                  void *stream) {
-    if (!c || (batch > 0 && !req_ids)) return KV_ERR_ARG;
+kv_status kv_contig_append(kv_contig_t c, const void *k_new, const void *v_new,
+                           const int32_t *req_ids, const int32_t *positions, int num_tokens,
+                           void *stream) {
+    if (!c || num_tokens < 0) return KV_ERR_ARG;
     if (kv_status st = require_device(c->device)) return st;
+    if (num_tokens == 0) return KV_OK;
+    if (!k_new || !v_new || !req_ids || !positions) return KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+        return KV_ERR_ARG;
+    return contig_append_rows(c, k_new, v_new, req_ids, positions, nullptr, num_tokens, stream);
+}
+
+static DecodeArgs contig_decode_args(kv_contig_t c, const void *q, const int32_t *req_ids,
+                                     const int32_t *seq_lens, int batch, int num_q_heads,
+                                     float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                     int num_splits, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
     DecodeArgs a{};
     a.q = q;
     a.max_blocks = (c->max_tokens + 15) / 16;  // the split plan of an equal-width block table
@@ -584,6 +593,45 @@ kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *r
     a.counter_slots = kv_pool::kCounterSlots;
     a.stream = as_stream(stream);
     a.chain = c->launch_overlap;
+    return a;
+}
+
+kv_status contig_decode_attention(kv_contig_t c, const void *q, const int32_t *req_ids,
+                                  const int32_t *seq_lens, int batch, int num_q_heads,
+                                  float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                  int num_splits, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (!c || (batch > 0 && !req_ids)) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
+    const DecodeArgs a = contig_decode_args(c, q, req_ids, seq_lens, batch, num_q_heads, scale, out,
+                                            out_dtype, lse_out, num_splits, workspace,
+                                            workspace_bytes, stream);
+    return launch_decode(a, true);
+}
+
+kv_status contig_append_and_decode(kv_contig_t c, const void *q, const void *k_new,
+                                   const void *v_new, const int32_t *req_ids,
+                                   const int32_t *seq_lens, int batch, int num_q_heads,
+                                   float scale, void *out, kv_dtype out_dtype, float *lse_out,
+                                   int num_splits, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (!c || batch < 0) return KV_ERR_ARG;
+    if (batch == 0) return KV_OK;
+    if (!req_ids || !seq_lens || !k_new || !v_new) return KV_ERR_ARG;
+    if (kv_status st = require_device(c->device)) return st;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+        return KV_ERR_ARG;
+    DecodeArgs a = contig_decode_args(c, q, req_ids, seq_lens, batch, num_q_heads, scale, out,
+                                      out_dtype, lse_out, num_splits, workspace, workspace_bytes,
+                                      stream);
+    a.new_k = k_new;
+    a.new_v = v_new;
+    const kv_status st = launch_decode(a, true);
+    if (st != KV_ERR_UNSUPPORTED) return st;
+    // shapes the fused kernel does not cover: the append, then the decode
+    if (kv_status st1 = contig_append_rows(c, k_new, v_new, req_ids, nullptr, seq_lens, batch, stream))
+        return st1;
+    a.new_k = a.new_v = nullptr;
     return launch_decode(a, true);
 }
 

@@ -250,3 +250,75 @@ def test_contig_launch_overlap_keeps_step_order():
     ref, ref_lse = oracle.linear_decode(kb, vb, np.arange(B), lens2, q_case, 1 / math.sqrt(d))
     assert_close_scaled(res[1][1], ref, 2e-3, "second contiguous step with launch overlap")
     np.testing.assert_allclose(res[1][3], ref_lse, atol=1e-3)
+
+
+def _contig_step(fused, hq, d, dtype, seed):
+    """One decode step on a ContigCase: a new token per request at position
+    seq_lens - 1 (request 2 takes none: its step length is 0), then a decode
+    of the step lengths.  Returns out, lse, each request's K and V rows after
+    the step, and the logical content the oracle attends."""
+    lens = [35, 17, 0, 300, 777, 64]
+    c = ContigCase(lens, 800, hq=hq, hkv=4, d=d, dtype=dtype, seed=seed)
+    g = W.rng(seed + 1)
+    k_new = W.normal(g, (c.B, c.hkv, c.d), dtype)
+    v_new = W.normal(g, (c.B, c.hkv, c.d), dtype)
+    step = (c.lens + 1).astype(np.int32)
+    step[2] = 0
+    for b, L in enumerate(step):
+        pk.kv_contig_ensure(c.ctx, int(c.req[b]), int(L))
+    out = torch.empty((c.B, c.hq, c.d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((c.B, c.hq), dtype=torch.float32, device="cuda")
+    maxb = -(-c.max_tokens // 16)
+    wsb = pk.kv_decode_workspace_size(c.B, c.hq, c.hkv, c.d, maxb, 0)
+    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    args = (c.B, c.hq, 1 / math.sqrt(c.d), out, pk.KV_F32, lse, 0, ws, wsb)
+    if fused:
+        pk.contig_append_and_decode(c.ctx, dev(c.q), dev(k_new), dev(v_new), dev(c.req), dev(step),
+                                    *args)
+    else:
+        has = np.flatnonzero(step > 0)
+        pk.kv_contig_append(c.ctx, dev(k_new[has]), dev(v_new[has]), dev(c.req[has]),
+                            dev((step[has] - 1).astype(np.int32)), len(has))
+        pk.contig_decode_attention(c.ctx, dev(c.q), dev(c.req), dev(step), *args)
+    torch.cuda.synchronize()
+    assert pk.kv_contig_get_device_error(c.ctx) == 0
+    rows, logical_k, logical_v = [], [], []
+    for b, L in enumerate(step):
+        k_ptr, v_ptr = pk.kv_contig_ptrs(c.ctx, int(c.req[b]))
+        rows.append(read_linear(k_ptr, c.hkv, c.head_stride, int(L), c.d, c.bf16))
+        rows.append(read_linear(v_ptr, c.hkv, c.head_stride, int(L), c.d, c.bf16))
+        kb = c.K[b] if L == 0 else np.concatenate([c.K[b], k_new[b:b + 1]])
+        vb = c.V[b] if L == 0 else np.concatenate([c.V[b], v_new[b:b + 1]])
+        logical_k.append(kb)
+        logical_v.append(vb)
+    res = [host(out), host(lse)] + rows
+    q = c.q
+    c.close()
+    return res, (logical_k, logical_v, step, q)
+
+
+@pytest.mark.parametrize("hq,d,dtype", [(32, 128, "bf16"), (16, 128, "bf16"), (8, 64, "f32")])
+def test_contig_fused_step_equals_append_then_decode(hq, d, dtype):
+    """contig_append_and_decode is one launch on the tensor-core path (8 and 4
+    query heads per kv head) and the two calls for fp32 / d64; either way the
+    output, the log-sum-exp and the requests' rows equal, bit for bit,
+    kv_contig_append at position seq_lens - 1 followed by
+    contig_decode_attention, and the output matches the oracle on the
+    appended content."""
+    require_cuda()
+    a, (lk, lv, step, q) = _contig_step(True, hq, d, dtype, seed=930 + hq + d)
+    b, _ = _contig_step(False, hq, d, dtype, seed=930 + hq + d)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    n = int(step.max())
+    kb, vb = [], []
+    for k, v in zip(lk, lv):
+        kp = np.zeros((4, n, d), k.dtype)
+        vp = np.zeros((4, n, d), v.dtype)
+        kp[:, :len(k)] = k.transpose(1, 0, 2)
+        vp[:, :len(v)] = v.transpose(1, 0, 2)
+        kb.append(kp)
+        vb.append(vp)
+    ref, _ = oracle.linear_decode(kb, vb, np.arange(len(step)), step, q, 1 / math.sqrt(d))
+    assert_close_scaled(a[0], ref, 1e-5 if dtype == "f32" else 2e-3, "fused contiguous step")
+    assert np.all(a[0][2] == 0)  # the request without a token: empty sequence

@@ -96,8 +96,9 @@ def test_paged_step_with_host_buffers_is_bit_identical(scheduled):
     assert np.all(np.isfinite(a[0]))
 
 
-def _contig_step(where, seed):
-    """Append one token per request at position L, then decode L + 1 tokens."""
+def _contig_step(where, seed, fused):
+    """Append one token per request at position L, then decode L + 1 tokens:
+    contig_append_and_decode, or kv_contig_append then contig_decode_attention."""
     lens = [35, 17, 1, 300, 777, 64]
     c = ContigCase(lens, 800, hq=32, hkv=4, d=128, dtype="bf16", seed=seed)
     pk.kv_contig_set_launch_overlap(c.ctx, True)
@@ -114,9 +115,13 @@ def _contig_step(where, seed):
     maxb = -(-c.max_tokens // 16)
     wsb = pk.kv_decode_workspace_size(c.B, c.hq, c.hkv, c.d, maxb, 0)
     ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
-    pk.kv_contig_append(c.ctx, t_k, t_v, t_req, t_pos, c.B)
-    pk.contig_decode_attention(c.ctx, t_q, t_req, t_lens, c.B, c.hq, 1 / math.sqrt(c.d), out,
-                               pk.KV_F32, lse, 0, ws, wsb)
+    if fused:
+        pk.contig_append_and_decode(c.ctx, t_q, t_k, t_v, t_req, t_lens, c.B, c.hq,
+                                    1 / math.sqrt(c.d), out, pk.KV_F32, lse, 0, ws, wsb)
+    else:
+        pk.kv_contig_append(c.ctx, t_k, t_v, t_req, t_pos, c.B)
+        pk.contig_decode_attention(c.ctx, t_q, t_req, t_lens, c.B, c.hq, 1 / math.sqrt(c.d), out,
+                                   pk.KV_F32, lse, 0, ws, wsb)
     torch.cuda.synchronize()
     assert pk.kv_contig_get_device_error(c.ctx) == 0
     rows = []
@@ -129,12 +134,14 @@ def _contig_step(where, seed):
     return res
 
 
-def test_contig_step_with_host_buffers_is_bit_identical():
-    """The contiguous path's append and decode, the step's arguments in
-    pinned host memory, against the same step with device buffers."""
+@pytest.mark.parametrize("fused", [True, False])
+def test_contig_step_with_host_buffers_is_bit_identical(fused):
+    """The contiguous path's step (the fused call, and the append and decode
+    calls), its arguments in pinned host memory, against the same step with
+    device buffers."""
     require_cuda()
-    a = _contig_step("device", 910)
-    b = _contig_step("host", 910)
+    a = _contig_step("device", 910, fused)
+    b = _contig_step("host", 910, fused)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
     assert np.all(np.isfinite(a[0]))
