@@ -41,7 +41,7 @@
  *     the pool, the contexts' memory and workspaces are device memory.
  *   - Element types: KV_F32 (IEEE fp32), KV_BF16 (bfloat16) or KV_F16 (IEEE
  *     half precision).  q, k_new and v_new use the pool's type; out may be
- *     KV_F32 or the pool's type.  The cascade decode takes bf16 pools only.
+ *     KV_F32 or the pool's type.  The cascade decode takes bf16 or fp16 pools.
  *   - head_dim must be 64 or 128, block_size must be 16, num_q_heads must be
  *     a multiple of num_kv_heads with num_q_heads / num_kv_heads <= 8.
  *
@@ -495,9 +495,12 @@ kv_status paged_decode_attention_noalloc(kv_pool_t p, const void *q, const int32
  *   seq_order      device int32[batch] or NULL: the order in which the suffix
  *                  grid takes the sequences (as paged_append_and_decode; e.g.
  *                  kv_cascade_order of the suffix lengths).
- * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16,
- * head_dim 128 and group_size * (num_q_heads / num_kv_heads) <= 128, else
- * KV_ERR_UNSUPPORTED.  Two kernels run in stream order: the prefix kernel
+ * Other arguments as paged_decode_attention.  Requires pool dtype KV_BF16 or
+ * KV_F16, head_dim 128, out_dtype KV_F32 or the pool's type and
+ * group_size * (num_q_heads / num_kv_heads) <= 128, else KV_ERR_UNSUPPORTED.
+ * The prefix kernel multiplies its softmax weights, split into two parts of
+ * the pool's type (about 16 significant bits with bf16, 22 with fp16), by V in
+ * that type.  Two kernels run in stream order: the prefix kernel
  * (tcgen05; rows = a group's sequences x the query heads of one kv head) and
  * the decode kernel over the suffixes, whose split-KV merge also takes the
  * prefix's partial results. */

@@ -23,10 +23,11 @@
 // Prefix kernel, per key tile of 128 keys (8 blocks of 16):
 //   S(j) = Q K_j^T   (tcgen05, M = 128 query rows, N = 128 keys, K = 128 dims)
 //   softmax warps: S -> P, per-row key limit; P is written over S as two
-//                    bf16 parts, P_hi = bf16(P) in columns 0-63 and
-//                    P_lo = bf16(P - P_hi) in columns 64-127, so the weights
-//                    keep about 16 significant bits (a bf16 P alone, 8 bits,
-//                    is off by up to 2^-9 of the largest V on short rows)
+//                    parts of the pool's 16-bit type t, P_hi = t(P) in
+//                    columns 0-63 and P_lo = t(P - P_hi) in columns 64-127,
+//                    so the weights keep about 16 significant bits with bf16
+//                    (a bf16 P alone, 8 bits, is off by up to 2^-9 of the
+//                    largest V on short rows) and about 22 with fp16
 //   O += P_hi V_j + P_lo V_j   (tcgen05, P from tensor memory)
 // Tensor memory: S double-buffered at columns [0,128) and [128,256), O at
 // [256,384).  MMA issue order: S(0), S(1), PV(0), S(2), PV(1), S(3), ...  so
@@ -78,7 +79,7 @@ KV_DEVICE float cs_max3(float a, float b, float c) {
 }
 
 struct CascadeParams {
-    const uint16_t *q;  // [batch][num_q_heads][128] bf16
+    const uint16_t *q;  // [batch][num_q_heads][128], the pool's 16-bit type
     const int32_t *tables;
     int max_blocks;
     int num_blocks;
@@ -136,7 +137,28 @@ KV_DEVICE int prefix_limit(const CascadeParams &p, int b) {
 // which a TMEM lane quadrant would not allow otherwise).  Each writes its P
 // into its own key half of the row and zeros into the other half, so the one
 // PV product yields two partial O rows, added in the epilogue.
-template <bool DUP, bool TW>
+// Two weights (x, y) as the packed 16-bit pair hi = t(x), t(y) of the pool's
+// type t and the packed remainders lo = t(x - hi.x), t(y - hi.y); hi + lo
+// carries about twice t's significant bits.  Widening t to fp32 is exact.
+template <bool F16>
+KV_DEVICE void split_weights(float x, float y, uint32_t &hi, uint32_t &lo) {
+    if constexpr (F16) {
+        hi = tc::pack_f16x2(x, y);
+        float hx, hy;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\t"
+            "cvt.f32.f16 %1, h;\n\t}"
+            : "=f"(hx), "=f"(hy)
+            : "r"(hi));
+        lo = tc::pack_f16x2(x - hx, y - hy);
+    } else {
+        hi = tc::pack_bf16x2(x, y);
+        // the high halves of the packed word, widened
+        const float hx = __uint_as_float(hi << 16), hy = __uint_as_float(hi & 0xffff0000u);
+        lo = tc::pack_bf16x2(x - hx, y - hy);
+    }
+}
+
+template <bool DUP, bool TW, bool F16>
 __global__ void __launch_bounds__(kCsThreads, 1)
     cascade_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const CascadeParams p) {
@@ -287,8 +309,10 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     } else if (warp == kCsMmaWarp) {
         // ================================================== MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, 128, false, true);
+            constexpr uint32_t idesc_qk = F16 ? tc::idesc_f16_f32(128, 128, false, false)
+                                              : tc::idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t idesc_pv = F16 ? tc::idesc_f16_f32(128, 128, false, true)
+                                              : tc::idesc_bf16_f32(128, 128, false, true);
             // Each 128-deep product is one block of PTX (two 32-bit adds per
             // MMA): descriptor low words formed once, offset in 16-byte units;
             // one high word (stride 1 KiB, 128-byte swizzle) for Q, K and V.
@@ -436,9 +460,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                                                      sc2, nm2);
                         const float2 e = make_float2(cs_ex2(xx.x), cs_ex2(xx.y));
                         acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
-                        whi[k] = tc::pack_bf16x2(e.x, e.y);
-                        const float hx = __uint_as_float(whi[k] << 16), hy = __uint_as_float(whi[k] & 0xffff0000u);
-                        wlo[k] = tc::pack_bf16x2(e.x - hx, e.y - hy);
+                        split_weights<F16>(e.x, e.y, whi[k], wlo[k]);
                     }
                     // my keys: P columns 32*half + 16i (hi) and 64 + 32*half + 16i (lo)
                     tc::tmem_st16(scol + 32 * half + 16 * i, whi);
@@ -580,10 +602,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                                                      sc2, nm2);
                         const float2 e = make_float2(cs_ex2(xx.x), cs_ex2(xx.y));
                         acc2[k & 3] = __fadd2_rn(acc2[k & 3], e);
-                        whi[k] = tc::pack_bf16x2(e.x, e.y);
-                        // widening bf16 -> fp32 is exact: the high halves of the packed word
-                        const float hx = __uint_as_float(whi[k] << 16), hy = __uint_as_float(whi[k] & 0xffff0000u);
-                        wlo[k] = tc::pack_bf16x2(e.x - hx, e.y - hy);
+                        split_weights<F16>(e.x, e.y, whi[k], wlo[k]);
                     }
                     tc::tmem_st16(scol + 16 * i, whi);
                     tc::tmem_st16(scol + 64 + 16 * i, wlo);
@@ -721,7 +740,7 @@ kv_status paged_decode_attention_cascade(
         max_prefix_blocks < 0 || prefix_splits < 0 || num_splits < 0)
         return KV_ERR_ARG;
     if (kv_status st = require_device(p->device)) return st;
-    if (p->dtype != KV_BF16 || p->head_dim != kCsD) return KV_ERR_UNSUPPORTED;
+    if ((p->dtype != KV_BF16 && p->dtype != KV_F16) || p->head_dim != kCsD) return KV_ERR_UNSUPPORTED;
     if (num_q_heads % p->num_kv_heads) return KV_ERR_ARG;
     const int g = num_q_heads / p->num_kv_heads;
     if ((long long)group_size * g > kCsRows) return KV_ERR_UNSUPPORTED;
@@ -771,7 +790,7 @@ kv_status paged_decode_attention_cascade(
     split_plan(batch, p->num_kv_heads, max_blocks, num_splits, &pb, &ms);
     const size_t need = decode_workspace_bytes(batch, num_q_heads, kCsD, ps + ms);
     if (!workspace || workspace_bytes < need) return KV_ERR_ARG;
-    if (out_dtype != KV_F32 && out_dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
+    if (out_dtype != KV_F32 && out_dtype != p->dtype) return KV_ERR_UNSUPPORTED;
 
     // prefix first: its partial results must be in place before the suffix's
     // merge reads them.  The suffix decode may overlap it (a programmatic
@@ -802,9 +821,11 @@ kv_status paged_decode_attention_cascade(
         cp.err = p->err;
         // groups of at most 64 rows: duplicated rows, keys split over two threads
         const bool dup = (long long)group_size * g <= 64;
-        auto fn = test_waits_enabled()
-                      ? (dup ? cascade_prefix_kernel<true, true> : cascade_prefix_kernel<false, true>)
-                      : (dup ? cascade_prefix_kernel<true, false> : cascade_prefix_kernel<false, false>);
+        const bool tw = test_waits_enabled(), f16 = p->dtype == KV_F16;
+        auto fn = f16 ? (tw ? (dup ? cascade_prefix_kernel<true, true, true> : cascade_prefix_kernel<false, true, true>)
+                            : (dup ? cascade_prefix_kernel<true, false, true> : cascade_prefix_kernel<false, false, true>))
+                      : (tw ? (dup ? cascade_prefix_kernel<true, true, false> : cascade_prefix_kernel<false, true, false>)
+                            : (dup ? cascade_prefix_kernel<true, false, false> : cascade_prefix_kernel<false, false, false>));
         if (kv_status st0 = cuda_status(
                 cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsSmemBytes)))
             return st0;

@@ -40,7 +40,7 @@ def build_and_step(inp, share: bool, max_blocks: int, seed: int, prefix_splits: 
     hq = inp["q"].shape[1]
     need = sum(-(-(int(L) + 1) // BS) for L in lens)
     nb = int(math.ceil(1.2 * need)) + (B // G + 1) * (P // BS)
-    pool = pk.kv_pool_create(nb, BS, hkv, d, pk.KV_BF16)
+    pool = pk.kv_pool_create(nb, BS, hkv, d, pk.KV_F16 if inp.get("dtype") == "f16" else pk.KV_BF16)
     alloc = pk.kv_pool_allocator(pool)
     pk.kv_allocator_set_order(alloc, W.permutation(W.rng(seed), nb))
     tables = np.full((B, max_blocks), -1, np.int32)
@@ -152,7 +152,8 @@ def oracle_step(inp):
     maxb = max(oracle.blocks_needed(int(L), BS) for L in new_lens)
     nb = sum(oracle.blocks_needed(int(L), BS) for L in new_lens)
     tables = oracle.build_block_tables(new_lens, BS, np.arange(nb, dtype=np.int32), maxb)
-    pk_, pv_ = W.empty_pool(nb, hkv, d, "bf16"), W.empty_pool(nb, hkv, d, "bf16")
+    dt = inp.get("dtype", "bf16")
+    pk_, pv_ = W.empty_pool(nb, hkv, d, dt), W.empty_pool(nb, hkv, d, dt)
     for b in range(B):
         j = np.arange(int(new_lens[b]))
         oracle.append(pk_, pv_, ks[b], vs[b], tables[b, j // BS].astype(np.int64) * BS + j % BS)
@@ -301,3 +302,31 @@ def test_cascade_prefix_attends_large_v_values_exactly(hq, hkv, B):
         assert_close_scaled(out[:, g_:, :], ref[:, g_:, :], 2e-3, "the other kv heads")
     finally:
         pk.kv_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("prefix_splits,order,suffix_splits", [(1, "none", 0), (3, "cascade", 5)])
+def test_cascade_on_fp16_storage(prefix_splits, order, suffix_splits):
+    """The same step on an fp16 pool: the prefix kernel multiplies fp16 Q and
+    K, and fp16 weight parts (P_hi + P_lo) by fp16 V; the suffix runs the fp16
+    decode.  Ragged last group, one and three prefix partitions, one and five
+    suffix partitions; against the oracle on the fp16 content."""
+    require_cuda()
+    inp = W.shared_prefix_inputs(batch=37, seed_offset=5, dtype="f16")
+    _check(inp, max_blocks=(2048 + 1 + 15) // 16, prefix_splits=prefix_splits, order=order,
+           suffix_splits=suffix_splits)
+
+
+def test_cascade_groups_of_128_rows_fp16():
+    """fp16 storage with 128-row groups (16 sequences x 8 query heads per kv
+    head: the kernel's other row layout)."""
+    require_cuda()
+    inp = W.shared_prefix_inputs(batch=20, seed_offset=6, dtype="f16")
+    B, d = len(inp["lens"]), inp["q"].shape[2]
+    inp["q"] = W.normal(W.rng(4343), (B, 64, d), "f16")  # 64 q heads over 8 kv heads
+    out_s, lse_s, _, _, _, out_c, lse_c = build_and_step(inp, True, (2048 + 1 + 15) // 16, seed=94,
+                                                         prefix_splits=2)
+    ref, ref_lse = oracle_step(inp)
+    assert_close_scaled(out_s, ref, 2e-3, "plain decode, fp16, 8 heads per kv head")
+    assert_close_scaled(out_c, ref, 2e-3, "cascade, fp16, 128-row groups")
+    live = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse_c[live], ref_lse[live], atol=1e-3)

@@ -141,18 +141,20 @@ def decode_lengths(name: str, seed_offset: int = 0) -> np.ndarray:
 
 
 def shared_prefix_inputs(name: str = "shared_prefix_step", seed_offset: int = 0,
-                         batch=None) -> dict:
+                         batch=None, dtype=None) -> dict:
     """Logical content of the shared-prefix step.
 
     lens [B] = cached lengths before the step; prefix_k/v [groups][prefix_len][Hkv][D];
     suffix_k/v: list of [max(L - prefix_len, 0)][Hkv][D] per sequence;
     new_k/new_v [B][Hkv][D] (the token appended this step); q [B][Hq][D].
     Sequence b belongs to group b // group_size and its first min(L, prefix_len)
-    tokens are that group's prefix.
+    tokens are that group's prefix.  ``dtype`` overrides the storage type.
     """
     cfg = dict(CONFIGS[name])
     if batch is not None:
         cfg["batch"] = batch
+    if dtype is not None:
+        cfg["dtype"] = dtype
     g = rng(cfg["seed"] + seed_offset)
     lens = lengths(g, cfg)
     B, P, Hkv, D, dt = cfg["batch"], cfg["prefix_len"], cfg["num_kv_heads"], cfg["head_dim"], cfg["dtype"]
@@ -169,7 +171,7 @@ def shared_prefix_inputs(name: str = "shared_prefix_step", seed_offset: int = 0,
     q = normal(g, (B, cfg["num_q_heads"], D), dt)
     return dict(lens=lens, prefix_k=prefix_k, prefix_v=prefix_v, suffix_k=suffix_k,
                 suffix_v=suffix_v, new_k=new_k, new_v=new_v, q=q, group_size=cfg["group_size"],
-                prefix_len=P)
+                prefix_len=P, dtype=dt)
 
 
 def prefill_inputs(name: str, num_blocks: int, batch=None, cached_len=None, chunk_len=None,
