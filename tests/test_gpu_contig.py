@@ -322,3 +322,58 @@ def test_contig_fused_step_equals_append_then_decode(hq, d, dtype):
     ref, _ = oracle.linear_decode(kb, vb, np.arange(len(step)), step, q, 1 / math.sqrt(d))
     assert_close_scaled(a[0], ref, 1e-5 if dtype == "f32" else 2e-3, "fused contiguous step")
     assert np.all(a[0][2] == 0)  # the request without a token: empty sequence
+
+
+KV_DEVERR_UNMAPPED = 0x8  # include/paged_kv.h
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f32")])
+def test_contig_fused_step_past_the_mapped_range_appends_nothing(d, dtype):
+    """Request 0 holds exactly one mapped page of tokens and its step length
+    is one more: the call sets KV_DEVERR_UNMAPPED and writes nothing, so the
+    request's last mapped row keeps its token (on the fused path the clamped
+    length must not patch or write that row); request 1's step is unaffected
+    and matches the oracle.  bf16 / d128 is the fused kernel, fp32 / d64 the
+    append and decode calls."""
+    require_cuda()
+    ctx = pk.kv_contig_create(4, 3 * 8192, 4, d, pk.KV_BF16 if dtype == "bf16" else pk.KV_F32)
+    head_stride, page, _ = pk.kv_contig_layout(ctx)
+    tpp = page // (d * (2 if dtype == "bf16" else 4))  # tokens per page
+    g = W.rng(960 + d)
+    lens = [tpp, 37]
+    K = [W.normal(g, (L, 4, d), dtype) for L in lens]
+    V = [W.normal(g, (L, 4, d), dtype) for L in lens]
+    for r, L in enumerate(lens):
+        pk.kv_contig_reserve(ctx, r)
+        pk.kv_contig_ensure(ctx, r, L)
+        pk.kv_contig_append(ctx, dev(K[r]), dev(V[r]), dev(np.full(L, r, np.int32)),
+                            dev(np.arange(L, dtype=np.int32)), L)
+    pk.kv_contig_ensure(ctx, 1, lens[1] + 1)  # request 0 is not grown
+    torch.cuda.synchronize()
+    assert pk.kv_contig_get_device_error(ctx) == 0
+    q = W.normal(g, (2, 16, d), dtype)
+    k_new = W.normal(g, (2, 4, d), dtype)
+    v_new = W.normal(g, (2, 4, d), dtype)
+    step = np.array([lens[0] + 1, lens[1] + 1], np.int32)
+    out = torch.empty((2, 16, d), dtype=torch.float32, device="cuda")
+    maxb = -(-3 * 8192 // 16)
+    wsb = pk.kv_decode_workspace_size(2, 16, 4, d, maxb, 0)
+    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    pk.contig_append_and_decode(ctx, dev(q), dev(k_new), dev(v_new), dev(np.arange(2, dtype=np.int32)),
+                                dev(step), 2, 16, 1 / math.sqrt(d), out, pk.KV_F32, None, 0, ws, wsb)
+    torch.cuda.synchronize()
+    assert pk.kv_contig_get_device_error(ctx) & KV_DEVERR_UNMAPPED
+    bf = dtype == "bf16"
+    k0, v0 = pk.kv_contig_ptrs(ctx, 0)
+    np.testing.assert_array_equal(read_linear(k0, 4, head_stride, lens[0], d, bf),
+                                  K[0].transpose(1, 0, 2))
+    np.testing.assert_array_equal(read_linear(v0, 4, head_stride, lens[0], d, bf),
+                                  V[0].transpose(1, 0, 2))
+    # request 1: its step, against the oracle on its appended content
+    n = lens[1] + 1
+    kb = np.concatenate([K[1], k_new[1:2]]).transpose(1, 0, 2).copy()
+    vb = np.concatenate([V[1], v_new[1:2]]).transpose(1, 0, 2).copy()
+    ref, _ = oracle.linear_decode([kb], [vb], np.zeros(1, np.int32), np.array([n], np.int32),
+                                  q[1:2], 1 / math.sqrt(d))
+    assert_close_scaled(host(out)[1:2], ref, 1e-5 if dtype == "f32" else 2e-3, "request 1")
+    pk.kv_contig_destroy(ctx)
